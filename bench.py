@@ -1,0 +1,439 @@
+"""MLA decode benchmark (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
+                    [--workload decode_h128_b32_n4096]
+
+A step is one decode step of the whole hot path for every sequence of the batch:
+append the new token's latent row (RoPE on its key), absorb W_UK into the query,
+latent attention over the cache (split-KV runs + log-sum-exp combine), and the
+W_UV up-projection (plus the output gate for the gated workload).  `value` is
+decoded tokens per second over the whole job with inputs resident in HBM; `e2e`
+is the same metric with the step's inputs copied from pinned host memory and the
+result copied back inside the timed region.
+
+Several copies of the latent cache rotate between steps (total well above the
+126 MB L2), so every step reads its cache from HBM.
+
+With --gpus N > 1 (launched by torch.distributed.run) every rank runs an
+independent replica of the workload: the decode path has no cross-sequence
+exchange, so batches are data-parallel (weak scaling, no collective on the data
+path).
+
+`--impl reference` times the float64 CPU oracle on a bounded sample of the same
+workload on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import mla_workloads as W  # noqa: E402
+
+ROTATE = 4  # cache copies rotated between steps
+
+THROTTLE_BITS = {
+    0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+    0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting", 0x10: "sync_boost",
+}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)) or None, "measured"
+    return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks (NVML)
+class ClockSampler:
+    def __init__(self, device_index: int, period_s: float = 0.02):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self._stop = threading.Event()
+        self._period = period_s
+        self._dev = device_index
+        self._ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self._ok = True
+        except Exception:
+            self._ok = False
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self._nv.nvmlDeviceGetClockInfo(self._h, self._nv.NVML_CLOCK_SM))
+                self.reasons |= int(self._nv.nvmlDeviceGetCurrentClocksEventReasons(self._h))
+            except Exception:
+                pass
+            time.sleep(self._period)
+
+    def __enter__(self):
+        if self._ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self._ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"]}
+        names = [n for bit, n in THROTTLE_BITS.items() if self.reasons & bit]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": names,
+                "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- workload
+def workload_bytes_flops(cfg, lens):
+    R = cfg["d_c"] + cfg["d_r"]
+    tokens = int(np.sum(lens))
+    bytes_attn = tokens * R * 2
+    flops_attn = tokens * cfg["H"] * (2 * R + 2 * cfg["d_c"])
+    return bytes_attn, flops_attn
+
+
+class DeviceWorkload:
+    """Resident inputs of one replica: ROTATE latent caches, each with a captured
+    decode-step graph, shared weights and the step's pinned host inputs."""
+
+    def __init__(self, name: str, seed: int, device):
+        import torch
+        import head_latent_attention_29_b300 as mla
+        from head_latent_attention_29_b300.step import DecodeStep
+        self.mla, self.torch = mla, torch
+        cfg = dict(W.WORKLOADS[name])
+        self.cfg, self.name = cfg, name
+        self.lens = W.seq_lens(cfg, seed)
+        B, H, d_c, d_r = cfg["B"], cfg["H"], cfg["d_c"], cfg["d_r"]
+        self.B, self.H = B, H
+        N_max = int(self.lens.max())
+        bf = torch.bfloat16
+        rb = cfg.get("rope_base", 1e4)
+
+        def up(x):
+            return torch.from_numpy(np.ascontiguousarray(W.bf16_bits(x)).view(np.int16)).view(bf).to(device)
+
+        def pin(x):
+            return torch.from_numpy(np.ascontiguousarray(W.bf16_bits(x)).view(np.int16)).view(bf).pin_memory()
+
+        # cache copy 0 is filled from the seeded draws through the library's own
+        # append (RoPE on the key); the other copies are device-side clones
+        c0 = mla.LatentCache(B, N_max, d_c, d_r, dtype=bf, device=device)
+        for b in range(B):
+            n = int(self.lens[b])
+            c, k = W.latent_rows(cfg, seed, b, n)
+            idx = torch.full((n,), b, dtype=torch.int32, device=device)
+            pos = torch.arange(n, dtype=torch.int32, device=device)
+            mla.cache_append(c0, up(c), up(k) if d_r else None, idx, pos, rb)
+        caches = [c0] + [mla.LatentCache(B, N_max, d_c, d_r, dtype=bf, device=device, data=c0.data.clone())
+                         for _ in range(ROTATE - 1)]
+        w_uk, w_uv = W.up_weights(cfg, seed)
+        w_uk, w_uv = up(w_uk), up(w_uv)
+        self.gated = d_r == 0 and "d_model" in cfg
+        w_g = None
+        q_nope, q_r = W.query(cfg, seed)
+        self.host = {"c_kv": pin(W.normal(seed, "step_c_kv", (B, d_c))), "q_nope": pin(q_nope[:, 0])}
+        if d_r:
+            self.host["k_r"] = pin(W.normal(seed, "step_k_r", (B, d_r)))
+            self.host["q_rope"] = pin(q_r[:, 0])
+        if self.gated:
+            h, wg = W.gate_inputs(cfg, seed)
+            self.host["h"] = pin(h)
+            w_g = up(wg)
+        seq_lens = torch.from_numpy(self.lens).to(device)
+        self.steps = [DecodeStep(c, w_uk, w_uv, seq_lens, cfg["scale"], rb, w_g) for c in caches]
+        for st in self.steps:
+            for k, v in self.host.items():
+                st.inputs[k].copy_(v)
+            st.launch()  # one eager run: one-time host setup happens outside capture
+        torch.cuda.synchronize(device)
+        for st in self.steps:
+            st.capture()
+        # end-to-end variant: H2D of the step inputs and D2H of the output inside the graph
+        self.o_host = torch.empty(tuple(self.steps[0].o.shape), dtype=bf).pin_memory()
+        self.e2e = [DecodeStep(c, w_uk, w_uv, seq_lens, cfg["scale"], rb, w_g) for c in caches]
+        for st in self.e2e:
+            st.launch()
+        torch.cuda.synchronize(device)
+        for st in self.e2e:
+            st.capture(self.host, self.o_host)
+        # attention alone, ten launches per graph over the rotating caches
+        self.attn_graph = torch.cuda.CUDAGraph()
+        s0 = self.steps[0]
+        with torch.cuda.graph(self.attn_graph):
+            for i in range(10):
+                st = self.steps[i % ROTATE]
+                mla.decode_attn(st.q_cat, st.cache, seq_lens, cfg["scale"], st.ws, st.o_lat, st.lse)
+        self.kernels_per_step = s0.kernels_per_step
+
+    def step(self, i: int):
+        self.steps[i % ROTATE].replay()
+
+
+def run_b300(args, rank, world, device):
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(device)
+    wl = DeviceWorkload(args.workload, args.seed + rank, device)
+    cfg = wl.cfg
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for i in range(args.warmup):
+        wl.step(i)
+    torch.cuda.synchronize(device)
+
+    # ---- device-resident throughput: K whole steps (graph replays)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            wl.step(i)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier()
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    tokens_per_step = wl.B * world
+    value = tokens_per_step / (ms_step * 1e-3)
+
+    # ---- dominant op (attention: split-KV kernel + combine), timed alone on its stream
+    n_rep = max(5, min(args.steps // 10, 200))
+    for _ in range(3):
+        wl.attn_graph.replay()
+    torch.cuda.synchronize(device)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(n_rep):
+        wl.attn_graph.replay()
+    a1.record(stream)
+    torch.cuda.synchronize(device)
+    attn_us = a0.elapsed_time(a1) * 1e3 / (10 * n_rep)
+
+    # ---- end to end: pinned inputs in, result out, host waits for every step
+    n_e2e = max(20, min(args.steps // 10, 2000))
+    for i in range(3):
+        wl.e2e[i % ROTATE].replay()
+    torch.cuda.synchronize(device)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        wl.e2e[i % ROTATE].replay()
+        torch.cuda.current_stream(device).synchronize()
+    barrier()
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    if world > 1:
+        t = torch.tensor([e2e_s], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = sum(v.numel() * v.element_size() for v in wl.host.values())
+    d2h = wl.o_host.numel() * wl.o_host.element_size()
+
+    hbm, tc_burst, tc_sust, peak_kind = _peaks()
+    bytes_attn, flops_attn = workload_bytes_flops(cfg, wl.lens)
+    achieved_gbs = bytes_attn / (attn_us * 1e-6) / 1e9
+    t_mem = bytes_attn / (hbm * 1e9)
+    t_tc = flops_attn / (tc_burst * 1e12)
+    roof_us = max(t_mem, t_tc) * 1e6
+    traffic = _ncu_traffic(args.workload)
+
+    out = {
+        "metric": "MLA decode tokens/s at H=128,d_c=512,B=32,N=4K bf16; % of roofline",
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) latents/keys/queries, N(0,1/512) up-projections)",
+        "config": {
+            "workload": args.workload, "B": cfg["B"], "H": cfg["H"], "d_c": cfg["d_c"], "d_r": cfg["d_r"],
+            "d_k": cfg["d_k"], "d_v": cfg["d_v"], "tokens_cached": int(np.sum(wl.lens)),
+            "parallelism": f"replicas x{world}",
+            "l2": f"{ROTATE} rotating cache copies ({ROTATE * bytes_attn / 1e6:.0f} MB > 126 MB L2)",
+            "step": "append+absorb_q+decode_attn(split+combine)+out_up" + ("+gate" if wl.gated else ""),
+        },
+        "gpu_launches": wl.kernels_per_step * args.steps,
+        "e2e": {"value": round(tokens_per_step / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "roofline": {
+            "bound": "hbm", "kernel": "decode_attn (split-KV tensor-core kernel + combine)",
+            "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved_gbs / hbm, 4), "traffic": traffic,
+            "peak_source": f"{peak_kind} hbm_gbs",
+            "attn_us": round(attn_us, 3), "algorithmic_bytes": bytes_attn, "algorithmic_flops": flops_attn,
+            "tflops": round(flops_attn / (attn_us * 1e-6) / 1e12, 1),
+            "roofline_us": round(roof_us, 3), "frac_of_roofline": round(roof_us / attn_us, 4),
+            "frac_of_roofline_sustained_tc": (round(max(t_mem, flops_attn / (tc_sust * 1e12)) * 1e6 / attn_us, 4)
+                                              if tc_sust else None),
+        },
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.workload, args.seed, budget_s=args.cpu_seconds)
+    return out
+
+
+def _ncu_traffic(workload):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        v = d.get(workload)
+        if v and v.get("kernel_hash") == _kernel_hash():
+            return v.get("dram_bytes_per_launch")
+    return None
+
+
+def _kernel_hash():
+    import hashlib
+    p = os.path.join(ROOT, "head_latent_attention_29_b300", "csrc", "k_decode_tc.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+def cpu_baseline(workload: str, seed: int, budget_s: float = 12.0):
+    """Time the float64 oracle's decode step (absorb_q, attention over the prebuilt
+    cache rows, out_up) on the host cores for a bounded sample of sequences."""
+    from oracle import mla_oracle as O
+    try:
+        from threadpoolctl import threadpool_info
+    except Exception:  # pragma: no cover
+        threadpool_info = lambda: []  # noqa: E731
+    cfg = dict(W.WORKLOADS[workload])
+    lens = W.seq_lens(cfg, seed)
+    q_nope, q_r = W.query(cfg, seed)
+    w_uk, w_uv = W.up_weights(cfg, seed)
+    wd = lambda x: W.widen(W.as_dtype(x, cfg["dtype"]), cfg["dtype"])
+    w_uk, w_uv = wd(w_uk), wd(w_uv)
+    q_nope, q_r = wd(q_nope[:, 0]), wd(q_r[:, 0])
+    base = cfg.get("rope_base", 1e4)
+    # prebuilt rows for a few sequences (the cache is resident state, not step work)
+    sample = list(range(min(4, cfg["B"])))
+    rows = {}
+    for b in sample:
+        c, k = W.latent_rows(cfg, seed, b, int(lens[b]))
+        rows[b] = O.cache_rows(wd(c), wd(k), np.arange(int(lens[b])), base)
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        for b in sample:
+            q_cat = O.absorb_q(q_nope[b], q_r[b], int(lens[b]) - 1, w_uk, base)
+            o_lat, _ = O.decode_absorbed(q_cat, rows[b], cfg["d_c"], cfg["scale"])
+            O.out_up(o_lat, w_uv)
+            done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    threads = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+    return {"value": round(done / el, 3), "unit": "tokens/s", "cores": max(threads) if threads else 1,
+            "kind": "oracle", "host_cpus": os.cpu_count(),
+            "sample": f"{done} decode steps of sequences {sample} (N={[int(lens[b]) for b in sample]}), "
+                      f"float64 numpy, {el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    cfg = W.WORKLOADS[args.workload]
+    steps = []
+    for _ in range(max(1, args.warmup)):
+        cpu_baseline(args.workload, args.seed, budget_s=0.5)
+    per = max(1.0, min(10.0, 60.0 / max(args.steps, 1)))
+    for _ in range(args.steps):
+        steps.append(cpu_baseline(args.workload, args.seed, budget_s=per))
+    vals = [s["value"] for s in steps]
+    v = statistics.median(vals)
+    cb = dict(steps[-1])
+    cb["value"] = round(v, 3)
+    return {
+        "impl": "reference",
+        "metric": "MLA decode tokens/s at H=128,d_c=512,B=32,N=4K bf16; % of roofline",
+        "value": round(v, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * cfg["B"] / v, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "B": cfg["B"], "H": cfg["H"], "d_c": cfg["d_c"], "d_r": cfg["d_r"],
+                   "parallelism": "host cores (oracle)"},
+        "cpu_baseline": cb,
+        "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
+    ap.add_argument("--workload", default="decode_h128_b32_n4096", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+    device = torch.device("cuda", local)
+    if world > 1:
+        torch.cuda.set_device(device)
+        dist.init_process_group("nccl", device_id=device)
+    try:
+        out = run_b300(args, rank, world, device)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+    finally:
+        if world > 1:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

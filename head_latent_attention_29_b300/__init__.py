@@ -1,0 +1,231 @@
+"""B300-native MLA decode over a latent KV cache with matrix absorption.
+
+Thin Python binding of ``libmla.so`` (C ABI declared in ``include/mla.h``).  Every
+step of the path runs in the library's CUDA kernels; this module only marshals
+torch tensors (device memory and the current CUDA stream) into pointers and
+sizes.  There is no fallback: if the library is missing or a call fails, an
+exception is raised.
+
+Pipeline of one decode step (absorbed MLA, "MLA multi-head latent attention:
+low-rank compression and matrix absorption", sections 3.1-3.2 and 5.1-5.2):
+
+    cache_append(cache, c_kv, k_r, seq_idx, pos)   # cache row = [c_KV || RoPE(k_R)]
+    q_cat = absorb_q(q_nope, q_rope, q_pos, w_uk)  # [q_nope W_UK || RoPE(q_R)]
+    o_lat, lse = decode_attn(q_cat, cache, seq_lens, scale, ws)
+    o = out_up(o_lat, w_uv)                        # W_UV applied after attention
+    gate(h, w_g, o.view(B, -1))                    # gated variant only
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "MlaError", "LatentCache", "lib", "cache_append", "absorb_q", "decode_workspace",
+    "decode_attn", "out_up", "gate", "get_device_error", "LIB_PATH",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmla.so")
+
+MLA_BF16, MLA_F32 = 0, 1
+_DT = {torch.bfloat16: MLA_BF16, torch.float32: MLA_F32}
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = _lib_handle.mla_status_string(status).decode() if _lib_handle is not None else str(status)
+        super().__init__(f"{where}: {msg}")
+        self.status = status
+
+
+class _Cache(ctypes.Structure):
+    _fields_ = [
+        ("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("B", ctypes.c_int32),
+        ("N_max", ctypes.c_int32), ("d_c", ctypes.c_int32), ("d_r", ctypes.c_int32),
+        ("_pad", ctypes.c_int32), ("row_stride", ctypes.c_int64),
+    ]
+
+
+_lib_handle = None
+
+_SIGS = {
+    "mla_abi_version": (ctypes.c_int32, []),
+    "mla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "mla_cache_append": (ctypes.c_int, [ctypes.POINTER(_Cache), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p]),
+    "mla_absorb_q": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                    ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p]),
+    "mla_decode_workspace_size": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    "mla_decode_attn": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(_Cache), ctypes.c_void_p, ctypes.c_int32,
+                                       ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p]),
+    "mla_out_up": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]),
+    "mla_gate": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]),
+    "mla_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmla.so from the package directory (raises if it was not built)."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libmla.so not built at {LIB_PATH}; run `python -m head_latent_attention_29_b300._build`")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(h, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib_handle = h
+    return _lib_handle
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise MlaError(status, where)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _stream(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _dev_tensor(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+class LatentCache:
+    """One layer's latent cache [B, N_max, row_stride] on the device.
+
+    Row t of sequence b holds [c_KV (d_c) || RoPE(k_R) (d_r)] (icman.com.cn MLA
+    article, section 2).  ``row_stride`` defaults to d_c + d_r rounded up to 16
+    bytes.  The tensor is allocated by torch and owned by this object."""
+
+    def __init__(self, B: int, N_max: int, d_c: int, d_r: int, dtype=torch.bfloat16, device="cuda",
+                 row_stride: int | None = None, data: torch.Tensor | None = None):
+        esz = 2 if dtype == torch.bfloat16 else 4
+        R = d_c + d_r
+        if row_stride is None:
+            row_stride = ((R * esz + 15) // 16) * 16 // esz
+        self.B, self.N_max, self.d_c, self.d_r, self.row_stride = B, N_max, d_c, d_r, row_stride
+        self.dtype = dtype
+        if data is None:
+            data = torch.zeros((B, N_max, row_stride), dtype=dtype, device=device)
+        elif tuple(data.shape) != (B, N_max, row_stride) or data.dtype != dtype:
+            raise ValueError("cache tensor shape/dtype mismatch")
+        self.data = data
+
+    @property
+    def rows(self) -> torch.Tensor:
+        """View [B, N_max, d_c + d_r] of the cached rows (padding excluded)."""
+        return self.data[..., : self.d_c + self.d_r]
+
+    def struct(self) -> _Cache:
+        return _Cache(self.data.data_ptr(), _DT[self.dtype], self.B, self.N_max, self.d_c, self.d_r, 0,
+                      self.row_stride)
+
+
+def cache_append(cache: LatentCache, c_kv: torch.Tensor, k_r: torch.Tensor | None, seq_idx: torch.Tensor,
+                 pos: torch.Tensor, rope_base: float = 10000.0) -> None:
+    """Write T rows: cache[seq_idx[i], pos[i]] = [c_kv[i] || RoPE(k_r[i], pos[i])]."""
+    _dev_tensor(c_kv, "c_kv", cache.dtype)
+    if cache.d_r > 0:
+        _dev_tensor(k_r, "k_r", cache.dtype)
+    _dev_tensor(seq_idx, "seq_idx", torch.int32)
+    _dev_tensor(pos, "pos", torch.int32)
+    T = seq_idx.numel()
+    st = cache.struct()
+    _check(lib().mla_cache_append(ctypes.byref(st), _ptr(c_kv), _ptr(k_r if cache.d_r > 0 else None), _ptr(seq_idx),
+                                  _ptr(pos), T, float(rope_base), _stream(c_kv)), "mla_cache_append")
+
+
+def absorb_q(q_nope: torch.Tensor, q_rope: torch.Tensor | None, q_pos: torch.Tensor, w_uk: torch.Tensor,
+             rope_base: float = 10000.0, out: torch.Tensor | None = None) -> torch.Tensor:
+    """q_cat [B, H, d_c + d_r] = [q_nope W_UK || RoPE(q_rope, q_pos)] per head."""
+    _dev_tensor(q_nope, "q_nope")
+    B, H, d_k = q_nope.shape
+    _dev_tensor(w_uk, "w_uk", q_nope.dtype)
+    d_c = w_uk.shape[2]
+    d_r = 0 if q_rope is None else q_rope.shape[2]
+    if q_rope is not None:
+        _dev_tensor(q_rope, "q_rope", q_nope.dtype)
+    _dev_tensor(q_pos, "q_pos", torch.int32)
+    if out is None:
+        out = torch.empty((B, H, d_c + d_r), dtype=q_nope.dtype, device=q_nope.device)
+    _check(lib().mla_absorb_q(_ptr(q_nope), _ptr(q_rope), _ptr(q_pos), _ptr(w_uk), _ptr(out), B, H, d_k, d_c, d_r,
+                              _DT[q_nope.dtype], float(rope_base), _stream(q_nope)), "mla_absorb_q")
+    return out
+
+
+def decode_workspace(B: int, H: int, d_c: int, dtype=torch.bfloat16, device="cuda") -> torch.Tensor:
+    n = lib().mla_decode_workspace_size(B, H, d_c, _DT[dtype])
+    if n == 0:
+        raise MlaError(2, "mla_decode_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def decode_attn(q_cat: torch.Tensor, cache: LatentCache, seq_lens: torch.Tensor, scale: float,
+                workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                lse: torch.Tensor | None = None, want_lse: bool = True):
+    """o_lat [B, H, d_c] (and lse [B, H] fp32) of absorbed decode attention."""
+    _dev_tensor(q_cat, "q_cat", cache.dtype)
+    B, H, R = q_cat.shape
+    if B != cache.B or R != cache.d_c + cache.d_r:
+        raise ValueError("q_cat shape does not match the cache")
+    _dev_tensor(seq_lens, "seq_lens", torch.int32)
+    if workspace is None:
+        workspace = decode_workspace(B, H, cache.d_c, cache.dtype, q_cat.device)
+    if out is None:
+        out = torch.empty((B, H, cache.d_c), dtype=cache.dtype, device=q_cat.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q_cat.device)
+    st = cache.struct()
+    _check(lib().mla_decode_attn(_ptr(q_cat), ctypes.byref(st), _ptr(seq_lens), H, float(scale), _ptr(workspace),
+                                 workspace.numel(), _ptr(out), _ptr(lse), _stream(q_cat)), "mla_decode_attn")
+    return out, lse
+
+
+def out_up(o_lat: torch.Tensor, w_uv: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """o [B, H, d_v] = o_lat W_UV^T per head (W_UV stored [H, d_v, d_c])."""
+    _dev_tensor(o_lat, "o_lat")
+    _dev_tensor(w_uv, "w_uv", o_lat.dtype)
+    B, H, d_c = o_lat.shape
+    d_v = w_uv.shape[1]
+    if out is None:
+        out = torch.empty((B, H, d_v), dtype=o_lat.dtype, device=o_lat.device)
+    _check(lib().mla_out_up(_ptr(o_lat), _ptr(w_uv), _ptr(out), B, H, d_c, d_v, _DT[o_lat.dtype], _stream(o_lat)),
+           "mla_out_up")
+    return out
+
+
+def gate(h: torch.Tensor, w_g: torch.Tensor, o: torch.Tensor) -> torch.Tensor:
+    """In place: o [B, width] *= sigmoid(h W_g)."""
+    _dev_tensor(h, "h")
+    _dev_tensor(w_g, "w_g", h.dtype)
+    _dev_tensor(o, "o", h.dtype)
+    B, d_model = h.shape
+    width = w_g.shape[1]
+    _check(lib().mla_gate(_ptr(h), _ptr(w_g), _ptr(o), B, d_model, width, _DT[h.dtype], _stream(h)), "mla_gate")
+    return o
+
+
+def get_device_error() -> tuple[int, int]:
+    """(status, raw word) recorded by the kernels since the last call; synchronises the device."""
+    word = ctypes.c_uint32(0)
+    st = lib().mla_get_device_error(ctypes.byref(word))
+    return st, word.value

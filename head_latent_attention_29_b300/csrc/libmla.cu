@@ -1,0 +1,5 @@
+// Single translation unit of libmla: the kernels share one device error word,
+// so all sources are compiled together.
+#include "k_simt.cu"
+#include "k_decode_tc.cu"
+#include "mla_api.cu"

@@ -1,0 +1,123 @@
+// extern "C" entry points of libmla: host-side validation and dispatch to the
+// kernels.  Nothing here allocates device memory or synchronises the host
+// (except mla_get_device_error, which reads the device error word).
+#include "mla_internal.cuh"
+
+namespace {
+
+using mla::aligned16;
+
+bool valid_dtype(int32_t dt) { return dt == MLA_BF16 || dt == MLA_F32; }
+
+size_t elem_size(int32_t dt) { return dt == MLA_BF16 ? 2 : 4; }
+
+mla_status check_cache(const mla_cache* c) {
+  if (c == nullptr || c->data == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!valid_dtype(c->dtype)) return MLA_ERR_INVALID_ARG;
+  if (c->B <= 0 || c->N_max <= 0 || c->d_c <= 0 || c->d_r < 0 || (c->d_r & 1) != 0) return MLA_ERR_INVALID_ARG;
+  if (c->row_stride < static_cast<int64_t>(c->d_c) + c->d_r) return MLA_ERR_INVALID_ARG;
+  if ((c->row_stride * static_cast<int64_t>(elem_size(c->dtype))) % 16 != 0) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(c->data)) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+MLA_API int32_t mla_abi_version(void) { return 1; }
+
+MLA_API const char* mla_status_string(mla_status st) {
+  switch (st) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: no kernel for this shape/dtype";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA: CUDA call failed";
+    case MLA_ERR_DEVICE_TIMEOUT: return "MLA_ERR_DEVICE_TIMEOUT: a kernel's bounded wait expired";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case MLA_ERR_DEVICE_INDEX: return "MLA_ERR_DEVICE_INDEX: device-side index or length out of range";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+MLA_API mla_status mla_cache_append(const mla_cache* cache, const void* c_kv, const void* k_r,
+                                    const int32_t* seq_idx, const int32_t* pos, int32_t T, float rope_base,
+                                    void* stream) {
+  mla_status st = check_cache(cache);
+  if (st != MLA_OK) return st;
+  if (T < 0) return MLA_ERR_INVALID_ARG;
+  if (T == 0) return MLA_OK;
+  if (c_kv == nullptr || seq_idx == nullptr || pos == nullptr) return MLA_ERR_INVALID_ARG;
+  if (cache->d_r > 0 && k_r == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!(rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
+  return mla::launch_cache_append(*cache, c_kv, k_r, seq_idx, pos, T, rope_base, as_stream(stream));
+}
+
+MLA_API mla_status mla_absorb_q(const void* q_nope, const void* q_rope, const int32_t* q_pos, const void* w_uk,
+                                void* q_cat, int32_t B, int32_t H, int32_t d_k, int32_t d_c, int32_t d_r,
+                                int32_t dtype, float rope_base, void* stream) {
+  if (!valid_dtype(dtype)) return MLA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || d_k <= 0 || d_c <= 0 || d_r < 0 || (d_r & 1) != 0) return MLA_ERR_INVALID_ARG;
+  if (q_nope == nullptr || w_uk == nullptr || q_cat == nullptr || q_pos == nullptr) return MLA_ERR_INVALID_ARG;
+  if (d_r > 0 && q_rope == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!(rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (static_cast<size_t>(32) * d_k * sizeof(float) > 200 * 1024) return MLA_ERR_UNSUPPORTED;
+  return mla::launch_absorb_q(q_nope, q_rope, q_pos, w_uk, q_cat, B, H, d_k, d_c, d_r, dtype, rope_base,
+                              as_stream(stream));
+}
+
+MLA_API size_t mla_decode_workspace_size(int32_t B, int32_t H, int32_t d_c, int32_t dtype) {
+  if (B <= 0 || H <= 0 || d_c <= 0) return 0;
+  if (dtype == MLA_F32) return 256;  // the fp32 path needs no scratch; a token size keeps the API uniform
+  if (dtype == MLA_BF16 && d_c == 512 && H <= 128) return mla::decode_tc_workspace_size(B);
+  return 0;
+}
+
+MLA_API mla_status mla_decode_attn(const void* q_cat, const mla_cache* cache, const int32_t* seq_lens, int32_t H,
+                                   float scale, void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
+                                   void* stream) {
+  mla_status st = check_cache(cache);
+  if (st != MLA_OK) return st;
+  if (q_cat == nullptr || seq_lens == nullptr || o_lat == nullptr || H <= 0) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_cat) || !aligned16(o_lat)) return MLA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) && !(scale < 0.f) && scale != 0.f) return MLA_ERR_INVALID_ARG;  // NaN
+  if (cache->dtype == MLA_F32) {
+    if (cache->d_c > 1024 || cache->d_r > 256 || H > 1024) return MLA_ERR_UNSUPPORTED;
+    return mla::launch_decode_f32(static_cast<const float*>(q_cat), *cache, seq_lens, H, scale,
+                                  static_cast<float*>(o_lat), lse, as_stream(stream));
+  }
+  if (cache->d_c != 512 || (cache->d_r != 0 && cache->d_r != 64) || H > 128) return MLA_ERR_UNSUPPORTED;
+  return mla::launch_decode_tc(q_cat, *cache, seq_lens, H, scale, workspace, workspace_bytes, o_lat, lse,
+                               as_stream(stream));
+}
+
+MLA_API mla_status mla_out_up(const void* o_lat, const void* w_uv, void* o, int32_t B, int32_t H, int32_t d_c,
+                              int32_t d_v, int32_t dtype, void* stream) {
+  if (!valid_dtype(dtype)) return MLA_ERR_INVALID_ARG;
+  if (o_lat == nullptr || w_uv == nullptr || o == nullptr) return MLA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || d_c <= 0 || d_v <= 0) return MLA_ERR_INVALID_ARG;
+  if (d_c > 1024) return MLA_ERR_UNSUPPORTED;
+  return mla::launch_out_up(o_lat, w_uv, o, B, H, d_c, d_v, dtype, as_stream(stream));
+}
+
+MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, int32_t d_model, int32_t width,
+                            int32_t dtype, void* stream) {
+  if (!valid_dtype(dtype)) return MLA_ERR_INVALID_ARG;
+  if (h == nullptr || w_g == nullptr || o == nullptr) return MLA_ERR_INVALID_ARG;
+  if (B <= 0 || d_model <= 0 || width <= 0) return MLA_ERR_INVALID_ARG;
+  return mla::launch_gate(h, w_g, o, B, d_model, width, dtype, as_stream(stream));
+}
+
+MLA_API mla_status mla_get_device_error(uint32_t* detail) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, mla::g_device_error, sizeof(word)) != cudaSuccess) return MLA_ERR_CUDA;
+  const unsigned int zero = 0;
+  if (cudaMemcpyToSymbol(mla::g_device_error, &zero, sizeof(zero)) != cudaSuccess) return MLA_ERR_CUDA;
+  if (detail != nullptr) *detail = word;
+  return static_cast<mla_status>(word & 0xFFu);
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// Declarations shared by the translation units of libmla (host launchers and the
+// device error word).  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+// Device error word: low byte = mla_status, bits 8.. = the site that set it.
+// First writer wins (atomicCAS from 0); mla_get_device_error() reads and clears.
+// libmla is built as one translation unit (libmla.cu), which defines it once.
+__device__ unsigned int g_device_error = 0;
+
+enum ErrorSite : unsigned int {
+  kSiteAppendIndex = 1,
+  kSiteDecodeLength = 2,
+  kSiteDecodeWait = 3,
+  kSiteDecodeTmem = 4,
+};
+
+__device__ __forceinline__ void record_error(mla_status st, unsigned int site) {
+  atomicCAS(&g_device_error, 0u, static_cast<unsigned int>(st) | (site << 8));
+}
+
+// Element load/store in fp32 arithmetic for the two storage types.
+__device__ __forceinline__ float ld_elem(const float* p) { return *p; }
+__device__ __forceinline__ float ld_elem(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void st_elem(float* p, float v) { *p = v; }
+__device__ __forceinline__ void st_elem(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+// ---- host launchers (one per kernel family), defined in the .cu files -------
+mla_status launch_cache_append(const mla_cache& c, const void* c_kv, const void* k_r, const int32_t* seq_idx,
+                               const int32_t* pos, int32_t T, float rope_base, cudaStream_t s);
+mla_status launch_absorb_q(const void* q_nope, const void* q_rope, const int32_t* q_pos, const void* w_uk,
+                           void* q_cat, int32_t B, int32_t H, int32_t d_k, int32_t d_c, int32_t d_r,
+                           int32_t dtype, float rope_base, cudaStream_t s);
+mla_status launch_out_up(const void* o_lat, const void* w_uv, void* o, int32_t B, int32_t H, int32_t d_c,
+                         int32_t d_v, int32_t dtype, cudaStream_t s);
+mla_status launch_gate(const void* h, const void* w_g, void* o, int32_t B, int32_t d_model, int32_t width,
+                       int32_t dtype, cudaStream_t s);
+mla_status launch_decode_f32(const float* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
+                             float scale, float* o_lat, float* lse, cudaStream_t s);
+
+// tensor-core decode (bf16): sizes and launch
+size_t decode_tc_workspace_size(int32_t B);
+mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
+                            float scale, void* ws, size_t ws_bytes, void* o_lat, float* lse, cudaStream_t s);
+
+}  // namespace mla

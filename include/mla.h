@@ -1,0 +1,194 @@
+/*
+ * mla.h -- C ABI of libmla: Multi-head Latent Attention (MLA) decode over a
+ * compressed latent KV cache, with the up-projections absorbed.
+ *
+ * The method (pages this library restates):
+ *   - "MLA multi-head latent attention: low-rank compression and matrix
+ *     absorption" (0539edu.com): section 2.2 (c_KV = h W_DKV, k = c_KV W_UK,
+ *     v = c_KV W_UV), section 3.1 (q k^T = (q W_UK^T) c_KV^T and
+ *     attn v = (attn c_KV) W_UV), sections 3.2 / 5.1 (absorbed inference with the
+ *     weights viewed as [h, d_k, d_c] and [h, d_v, d_c]), section 5.2 (a
+ *     preallocated latent cache written by position).
+ *   - icman.com.cn MLA article, section 2 "decoupled RoPE": each cached token is
+ *     a 512-wide latent c_KV followed by a 64-wide key k_R with RoPE applied.
+ *   - attention-variants interview guide (hotelren.com): section 6.2 (one RoPE
+ *     key shared by every head), section 7.3 (max-subtracted softmax).
+ *   - "Gated MLA" (tahou.com): sections 2.6 / 3.2 (full-rank sigmoid output gate
+ *     over the concatenated v width), section 3.3 (no positional encoding).
+ *
+ * Conventions shared by every call:
+ *   - Every tensor argument is a DEVICE pointer owned by the caller, unless the
+ *     argument says "host".  The library never allocates device memory and never
+ *     synchronises the host, except in mla_get_device_error().  All work is queued
+ *     asynchronously on `stream` (a cudaStream_t passed as void*; NULL = the
+ *     legacy default stream).
+ *   - Tensors are dense, row-major, with the shapes given in brackets; the cache
+ *     may have padded rows (row_stride).  Element type is given by an mla_dtype
+ *     argument: MLA_BF16 (bfloat16 storage, fp32 arithmetic) or MLA_F32.
+ *   - Pointers must be 16-byte aligned.  Bad arguments that the host can see
+ *     (null pointers, non-positive or unsupported sizes, misalignment, a
+ *     workspace that is too small) return MLA_ERR_INVALID_ARG / MLA_ERR_WORKSPACE
+ *     and launch nothing.  Bad values that only the device can see (an index or a
+ *     sequence length out of range) are skipped/clamped by the kernels and
+ *     recorded in a device error word, which mla_get_device_error() returns.
+ *   - No exception crosses this ABI; every entry point returns mla_status.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,    /* a host-visible argument is invalid            */
+  MLA_ERR_UNSUPPORTED = 2,    /* valid shape that this build has no kernel for */
+  MLA_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed             */
+  MLA_ERR_DEVICE_TIMEOUT = 4, /* a kernel's bounded wait expired (device word) */
+  MLA_ERR_WORKSPACE = 5,      /* workspace pointer null or too small           */
+  MLA_ERR_DEVICE_INDEX = 6    /* a device-side index/length was out of range   */
+} mla_status;
+
+typedef enum { MLA_BF16 = 0, MLA_F32 = 1 } mla_dtype;
+
+/*
+ * One layer's latent cache: data[b][t][0 : d_c + d_r] for b < B, t < N_max.
+ * Row t of sequence b holds [c_KV(t) || RoPE(k_R(t), t)] (icman.com.cn section 2
+ * cache-row figure; the position-indexed preallocated buffer of 0539edu.com
+ * section 5.2).  row_stride >= d_c + d_r elements, and row_stride * element size
+ * must be a multiple of 16 bytes.  The caller owns the buffer and the per-sequence
+ * lengths; rows at t >= length may hold anything (they are never read into a
+ * result).
+ */
+typedef struct {
+  void* data;         /* device pointer, [B][N_max][row_stride] of dtype          */
+  int32_t dtype;      /* mla_dtype                                                */
+  int32_t B;          /* sequences                                                */
+  int32_t N_max;      /* rows per sequence                                        */
+  int32_t d_c;        /* latent width                                             */
+  int32_t d_r;        /* decoupled RoPE key width (0 = no positional key)         */
+  int32_t _pad;
+  int64_t row_stride; /* elements between consecutive rows                        */
+} mla_cache;
+
+/* Version of this ABI (bumped on any incompatible change). */
+MLA_API int32_t mla_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+MLA_API const char* mla_status_string(mla_status status);
+
+/*
+ * mla_cache_append -- write T new tokens into the latent cache.
+ *   For each i < T: cache[seq_idx[i]][pos[i]] = [c_kv[i] || RoPE(k_r[i], pos[i])].
+ *   RoPE rotates pairs (2j, 2j+1) of k_r by angle pos * base^(-2j/d_r); the angle
+ *   is formed in double precision.  (Decoupled RoPE key: icman.com.cn section 2;
+ *   hotelren.com section 6.2; append-by-position: 0539edu.com section 5.2.)
+ *   c_kv     [T, d_c]   dtype = cache->dtype
+ *   k_r      [T, d_r]   dtype = cache->dtype; may be NULL iff d_r == 0
+ *   seq_idx  [T] int32  sequence of each row, in [0, B)
+ *   pos      [T] int32  position of each row, in [0, N_max)
+ *   A row whose seq_idx/pos is out of range is skipped and recorded as
+ *   MLA_ERR_DEVICE_INDEX in the device error word.  Rows must not alias.
+ */
+MLA_API mla_status mla_cache_append(const mla_cache* cache, const void* c_kv, const void* k_r,
+                                    const int32_t* seq_idx, const int32_t* pos, int32_t T,
+                                    float rope_base, void* stream);
+
+/*
+ * mla_absorb_q -- fold W_UK into the query and rotate the RoPE part.
+ *   q_cat[b][h] = [ q_nope[b][h] . W_UK[h]  ||  RoPE(q_rope[b][h], q_pos[b]) ]
+ *   i.e. q_lat[b][h][c] = sum_d q_nope[b][h][d] * W_UK[h][d][c]
+ *   (0539edu.com sections 3.1, 3.2 and 5.1: q W_UK^T computed once per query, with
+ *   W_UK viewed as [h, d_k, d_c]).  Arithmetic in fp32; q_cat stored in dtype.
+ *   q_nope [B, H, d_k]; q_rope [B, H, d_r] (NULL iff d_r == 0);
+ *   q_pos [B] int32 (query position, normally length-1); W_UK [H, d_k, d_c];
+ *   q_cat [B, H, d_c + d_r] (output).
+ */
+MLA_API mla_status mla_absorb_q(const void* q_nope, const void* q_rope, const int32_t* q_pos,
+                                const void* w_uk, void* q_cat, int32_t B, int32_t H, int32_t d_k,
+                                int32_t d_c, int32_t d_r, int32_t dtype, float rope_base,
+                                void* stream);
+
+/*
+ * mla_decode_workspace_size -- bytes of device workspace mla_decode_attn needs
+ * for B sequences and H heads of width d_c (split-KV partials, the block prefix
+ * table and the split plan).  The size depends on the current device's SM count.
+ * Returns 0 if the shape is unsupported.
+ */
+MLA_API size_t mla_decode_workspace_size(int32_t B, int32_t H, int32_t d_c, int32_t dtype);
+
+/*
+ * mla_decode_attn -- absorbed decode attention over the latent cache.
+ *   For each sequence b with n = seq_lens[b] cached tokens and each head h:
+ *     s_t  = scale * ( q_cat[b][h] . cache[b][t] )     over the d_c + d_r row
+ *     p    = softmax_t(s)                              (max-subtracted)
+ *     o_lat[b][h] = sum_t p_t * cache[b][t][0 : d_c]
+ *     lse[b][h]   = ln sum_t exp(s_t)
+ *   (0539edu.com sections 3.1-3.2: scores against c_KV directly, o_lat = P c_KV;
+ *   the 64-wide rotated key term is the decoupled RoPE of icman.com.cn section 2;
+ *   hotelren.com section 7.3 for the max subtraction.)
+ *   The tokens of all sequences are split into equal runs across the GPU; each
+ *   run produces an unnormalised partial (m, l, O) and a log-sum-exp combine
+ *   merges the runs of each sequence.
+ *   q_cat     [B, H, d_c + d_r]  dtype = cache->dtype
+ *   seq_lens  [B] int32 device; 0 <= seq_lens[b] <= N_max.  A sequence of length 0
+ *             gives o_lat = 0 and lse = -inf.  Out-of-range lengths are clamped
+ *             and recorded as MLA_ERR_DEVICE_INDEX.
+ *   workspace device scratch of at least mla_decode_workspace_size() bytes,
+ *             256-byte aligned; contents need no initialisation; calls that
+ *             share one workspace must be ordered on one stream.
+ *   o_lat     [B, H, d_c] dtype (output);  lse [B, H] float32 or NULL.
+ *   bf16 path: d_c = 512, d_r in {0, 64}, 1 <= H <= 128 (tensor-core kernel,
+ *   bf16 operands, fp32 accumulation).  f32 path: any d_c <= 1024, d_r <= 256,
+ *   H <= 1024 (fp32 CUDA-core kernel).  Other shapes: MLA_ERR_UNSUPPORTED.
+ */
+MLA_API mla_status mla_decode_attn(const void* q_cat, const mla_cache* cache,
+                                   const int32_t* seq_lens, int32_t H, float scale,
+                                   void* workspace, size_t workspace_bytes, void* o_lat,
+                                   float* lse, void* stream);
+
+/*
+ * mla_out_up -- apply W_UV after attention, per head:
+ *   o[b][h][d] = sum_c o_lat[b][h][c] * W_UV[h][d][c]
+ *   (0539edu.com section 3.1, attn v = (attn c_KV) W_UV; weight view [h, d_v, d_c]
+ *   of section 3.2).  o_lat [B, H, d_c]; W_UV [H, d_v, d_c]; o [B, H, d_v].
+ *   fp32 arithmetic, dtype storage.
+ */
+MLA_API mla_status mla_out_up(const void* o_lat, const void* w_uv, void* o, int32_t B, int32_t H,
+                              int32_t d_c, int32_t d_v, int32_t dtype, void* stream);
+
+/*
+ * mla_gate -- full-rank output gate of the gated variant, in place:
+ *   o[b][j] *= sigmoid( sum_i h[b][i] * W_g[i][j] ),  j < width (= H * d_v)
+ *   (tahou.com sections 2.6 and 3.2: one gate value per channel of the
+ *   concatenated v-width output, computed from the token's own input).
+ *   h [B, d_model]; W_g [d_model, width]; o [B, width] (read and written).
+ */
+MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, int32_t d_model,
+                            int32_t width, int32_t dtype, void* stream);
+
+/*
+ * mla_get_device_error -- wait for the device, then read and clear the device
+ * error word written by the kernels of this library on the current device.
+ * Returns MLA_OK if no kernel recorded an error since the last call, otherwise
+ * the recorded status (MLA_ERR_DEVICE_TIMEOUT, MLA_ERR_DEVICE_INDEX).  If
+ * `detail` is not NULL it receives the raw word (status in the low byte, the
+ * site that recorded it above).
+ */
+MLA_API mla_status mla_get_device_error(uint32_t* detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

@@ -1,0 +1,95 @@
+"""CPU-side checks of the C ABI: the library builds for sm_103a, loads without a
+GPU, exports every symbol include/mla.h declares, and rejects host-visible bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def libmla():
+    from head_latent_attention_29_b300 import _build
+    _build.build()
+    import head_latent_attention_29_b300 as mla
+    return mla.lib()
+
+
+def _declared_symbols():
+    with open(os.path.join(ROOT, "include", "mla.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path():
+    syms = _declared_symbols()
+    for name in ["mla_cache_append", "mla_absorb_q", "mla_decode_attn", "mla_decode_workspace_size",
+                 "mla_out_up", "mla_gate", "mla_get_device_error", "mla_status_string", "mla_abi_version"]:
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(libmla):
+    for name in _declared_symbols():
+        assert hasattr(libmla, name), name
+
+
+def test_abi_version_and_status_strings(libmla):
+    assert libmla.mla_abi_version() == 1
+    for st in range(7):
+        s = libmla.mla_status_string(st).decode()
+        assert s.startswith("MLA_")
+    assert libmla.mla_status_string(99).decode() == "MLA_ERR_UNKNOWN"
+
+
+def test_workspace_size_rules(libmla):
+    ws = libmla.mla_decode_workspace_size
+    assert ws(32, 128, 512, 0) > 32 * 128 * 512 * 4          # partials for at least one run per sequence
+    assert ws(64, 128, 512, 0) > ws(32, 128, 512, 0)
+    assert ws(32, 128, 256, 0) == 0                         # bf16 tensor-core path needs d_c = 512
+    assert ws(32, 256, 512, 0) == 0                         # and at most 128 heads
+    assert ws(1, 4, 32, 1) > 0                              # fp32 path takes any small shape
+    assert ws(0, 4, 32, 1) == 0
+
+
+def test_host_validation_rejects_bad_arguments(libmla):
+    import head_latent_attention_29_b300 as mla
+    INVALID = 1
+    null = ctypes.c_void_p(0)
+    # null cache / null data pointer
+    assert libmla.mla_cache_append(None, null, null, null, null, 1, 10000.0, null) == INVALID
+    c = mla._Cache(0, 0, 1, 8, 512, 64, 0, 576)
+    assert libmla.mla_cache_append(ctypes.byref(c), null, null, null, null, 1, 10000.0, null) == INVALID
+    # misaligned cache pointer, bad row stride, odd RoPE width
+    c = mla._Cache(0x1008, 0, 1, 8, 512, 64, 0, 576)
+    assert libmla.mla_decode_attn(null, ctypes.byref(c), null, 128, 0.1, null, 0, null, null, null) == INVALID
+    c = mla._Cache(0x1000, 0, 1, 8, 512, 64, 0, 570)
+    assert libmla.mla_decode_attn(null, ctypes.byref(c), null, 128, 0.1, null, 0, null, null, null) == INVALID
+    c = mla._Cache(0x1000, 0, 1, 8, 512, 63, 0, 576)
+    assert libmla.mla_decode_attn(null, ctypes.byref(c), null, 128, 0.1, null, 0, null, null, null) == INVALID
+    # non-positive sizes and null tensors
+    assert libmla.mla_absorb_q(null, null, null, null, null, 0, 128, 128, 512, 64, 0, 10000.0, null) == INVALID
+    assert libmla.mla_out_up(null, null, null, 1, 1, 1, 1, 0, null) == INVALID
+    assert libmla.mla_gate(null, null, null, 1, 1, 1, 0, null) == INVALID
+    # unknown dtype
+    assert libmla.mla_out_up(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16), 1, 1, 1, 1, 7, null) == INVALID
+
+
+def test_unsupported_bf16_shapes_are_refused(libmla):
+    import head_latent_attention_29_b300 as mla
+    UNSUPPORTED = 2
+    c = mla._Cache(0x1000, 0, 1, 8, 256, 64, 0, 320)   # d_c = 256 has no tensor-core kernel
+    p = ctypes.c_void_p(0x2000)
+    assert libmla.mla_decode_attn(p, ctypes.byref(c), p, 128, 0.1, p, 1 << 20, p, None, None) == UNSUPPORTED
+    c = mla._Cache(0x1000, 0, 1, 8, 512, 64, 0, 576)   # more than 128 heads
+    assert libmla.mla_decode_attn(p, ctypes.byref(c), p, 256, 0.1, p, 1 << 20, p, None, None) == UNSUPPORTED
+
+
+def test_product_path_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    import head_latent_attention_29_b300 as mla
+    monkeypatch.setattr(mla, "_lib_handle", None)
+    monkeypatch.setattr(mla, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        mla.lib()
