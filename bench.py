@@ -66,23 +66,36 @@ class ClockSampler:
         self._period = period_s
         self._dev = device_index
         self._ok = False
+        self.error = None
         try:
             import pynvml
+            import torch
             pynvml.nvmlInit()
             self._nv = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            # NVML numbers GPUs without regard to CUDA_VISIBLE_DEVICES: find ours by UUID
+            try:
+                uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+                self._h = pynvml.nvmlDeviceGetHandleByUUID(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+            except Exception:
+                self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self._reasons_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
             self._ok = True
-        except Exception:
+        except Exception as e:  # reported in the JSON line
+            self.error = repr(e)[:200]
             self._ok = False
 
     def _run(self):
         while not self._stop.is_set():
             try:
                 self.samples.append(self._nv.nvmlDeviceGetClockInfo(self._h, self._nv.NVML_CLOCK_SM))
-                self.reasons |= int(self._nv.nvmlDeviceGetCurrentClocksEventReasons(self._h))
-            except Exception:
-                pass
+            except Exception as e:
+                self.error = repr(e)[:200]
+            try:
+                self.reasons |= int(self._reasons_fn(self._h))
+            except Exception as e:
+                self.error = repr(e)[:200]
             time.sleep(self._period)
 
     def __enter__(self):
@@ -98,7 +111,7 @@ class ClockSampler:
 
     def summary(self):
         if not self._ok or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"], "error": self.error}
         names = [n for bit, n in THROTTLE_BITS.items() if self.reasons & bit]
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": names,
                 "samples": len(self.samples)}
@@ -363,8 +376,9 @@ def cpu_baseline(workload: str, seed: int, budget_s: float = 12.0):
         if el >= budget_s:
             break
     threads = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+    env = {k: os.environ[k] for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS") if k in os.environ}
     return {"value": round(done / el, 3), "unit": "tokens/s", "cores": max(threads) if threads else 1,
-            "kind": "oracle", "host_cpus": os.cpu_count(),
+            "kind": "oracle", "host_cpus": os.cpu_count(), "thread_env": env,
             "sample": f"{done} decode steps of sequences {sample} (N={[int(lens[b]) for b in sample]}), "
                       f"float64 numpy, {el:.1f} s"}
 

@@ -85,13 +85,15 @@ def test_decode_large_scores_trigger_rescale(mla):
     lens = np.array([3000, 2000], dtype=np.int32)
     d_c, d_r, H = 512, 64, 128
     q_bits, rows = direct_decode_inputs(5, lens, H, d_c, d_r)
-    # make scores grow along the sequence: rows get an increasing component along q
+    # make scores grow along the sequence through the RoPE key columns (which do
+    # not enter o_lat, so the output keeps unit magnitude): the score of token t
+    # rises by ~20 (natural units) from the first block to the last
     for b, r in enumerate(rows):
         f = W.bf16_to_f32(r)
-        f[:, 0] = np.linspace(-3, 3, f.shape[0]).astype(np.float32) * 4
+        f[:, d_c] = np.linspace(-3, 3, f.shape[0]).astype(np.float32) * 4
         rows[b] = W.bf16_bits(f)
     qf = W.bf16_to_f32(q_bits)
-    qf[..., 0] = 6.0
+    qf[..., d_c] = 6.0
     q_bits = W.bf16_bits(qf)
     scale = 1.0 / math.sqrt(192)
     q, cache = upload_direct(mla, q_bits, rows, d_c, d_r, int(lens.max()))
