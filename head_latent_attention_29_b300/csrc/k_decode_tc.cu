@@ -16,7 +16,9 @@
 //        of S = Q C^T, 288 columns), computes S for 64-token blocks into a
 //        double-buffered 64-column accumulator, runs the online softmax (one
 //        thread per head row, no cross-thread reduction), and writes the bf16
-//        probabilities P straight into CTA 1's shared memory.
+//        probabilities P straight into CTA 1's shared memory with st.async,
+//        which completes bytes on CTA 1's barrier (no cluster-scope fences on
+//        the producer side).
 //      - CTA 1 (output CTA) accumulates O += P C[:, 0:512] with two N = 256
 //        MMAs per 16-token step into its full 512-column tensor memory, and
 //        rescales O in place on the rare blocks where the running maximum of a
@@ -35,6 +37,14 @@
 #include "mla_internal.cuh"
 #include "mla_ptx.cuh"
 
+// Timing hooks: empty in the library; an instrumented build may define them to
+// record (block, event) timestamps.
+#ifndef MLA_TRACE_POINT
+#define MLA_TRACE_POINT(block, event) \
+  do {                                 \
+  } while (0)
+#endif
+
 namespace mla {
 namespace dtc {
 
@@ -42,49 +52,58 @@ constexpr int kBN = 64;                     // tokens per block
 constexpr int kDC = 512;                    // latent width
 constexpr int kChDC = kDC / 64;             // 8 chunks of 64 columns cover the latent
 constexpr int kChunk = kBN * 128;           // bytes of one [64 tok x 64 col] bf16 chunk
-constexpr int kStages = 3;
-constexpr int kStageDC = kChDC * kChunk;    // 64 KB of latent chunks per stage
 constexpr int kM = 128;                     // head rows per MMA
 constexpr int kMaxPairs = 160;              // upper bound on clusters per launch
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P stays <= 256
+constexpr int kThreads = 384;               // 12 warps: see the role map in the kernel
 
-// Shared-memory map (offsets from a 1024-aligned base; identical in both CTAs so
-// that remote addresses map one to one).
-constexpr int kOffStage = 0;                           // kStages x 64 KB latent chunks
+constexpr int kStages = 3;                  // score CTA TMA ring depth (HBM stream)
+constexpr int kStagesO = 2;                 // output CTA ring depth (its loads hit L2)
+constexpr int kPBufs = 4;                   // P tiles in flight between the CTAs
+constexpr int kStageDC = kChDC * kChunk;    // 64 KB of latent chunks per stage
+constexpr int kSBufs = 3;                   // score accumulators in tensor memory
+constexpr int kPBytes = kM * 128;           // one bf16 P tile (128 heads x 64 tokens)
+constexpr int kRefBytes = kM * 4;           // per-row softmax reference sent with a tile
+constexpr uint32_t kPTxBytes = kPBytes + kRefBytes;
+
+// Shared-memory map (offsets from a 1024-aligned base).  Identical in both CTAs so
+// that a local offset names the same object in the peer.
+constexpr int kOffStage = 0;                           // kStages (score) / kStagesO (output) x 64 KB
 constexpr int kOffRope = kStages * kStageDC;           // score CTA: kStages x 8 KB RoPE chunks
-constexpr int kOffP = kStages * kStageDC;              // output CTA: 2 x 16 KB P tiles
-constexpr int kPBytes = kM * 128;
-constexpr int kOffAlpha = kOffP + 2 * kPBytes;         // output CTA: 2 x 128 fp32 row factors
-constexpr int kOffBar = kOffAlpha + 2 * kM * 4;
+constexpr int kOffX = kOffRope + kStages * kChunk;     // score CTA: reference exchange between groups
+constexpr int kOffP = kStagesO * kStageDC;             // output CTA: kPBufs P tiles
+constexpr int kOffRef = kOffP + kPBufs * kPBytes;      // output CTA: kPBufs x 128 references
+constexpr int kOffBar = (kOffX + kRefBytes > kOffRef + kPBufs * kRefBytes) ? kOffX + kRefBytes
+                                                                            : kOffRef + kPBufs * kRefBytes;
+static_assert(kOffP % 1024 == 0, "P tiles must sit on 1024-byte boundaries");
 enum : int {
-  kBarFull = 0,                     // [kStages] TMA landed
-  kBarEmpty = kBarFull + kStages,   // [kStages] stage consumed by this CTA's MMAs
-  kBarSFull = kBarEmpty + kStages,  // [2] score CTA: S buffer written
-  kBarSEmpty = kBarSFull + 2,       // [2] score CTA: S buffer read
-  kBarQReady = kBarSEmpty + 2,      // score CTA: query loaded into tensor memory
-  kBarPFree = kBarQReady + 1,       // [2] score CTA: output CTA released P tile
-  kBarPFull = kBarPFree + 2,        // [2] output CTA: P tile and factors written
-  kBarPvGo = kBarPFull + 2,         // output CTA: block may be multiplied
-  kBarODone = kBarPvGo + 1,         // [2] output CTA: PV of a block completed
-  kBarDrain = kBarODone + 2,        // MMA drain at teardown
+  kBarFull = 0,                       // [kStages] stage landed
+  kBarEmpty = kBarFull + kStages,     // [kStages] stage consumed by this CTA's MMAs
+  kBarSFull = kBarEmpty + kStages,    // [kSBufs] score: S buffer written
+  kBarSEmpty = kBarSFull + kSBufs,    // [kSBufs] score: S buffer read
+  kBarQReady = kBarSEmpty + kSBufs,   // score: query in tensor memory
+  kBarRefReady = kBarQReady + 1,      // [2] score: reference of a block published (per softmax group)
+  kBarPFree = kBarRefReady + 2,       // [kPBufs] score: output CTA released a P tile
+  kBarPFull = kBarPFree + kPBufs,     // [kPBufs] output: P tile + references landed (tx bytes)
+  kBarPvGo = kBarPFull + kPBufs,      // [kPBufs] output: block may be multiplied
+  kBarODone = kBarPvGo + kPBufs,      // [kPBufs] output: PV of a block completed
+  kBarDrain = kBarODone + kPBufs,     // MMA drain at teardown
   kNumBars = kBarDrain + 1,
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffMisc + 128;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
-static_assert(kOffRope + kStages * kChunk <= kOffP + 2 * kPBytes, "score CTA map");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 // tensor-memory columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0;     // score CTA: query, R/2 columns (bf16 pairs)
-constexpr uint32_t kColS = 320;   // score CTA: two 64-column S buffers
+constexpr uint32_t kColS = 320;   // score CTA: kSBufs 64-column S buffers (columns 320..511)
 // output CTA: O occupies columns [0, 512)
 
 struct Misc {                     // at kOffMisc
   uint32_t tmem;
   int abort;
-  int flag[2];                    // output CTA: block id + 1 of a block that rescaled
   long long lo, hi, cum0;
   int b0, len0;
 };
@@ -99,7 +118,7 @@ struct Args {
   int32_t* cum;                // workspace: [B + 1] first block of each sequence
   float* part_m;               // [slots][128] running max (log2 units)
   float* part_l;               // [slots][128] running sum
-  float* part_o;               // [slots][128][512] unnormalised output
+  float* part_o;               // [slots][512][128] unnormalised output, latent-column major
 };
 
 __device__ __forceinline__ int clamp_len(int n, int n_max) { return n < 0 ? 0 : (n > n_max ? n_max : n); }
@@ -213,8 +232,11 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table) {
   }
 }
 
-__global__ void __launch_bounds__(256, 1) decode_split_kernel(const __grid_constant__ CUtensorMap map,
-                                                              const Args a) {
+// Role map (12 warps).  Score CTA: warp 0 TMA, warp 1 S MMA, warp 2 run planning,
+// warps 4-7 softmax group A (even blocks), warps 8-11 softmax group B (odd blocks).
+// Output CTA: warp 0 TMA, warp 1 PV MMA, warps 4-7 correction + epilogue.
+__global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_constant__ CUtensorMap map,
+                                                                   const Args a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -231,18 +253,26 @@ __global__ void __launch_bounds__(256, 1) decode_split_kernel(const __grid_const
       mbar_init(bar_addr(sbase, kBarFull + i), 1);
       mbar_init(bar_addr(sbase, kBarEmpty + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(bar_addr(sbase, kBarSFull + i), 1);
       mbar_init(bar_addr(sbase, kBarSEmpty + i), 128);
+    }
+    for (int i = 0; i < 2; ++i) mbar_init(bar_addr(sbase, kBarRefReady + i), 128);
+    // Per-P-tile barriers: the output CTA's correction warps can run up to kPBufs-1
+    // blocks ahead of its MMA warp, so every per-block handshake there has one
+    // barrier per tile and never more than one phase outstanding.
+    for (int i = 0; i < kPBufs; ++i) {
       mbar_init(bar_addr(sbase, kBarPFree + i), 1);
-      mbar_init(bar_addr(sbase, kBarPFull + i), 128);
+      mbar_init(bar_addr(sbase, kBarPFull + i), 1);
+      mbar_init(bar_addr(sbase, kBarPvGo + i), 128);
       mbar_init(bar_addr(sbase, kBarODone + i), 1);
     }
     mbar_init(bar_addr(sbase, kBarQReady), 128);
-    mbar_init(bar_addr(sbase, kBarPvGo), 128);
     mbar_init(bar_addr(sbase, kBarDrain), 1);
     misc->abort = 0;
-    misc->flag[0] = misc->flag[1] = 0;
+    if (!score_cta) {  // the first kPBufs P tiles are expected before any is sent
+      for (int i = 0; i < kPBufs; ++i) mbar_arrive_expect_tx(bar_addr(sbase, kBarPFull + i), kPTxBytes);
+    }
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) tma_prefetch_desc(&map);
@@ -260,229 +290,291 @@ __global__ void __launch_bounds__(256, 1) decode_split_kernel(const __grid_const
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const int nload = score_cta ? nch : kChDC;
-      Cursor c;
-      c.start(*misc, a.seq_lens, a.N_max);
-      for (int k = 0; c.ok(); c.next(), ++k) {
-        const int st = k % kStages;
-        if (!mbar_wait(bar_addr(sbase, kBarEmpty + st), ((k / kStages) & 1) ^ 1, abort)) break;
-        mbar_arrive_expect_tx(bar_addr(sbase, kBarFull + st), nload * kChunk);
-        for (int ch = 0; ch < nload; ++ch) {
-          const uint32_t dst = ch < kChDC ? sbase + kOffStage + st * kStageDC + ch * kChunk
-                                          : sbase + kOffRope + st * kChunk;
-          tma_load_3d(dst, &map, bar_addr(sbase, kBarFull + st), ch * 64, c.t0(), c.b);
-        }
+    const uint32_t leader = elect_one();
+    const int nload = score_cta ? nch : kChDC;
+    const int nst = score_cta ? kStages : kStagesO;
+    Cursor c;
+    c.start(*misc, a.seq_lens, a.N_max);
+    // the score CTA's query goes out before the cache stream floods the memory system
+    if (score_cta && c.ok()) warp_wait(bar_addr(sbase, kBarQReady), 0, abort);
+    for (int k = 0; c.ok(); c.next(), ++k) {
+      const int st = k % nst;
+      if (!warp_wait(bar_addr(sbase, kBarEmpty + st), ((k / nst) & 1) ^ 1, abort)) break;
+      MLA_TRACE_POINT(k, score_cta ? 8 : 7);
+      mbar_arrive_expect_tx_if(leader, bar_addr(sbase, kBarFull + st), nload * kChunk);
+      for (int ch = 0; ch < nload; ++ch) {
+        const uint32_t dst = ch < kChDC ? sbase + kOffStage + st * kStageDC + ch * kChunk
+                                        : sbase + kOffRope + st * kChunk;
+        tma_load_3d_if(leader, dst, &map, bar_addr(sbase, kBarFull + st), ch * 64, c.t0(), c.b);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      Cursor c;
-      c.start(*misc, a.seq_lens, a.N_max);
-      if (score_cta) {
-        constexpr uint32_t idesc = idesc_bf16(kM, kBN, false, false);
-        int seg = 0;
-        for (int k = 0; c.ok(); c.next(), ++k) {
-          if (c.first()) {
-            if (!mbar_wait(bar_addr(sbase, kBarQReady), seg & 1, abort)) break;
-            ++seg;
-          }
-          const int st = k % kStages, sb = k & 1;
-          if (!mbar_wait(bar_addr(sbase, kBarFull + st), (k / kStages) & 1, abort)) break;
-          if (!mbar_wait(bar_addr(sbase, kBarSEmpty + sb), ((k >> 1) & 1) ^ 1, abort)) break;
-          tc_fence_after();
-          const uint32_t d = tmem + kColS + sb * kBN;
-          for (int ch = 0; ch < nch; ++ch) {
-            const uint32_t chunk = ch < kChDC ? sbase + kOffStage + st * kStageDC + ch * kChunk
-                                              : sbase + kOffRope + st * kChunk;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bdesc = sdesc_sw128(chunk + kk * 32, 16, 1024);
-              mma_ts(d, tmem + kColQ + ch * 32 + kk * 8, bdesc, idesc, (ch | kk) != 0);
-            }
-          }
-          tc_commit(bar_addr(sbase, kBarEmpty + st));
-          tc_commit(bar_addr(sbase, kBarSFull + sb));
-        }
-      } else {
-        constexpr uint32_t idesc = idesc_bf16(kM, 256, false, true);
-        for (int k = 0; c.ok(); c.next(), ++k) {
-          const int st = k % kStages, sb = k & 1;
-          if (!mbar_wait(bar_addr(sbase, kBarPvGo), k & 1, abort)) break;
-          if (!mbar_wait(bar_addr(sbase, kBarFull + st), (k / kStages) & 1, abort)) break;
-          tc_fence_after();
-          const uint32_t pa = sbase + kOffP + sb * kPBytes;
-          const uint32_t stage = sbase + kOffStage + st * kStageDC;
-          const bool acc0 = !c.first();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = sdesc_sw128(pa + kk * 32, 16, 1024);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const uint64_t bdesc = sdesc_sw128(stage + half * 4 * kChunk + kk * 16 * 128, kChunk, 1024);
-              mma_ss(tmem + half * 256, adesc, bdesc, idesc, (acc0 || kk > 0) ? 1u : 0u);
-            }
-          }
-          tc_commit(bar_addr(sbase, kBarEmpty + st));
-          tc_commit(bar_addr(sbase, kBarODone + sb));
-          tc_commit_mc(bar_addr(sbase, kBarPFree + sb), static_cast<uint16_t>(1u));  // to the score CTA
-        }
-      }
-      // drain: every MMA this thread issued has completed before teardown
-      tc_commit(bar_addr(sbase, kBarDrain));
-      mbar_wait(bar_addr(sbase, kBarDrain), 0, abort);
-    }
-  } else if (warp >= 4) {
-    const int r = threadIdx.x - 128;                       // head row == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(r & ~31) << 16;
+    const uint32_t leader = elect_one();
     Cursor c;
     c.start(*misc, a.seq_lens, a.N_max);
     if (score_cta) {
-      // ---------------------------------------------------------- softmax
-      float m_ref = 0.f, l = 0.f;
-      int k = 0;
-      for (; c.ok(); c.next(), ++k) {
+      // S = Q C^T: M = 128 heads, N = 64 tokens, A (the query) from tensor memory
+      constexpr uint32_t idesc = idesc_bf16(kM, kBN, false, false);
+      int seg = 0;
+      for (int k = 0; c.ok(); c.next(), ++k) {
         if (c.first()) {
-          // query of this sequence into tensor memory (rows >= H are zero)
-          const uint4* src = reinterpret_cast<const uint4*>(a.q_cat + (static_cast<long long>(c.b) * a.H + r) * a.R);
-          for (int j = 0; j < nch; ++j) {
-            uint32_t v[32];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              uint4 x = make_uint4(0u, 0u, 0u, 0u);
-              if (r < a.H) x = __ldg(src + j * 8 + u);
-              v[4 * u] = x.x;
-              v[4 * u + 1] = x.y;
-              v[4 * u + 2] = x.z;
-              v[4 * u + 3] = x.w;
-            }
-            tmem_st32(tmem + lane_off + kColQ + j * 32, v);
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(bar_addr(sbase, kBarQReady));
+          if (!warp_wait(bar_addr(sbase, kBarQReady), seg & 1, abort)) break;
+          ++seg;
         }
-        const int sb = k & 1;
-        if (!warp_wait(bar_addr(sbase, kBarSFull + sb), (k >> 1) & 1, abort)) break;
+        const int st = k % kStages, sb = k % kSBufs;
+        if (!warp_wait(bar_addr(sbase, kBarFull + st), (k / kStages) & 1, abort)) break;
+        if (!warp_wait(bar_addr(sbase, kBarSEmpty + sb), ((k / kSBufs) & 1) ^ 1, abort)) break;
+        MLA_TRACE_POINT(k, 0);
         tc_fence_after();
-        uint32_t sr[64];
-        tmem_ld64(tmem + lane_off + kColS + sb * kBN, sr);
-        tmem_wait_ld();
+        const uint32_t d = tmem + kColS + sb * kBN;
+        const uint32_t stage = sbase + kOffStage + st * kStageDC;
+#pragma unroll
+        for (int ch = 0; ch < kChDC; ++ch) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts_if(leader, d, tmem + kColQ + ch * 32 + kk * 8, sdesc_sw128(stage + ch * kChunk + kk * 32, 16, 1024),
+                      idesc, (ch | kk) != 0);
+        }
+        if (nch > kChDC) {  // the RoPE chunk
+          const uint32_t rope = sbase + kOffRope + st * kChunk;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts_if(leader, d, tmem + kColQ + kChDC * 32 + kk * 8, sdesc_sw128(rope + kk * 32, 16, 1024), idesc, 1u);
+        }
+        tc_commit_if(leader, bar_addr(sbase, kBarEmpty + st));
+        tc_commit_if(leader, bar_addr(sbase, kBarSFull + sb));
+        MLA_TRACE_POINT(k, 15);
+      }
+    } else {
+      // O += P C: M = 128 heads, N = 256 latent columns per MMA, both operands in smem
+      constexpr uint32_t idesc = idesc_bf16(kM, 256, false, true);
+      for (int k = 0; c.ok(); c.next(), ++k) {
+        const int st = k % kStagesO, pb = k % kPBufs;
+        if (!warp_wait(bar_addr(sbase, kBarPvGo + pb), (k / kPBufs) & 1, abort)) break;
+        MLA_TRACE_POINT(k, 5);
+        if (!warp_wait(bar_addr(sbase, kBarFull + st), (k / kStagesO) & 1, abort)) break;
+        MLA_TRACE_POINT(k, 6);
+        tc_fence_after();
+        const uint32_t pa = sbase + kOffP + pb * kPBytes;
+        const uint32_t stage = sbase + kOffStage + st * kStageDC;
+        const uint32_t acc0 = c.first() ? 0u : 1u;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t adesc = sdesc_sw128(pa + kk * 32, 16, 1024);
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+            mma_ss_if(leader, tmem + half * 256, adesc, sdesc_sw128(stage + half * 4 * kChunk + kk * 16 * 128, kChunk, 1024),
+                      idesc, acc0 | (kk > 0 ? 1u : 0u));
+        }
+        tc_commit_if(leader, bar_addr(sbase, kBarEmpty + st));
+        tc_commit_if(leader, bar_addr(sbase, kBarODone + pb));
+        tc_commit_mc_if(leader, bar_addr(sbase, kBarPFree + pb), static_cast<uint16_t>(1u));  // to the score CTA
+      }
+    }
+    // drain: every MMA this warp issued has completed before teardown
+    tc_commit_if(leader, bar_addr(sbase, kBarDrain));
+    warp_wait(bar_addr(sbase, kBarDrain), 0, abort);
+  } else if (warp >= 4 && score_cta) {
+    // ------------------------------------------------------------ softmax (two groups)
+    // Group g handles blocks k with k % 2 == g.  Consecutive blocks only share the
+    // per-row reference m: the group of block k reads block k-1's reference from
+    // shared memory, raises it when the block's maximum exceeds it by more than
+    // 2^8, publishes it for block k+1, then exponentiates and ships P while the
+    // other group works on the next block.
+    const int grp = (warp - 4) >> 2;
+    const int r = (threadIdx.x - 128) & 127;                    // head row == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(r & ~31) << 16;
+    float* ref_x = reinterpret_cast<float*>(gbase + kOffX);    // reference exchange between the groups
+    Cursor c;
+    c.start(*misc, a.seq_lens, a.N_max);
+    int k = 0, last_mine = -1;
+    for (; c.ok(); c.next(), ++k) {
+      if ((k & 1) != grp) continue;
+      last_mine = k;
+      if (c.first()) {
+        // the previous block's S product (other group, older query) must be finished
+        if (k > 0 && !warp_wait(bar_addr(sbase, kBarSFull + (k - 1) % kSBufs), ((k - 1) / kSBufs) & 1, abort)) break;
+        if (r == 0) MLA_TRACE_POINT(k, 9);
+        // query of this sequence into tensor memory (rows >= H are zero)
+        const uint4* src = reinterpret_cast<const uint4*>(a.q_cat + (static_cast<long long>(c.b) * a.H + r) * a.R);
+        for (int j0 = 0; j0 < nch; j0 += 3) {  // three 128-byte pieces of the row in flight at once
+          uint4 x[24];
+#pragma unroll
+          for (int u = 0; u < 24; ++u) {
+            const int j = j0 + (u >> 3);
+            x[u] = (r < a.H && j < nch) ? __ldg(src + j * 8 + (u & 7)) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int jj = 0; jj < 3; ++jj) {
+            if (j0 + jj < nch) {
+              uint32_t v[32];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                v[4 * u] = x[jj * 8 + u].x;
+                v[4 * u + 1] = x[jj * 8 + u].y;
+                v[4 * u + 2] = x[jj * 8 + u].z;
+                v[4 * u + 3] = x[jj * 8 + u].w;
+              }
+              tmem_st32(tmem + lane_off + kColQ + (j0 + jj) * 32, v);
+            }
+          }
+        }
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar_addr(sbase, kBarSEmpty + sb));
+        mbar_arrive(bar_addr(sbase, kBarQReady));
+        if (r == 0) MLA_TRACE_POINT(k, 10);
+      }
+      const int sbuf = k % kSBufs, pb = k % kPBufs;
+      if (!warp_wait(bar_addr(sbase, kBarSFull + sbuf), (k / kSBufs) & 1, abort)) break;
+      if (r == 0) MLA_TRACE_POINT(k, 1);
+      tc_fence_after();
+      uint32_t sr[64];
+      tmem_ld64(tmem + lane_off + kColS + sbuf * kBN, sr);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar_addr(sbase, kBarSEmpty + sbuf));
 
-        const int nv = c.rows();
-        float mloc = -INFINITY;
+      const int nv = c.rows();
+      if (nv < kBN) {
 #pragma unroll
-        for (int j = 0; j < kBN; ++j) {
-          const float x = j < nv ? __uint_as_float(sr[j]) * a.scale_log2 : -INFINITY;
-          sr[j] = __float_as_uint(x);
-          mloc = fmaxf(mloc, x);
-        }
-        float alpha = 1.f;
-        bool rescaled = false;
-        if (c.first()) {
-          m_ref = mloc;
-          l = 0.f;
-        } else if (mloc > m_ref + kRescaleThreshold) {
-          alpha = fast_exp2(m_ref - mloc);
-          m_ref = mloc;
-          l *= alpha;
-          rescaled = true;
-        }
-        uint32_t pk[32];
-        float lsum = 0.f;
+        for (int j = 0; j < kBN; ++j)
+          if (j >= nv) sr[j] = __float_as_uint(-INFINITY);
+      }
+      float mx[8];
 #pragma unroll
-        for (int j = 0; j < kBN; j += 2) {
-          const float p0 = fast_exp2(__uint_as_float(sr[j]) - m_ref);
-          const float p1 = fast_exp2(__uint_as_float(sr[j + 1]) - m_ref);
-          lsum += p0 + p1;
-          pk[j >> 1] = pack_bf16x2(p0, p1);
-        }
-        l += lsum;
-        if (!warp_wait(bar_addr(sbase, kBarPFree + sb), ((k >> 1) & 1) ^ 1, abort)) break;
-        // P row r into the output CTA's P tile (K-major, 128-byte swizzle)
-        const uint32_t prow = sbase + kOffP + sb * kPBytes + (r >> 3) * 1024 + (r & 7) * 128;
+      for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[i]);
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          st_cluster_v4(prow + ((cc ^ (r & 7)) << 4), 1u, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2],
-                        pk[4 * cc + 3]);
-        st_cluster_f32(sbase + kOffAlpha + sb * kM * 4 + r * 4, 1u, alpha);
-        if (__any_sync(0xffffffffu, rescaled) && lane == 0)
-          st_cluster_f32(sbase + kOffMisc + offsetof(Misc, flag) + sb * 4, 1u, __int_as_float(k + 1));
-        fence_proxy_async_cluster();
-        mbar_arrive_cluster(bar_addr(sbase, kBarPFull + sb), 1u);
-        if (c.last() && r < a.H) {
-          const long long slot = cluster_id_x() + c.b;
-          a.part_m[slot * kM + r] = m_ref;
-          a.part_l[slot * kM + r] = l;
+      for (int j = 8; j < kBN; ++j) mx[j & 7] = fmaxf(mx[j & 7], __uint_as_float(sr[j]));
+      const float mloc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * a.scale_log2;
+      // reference of block k-1 (published by the other group)
+      float m_ref;
+      if (k > 0 && !warp_wait(bar_addr(sbase, kBarRefReady + (grp ^ 1)), ((k - 1) >> 1) & 1, abort)) break;
+      if (c.first()) {
+        m_ref = mloc;
+      } else {
+        m_ref = ref_x[r];
+        if (mloc > m_ref + kRescaleThreshold) m_ref = mloc;
+      }
+      ref_x[r] = m_ref;  // for block k+1 (ordered by the arrive below)
+      mbar_arrive(bar_addr(sbase, kBarRefReady + grp));
+
+      uint32_t pk[32];
+      const float neg = -m_ref;
+#pragma unroll
+      for (int j = 0; j < kBN; j += 2) {
+        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[j]), a.scale_log2, neg));
+        const float p1 = fast_exp2(fmaf(__uint_as_float(sr[j + 1]), a.scale_log2, neg));
+        pk[j >> 1] = pack_bf16x2(p0, p1);
+      }
+      if (!warp_wait(bar_addr(sbase, kBarPFree + pb), ((k / kPBufs) & 1) ^ 1, abort)) break;
+      if (r == 0) MLA_TRACE_POINT(k, 2);
+      // P row r into the output CTA's P tile (K-major, 128-byte swizzle) and the row's
+      // reference; every store completes its bytes on the output CTA's P barrier
+      const uint32_t pbar = bar_addr(sbase, kBarPFull + pb);
+      const uint32_t prow = sbase + kOffP + pb * kPBytes + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+        st_async_v4(prow + ((cc ^ (r & 7)) << 4), pbar, 1u, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      st_async_b32(sbase + kOffRef + pb * kRefBytes + r * 4, pbar, 1u, __float_as_uint(m_ref));
+      if (r == 0) MLA_TRACE_POINT(k, 3);
+    }
+    // the output CTA has consumed this group's last tile (its release, an arrival
+    // into this CTA, has landed) before this CTA exits
+    if (last_mine >= 0)
+      warp_wait(bar_addr(sbase, kBarPFree + last_mine % kPBufs), (last_mine / kPBufs) & 1, abort);
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ output CTA: correction + epilogue
+    // Tracks the row maximum m (the references it receives) and the row sum l of the
+    // bf16 P tiles it multiplies, rescales O in place when a row's reference rose,
+    // and writes the unnormalised partial (m, l, O) at the end of each sequence run.
+    const int r = threadIdx.x - 128;
+    const uint32_t lane_off = static_cast<uint32_t>(r & ~31) << 16;
+    Cursor c;
+    c.start(*misc, a.seq_lens, a.N_max);
+    float m = 0.f, l = 0.f;
+    int k = 0;
+    for (; c.ok(); c.next(), ++k) {
+      const int pb = k % kPBufs, st = k % kStagesO;
+      if (!warp_wait<true>(bar_addr(sbase, kBarPFull + pb), (k / kPBufs) & 1, abort)) break;
+      if (r == 0) MLA_TRACE_POINT(k, 4);
+      const float ref = reinterpret_cast<const float*>(gbase + kOffRef + pb * kRefBytes)[r];
+      float alpha = 1.f;
+      if (!c.first()) alpha = fast_exp2(m - ref);
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        const int kp = k - 1;  // PV of the previous block has to be complete
+        if (!warp_wait(bar_addr(sbase, kBarODone + kp % kPBufs), (kp / kPBufs) & 1, abort)) break;
+        tc_fence_after();
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t v[64];
+          tmem_ld64(tmem + lane_off + cc * 64, v);
+          tmem_wait_ld();
+          uint32_t lo32[32], hi32[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            lo32[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+            hi32[j] = __float_as_uint(__uint_as_float(v[32 + j]) * alpha);
+          }
+          tmem_st32(tmem + lane_off + cc * 64, lo32);
+          tmem_st32(tmem + lane_off + cc * 64 + 32, hi32);
+        }
+        tmem_wait_st();
+      }
+      const int nv = c.rows();
+      if (nv < kBN) {
+        // rows past the end of the sequence must not carry NaN/Inf into P C.  Once PV
+        // of block k-2 is done the stage can only hold block k (or be loading it).
+        if (k >= 2 && !warp_wait(bar_addr(sbase, kBarODone + (k - 2) % kPBufs), ((k - 2) / kPBufs) & 1, abort)) break;
+        if (!warp_wait(bar_addr(sbase, kBarFull + st), (k / kStagesO) & 1, abort)) break;
+        uint8_t* stage = gbase + kOffStage + st * kStageDC;
+        const int npieces = (kBN - nv) * kChDC * 8;  // 16-byte pieces
+        for (int q = r; q < npieces; q += 128) {
+          const int row = nv + q / (kChDC * 8);
+          const int rem = q % (kChDC * 8);
+          const int ch = rem >> 3, piece = rem & 7;
+          *reinterpret_cast<uint4*>(stage + ch * kChunk + row * 128 + piece * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      // the output CTA's releases of the last two P tiles have landed before exit
-      for (int i = k - 2; i < k; ++i)
-        if (i >= 0) warp_wait(bar_addr(sbase, kBarPFree + (i & 1)), (i >> 1) & 1, abort);
-    } else {
-      // ---------------------------------------------------------- correction + epilogue
-      int k = 0;
-      for (; c.ok(); c.next(), ++k) {
-        const int sb = k & 1, st = k % kStages;
-        if (!warp_wait<true>(bar_addr(sbase, kBarPFull + sb), (k >> 1) & 1, abort)) break;
-        const bool need = !c.first() && misc->flag[sb] == k + 1;
-        if (need) {
-          const float alpha = reinterpret_cast<const float*>(gbase + kOffAlpha)[sb * kM + r];
-          const int kp = k - 1;  // PV of the previous block has to be complete
-          if (!warp_wait(bar_addr(sbase, kBarODone + (kp & 1)), (kp >> 1) & 1, abort)) break;
-          tc_fence_after();
-          for (int cc = 0; cc < 8; ++cc) {
-            uint32_t v[64];
-            tmem_ld64(tmem + lane_off + cc * 64, v);
-            tmem_wait_ld();
-            uint32_t lo32[32], hi32[32];
+      fence_proxy_async_cta();  // P arrived through st.async; zeroed rows through generic stores
+      tc_fence_before();
+      mbar_arrive(bar_addr(sbase, kBarPvGo + pb));
+      // off the critical path (the MMA only reads the tile too): the row sum of the
+      // P tile as stored, i.e. of the values the MMA multiplies
+      const uint8_t* prow = gbase + kOffP + pb * kPBytes + (r >> 3) * 1024 + (r & 7) * 128;
+      float ps = 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              lo32[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-              hi32[j] = __float_as_uint(__uint_as_float(v[32 + j]) * alpha);
-            }
-            tmem_st32(tmem + lane_off + cc * 64, lo32);
-            tmem_st32(tmem + lane_off + cc * 64 + 32, hi32);
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint4 v = *reinterpret_cast<const uint4*>(prow + cc * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ps += __uint_as_float(w[i] << 16) + __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+      l = c.first() ? ps : l * alpha + ps;
+      m = ref;
+      // this buffer's next tile (block k + kPBufs) is sent only after PV of block k
+      if (r == 0) mbar_arrive_expect_tx(bar_addr(sbase, kBarPFull + pb), kPTxBytes);
+      if (c.last()) {
+        if (!warp_wait(bar_addr(sbase, kBarODone + pb), (k / kPBufs) & 1, abort)) break;
+        if (r == 0) MLA_TRACE_POINT(k, 11);
+        tc_fence_after();
+        const long long slot = cluster_id_x() + c.b;
+        float* dst = a.part_o + slot * (kDC * kM) + r;  // [c][h]: a warp stores 128 contiguous bytes
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t v[64];
+          tmem_ld64(tmem + lane_off + cc * 64, v);
+          tmem_wait_ld();
+          if (r < a.H) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) dst[(cc * 64 + j) * kM] = __uint_as_float(v[j]);
           }
-          tmem_wait_st();
         }
-        const int nv = c.rows();
-        if (nv < kBN) {
-          // rows past the end of the sequence must not carry NaN/Inf into P C
-          if (!warp_wait(bar_addr(sbase, kBarFull + st), (k / kStages) & 1, abort)) break;
-          uint8_t* stage = gbase + kOffStage + st * kStageDC;
-          const int npieces = (kBN - nv) * kChDC * 8;  // 16-byte pieces
-          for (int q = r; q < npieces; q += 128) {
-            const int row = nv + q / (kChDC * 8);
-            const int rem = q % (kChDC * 8);
-            const int ch = rem >> 3, piece = rem & 7;
-            *reinterpret_cast<uint4*>(stage + ch * kChunk + row * 128 + piece * 16) = make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_cta();
+        if (r < a.H) {
+          a.part_m[slot * kM + r] = m;
+          a.part_l[slot * kM + r] = l;
         }
         tc_fence_before();
-        mbar_arrive(bar_addr(sbase, kBarPvGo));
-        if (c.last()) {
-          if (!warp_wait(bar_addr(sbase, kBarODone + sb), (k >> 1) & 1, abort)) break;
-          tc_fence_after();
-          const long long slot = cluster_id_x() + c.b;
-          float4* dst = reinterpret_cast<float4*>(a.part_o + (slot * kM + r) * kDC);
-          for (int cc = 0; cc < 8; ++cc) {
-            uint32_t v[64];
-            tmem_ld64(tmem + lane_off + cc * 64, v);
-            tmem_wait_ld();
-            if (r < a.H) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                dst[cc * 16 + j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                               __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-            }
-          }
-          tc_fence_before();
-        }
+        if (r == 0) MLA_TRACE_POINT(k, 12);
       }
     }
   }
@@ -498,44 +590,41 @@ __global__ void __launch_bounds__(256, 1) decode_split_kernel(const __grid_const
 }
 
 // Merge the partials of each sequence: M = max m_s, L = sum l_s 2^(m_s - M),
-// o = sum 2^(m_s - M) O_s / L, lse = (M + log2 L) ln 2.  One block per (head, b).
+// o = sum 2^(m_s - M) O_s / L, lse = (M + log2 L) ln 2.  One block per (32 latent
+// columns, sequence), one thread per head: partial reads are coalesced over heads.
 template <typename TOut>
 __global__ void __launch_bounds__(128) combine_kernel(const Args a, TOut* __restrict__ o_lat,
                                                       float* __restrict__ lse) {
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int cb32 = blockIdx.x, b = blockIdx.y, h = threadIdx.x;
+  if (h >= a.H) return;
   const long long T = a.hdr[0], P = a.hdr[1];
   const long long cb = a.cum[b], ce = a.cum[b + 1];
-  const int c0 = tid * 4;
-  TOut* out = o_lat + (static_cast<long long>(b) * a.H + h) * kDC + c0;
-  if (ce <= cb || P <= 0) {
+  TOut* out = o_lat + (static_cast<long long>(b) * a.H + h) * kDC + cb32 * 32;
+  float acc[32];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) st_elem(out + i, 0.f);
-    if (lse != nullptr && tid == 0) lse[static_cast<long long>(b) * a.H + h] = -INFINITY;
-    return;
+  for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+  float M = -INFINITY, L = 0.f;
+  if (ce > cb && P > 0) {
+    // run p covers blocks [p T / P, (p + 1) T / P); run of block g = ceil((g + 1) P / T) - 1
+    const long long p_first = ((cb + 1) * P + T - 1) / T - 1;
+    const long long p_last = (ce * P + T - 1) / T - 1;
+    for (long long p = p_first; p <= p_last; ++p) M = fmaxf(M, a.part_m[(p + b) * kM + h]);
+    for (long long p = p_first; p <= p_last; ++p) {
+      const long long slot = p + b;
+      const float w = exp2f(a.part_m[slot * kM + h] - M);
+      L += w * a.part_l[slot * kM + h];
+      const float* src = a.part_o + slot * (kDC * kM) + static_cast<long long>(cb32 * 32) * kM + h;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc[j] = fmaf(w, src[j * kM], acc[j]);
+    }
+    const float inv = 1.f / L;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[j] *= inv;
   }
-  // run p covers blocks [p T / P, (p + 1) T / P); run of block g = ceil((g + 1) P / T) - 1
-  const long long p_first = ((cb + 1) * P + T - 1) / T - 1;
-  const long long p_last = (ce * P + T - 1) / T - 1;
-  float M = -INFINITY;
-  for (long long p = p_first; p <= p_last; ++p) M = fmaxf(M, a.part_m[(p + b) * kM + h]);
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (long long p = p_first; p <= p_last; ++p) {
-    const long long slot = p + b;
-    const float w = exp2f(a.part_m[slot * kM + h] - M);
-    L += w * a.part_l[slot * kM + h];
-    const float4 v = *reinterpret_cast<const float4*>(a.part_o + (slot * kM + h) * kDC + c0);
-    acc.x += w * v.x;
-    acc.y += w * v.y;
-    acc.z += w * v.z;
-    acc.w += w * v.w;
-  }
-  const float inv = 1.f / L;
-  st_elem(out + 0, acc.x * inv);
-  st_elem(out + 1, acc.y * inv);
-  st_elem(out + 2, acc.z * inv);
-  st_elem(out + 3, acc.w * inv);
-  if (lse != nullptr && tid == 0) lse[static_cast<long long>(b) * a.H + h] = (M + log2f(L)) * 0.69314718055994531f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) st_elem(out + j, acc[j]);
+  if (lse != nullptr && cb32 == 0)
+    lse[static_cast<long long>(b) * a.H + h] = (ce > cb && P > 0) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
 // ---------------------------------------------------------------- host side
@@ -584,7 +673,7 @@ static int pairs_for_device() {
     return -1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * kMaxPairs, 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemAlloc;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -644,7 +733,7 @@ mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * npairs, 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemAlloc;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -656,7 +745,7 @@ mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel, map, a);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
-  dim3 grid(H, c.B);
+  dim3 grid(kDC / 32, c.B);
   combine_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(a, static_cast<__nv_bfloat16*>(o_lat), lse);
   return cuda_status(cudaGetLastError());
 }

@@ -55,6 +55,16 @@ __device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t nthreads, bo
   return out != 0;
 }
 
+// One lane of the (converged) warp: 1 for the elected lane, 0 for the others.
+// Single-thread tcgen05 / TMA instructions are issued by the whole warp with the
+// elected lane as predicate, so that their operands stay warp-uniform; issuing
+// them from a divergent lone thread costs far more issue cycles per instruction.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t e;
+  asm volatile("{\n\t.reg .pred p;\n\t.reg .b32 r;\n\telect.sync r|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+  return e;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
@@ -121,6 +131,21 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
 }
 
+// Predicated (elected-lane) forms, executed by the whole warp.
+__device__ __forceinline__ void mbar_arrive_expect_tx_if(uint32_t pred, uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t@q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n\t}"
+               :: "r"(pred), "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_if(uint32_t pred, uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                               int x, int y, int z) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+      "@q cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%1], [%2, {%3, %4, %5}], [%6];\n\t}"
+      :: "r"(pred), "r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
+}
+
 // 3-D tiled TMA load into this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y, int z) {
@@ -128,6 +153,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];"
       :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
+}
+
+// Prefetch a 3-D tile into L2 (no shared memory involved).
+__device__ __forceinline__ void tma_prefetch_3d_if(uint32_t pred, const CUtensorMap* map, int x, int y, int z) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+      "@q cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%1, {%2, %3, %4}];\n\t}"
+      :: "r"(pred), "l"(map), "r"(x), "r"(y), "r"(z) : "memory");
 }
 
 // Same, with an L2 cache-eviction policy.
@@ -177,6 +210,39 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t local, uint32_t cta, flo
       :: "r"(local), "r"(cta), "f"(v) : "memory");
 }
 
+// Asynchronous 16-byte store into the shared memory of cluster CTA `cta` (at the
+// offset `local` has in this CTA), completing 16 bytes of transaction count on that
+// CTA's barrier at offset `bar`.  Visibility comes with the barrier phase.
+__device__ __forceinline__ void st_async_v4(uint32_t local, uint32_t bar, uint32_t cta, uint32_t a, uint32_t b,
+                                            uint32_t c, uint32_t d) {
+  asm volatile(
+      "{\n\t.reg .b32 ra, rb;\n\tmapa.shared::cluster.u32 ra, %0, %2;\n\tmapa.shared::cluster.u32 rb, %1, %2;\n\t"
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [ra], {%3, %4, %5, %6}, [rb];\n\t}"
+      :: "r"(local), "r"(bar), "r"(cta), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void st_async_b32(uint32_t local, uint32_t bar, uint32_t cta, uint32_t v) {
+  asm volatile(
+      "{\n\t.reg .b32 ra, rb;\n\tmapa.shared::cluster.u32 ra, %0, %2;\n\tmapa.shared::cluster.u32 rb, %1, %2;\n\t"
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [ra], %3, [rb];\n\t}"
+      :: "r"(local), "r"(bar), "r"(cta), "r"(v) : "memory");
+}
+
+// Bulk copy (copy engine) of `bytes` from this CTA's shared memory to the same-offset
+// region `dst_local` of cluster CTA `cta`, completing bytes on that CTA's barrier.
+__device__ __forceinline__ void bulk_copy_to_cluster_if(uint32_t pred, uint32_t dst_local, uint32_t src, uint32_t bytes,
+                                                        uint32_t bar_local, uint32_t cta) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t.reg .b32 rd, rb;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+      "mapa.shared::cluster.u32 rd, %1, %5;\n\tmapa.shared::cluster.u32 rb, %4, %5;\n\t"
+      "@q cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [rd], [%2], %3, [rb];\n\t}"
+      :: "r"(pred), "r"(dst_local), "r"(src), "r"(bytes), "r"(bar_local), "r"(cta) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -210,6 +276,35 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
                :: "r"(bar), "h"(mask) : "memory");
+}
+
+// Elected-lane forms of commit and MMA (see elect_one).
+__device__ __forceinline__ void tc_commit_if(uint32_t pred, uint32_t bar) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+               "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}"
+               :: "r"(pred), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_mc_if(uint32_t pred, uint32_t bar, uint16_t mask) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+               "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%1], %2;\n\t}"
+               :: "r"(pred), "r"(bar), "h"(mask) : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_if(uint32_t pred, uint32_t d, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 q, %0, 0;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, p;\n\t}"
+      :: "r"(pred), "r"(d), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void mma_ss_if(uint32_t pred, uint32_t d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 q, %0, 0;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, p;\n\t}"
+      :: "r"(pred), "r"(d), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate).
