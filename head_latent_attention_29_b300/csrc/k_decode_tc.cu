@@ -157,12 +157,6 @@ struct Cursor {
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
 
-template <bool kCluster = false>
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  const bool ok = mbar_wait<kCluster>(bar, parity, abort);
-  return __all_sync(0xffffffffu, ok);
-}
-
 // Plan the run of this cluster: total blocks T, runs P = min(clusters, T), this
 // run's [lo, hi), and the sequence that holds block lo.  One warp.
 __device__ void plan_run(const Args& a, Misc* misc, bool write_table) {

@@ -1,0 +1,270 @@
+// Per-head batched GEMMs on the tensor cores (bf16 in, fp32 accumulate):
+//
+//   absorb_q : q_lat[b][h][c] = sum_d q_nope[b][h][d] W_UK[h][d][c]
+//              (0539edu.com sections 3.1 / 5.1: W_UK folded into the query)
+//   out_up   : o[b][h][d]     = sum_c o_lat[b][h][c] W_UV[h][d][c]
+//              (0539edu.com section 3.1: W_UV applied after attention)
+//
+// Both are computed transposed, D[m][n] = sum_k A_h[m][k] X_h[n][k], with the
+// weight dimension as M (128-row tiles) and the batch as N, so that the weights --
+// the bytes that dominate -- are streamed once through TMA and every MMA is a full
+// M = 128 tcgen05 instruction.  W_UK[h] ([d_k][d_c]) is an MN-major A operand,
+// W_UV[h] ([d_v][d_c]) a K-major one; the per-head activations are K-major B
+// operands read straight from [B][H][K] through a 3-D tensor map.
+#include "mla_internal.cuh"
+#include "mla_ptx.cuh"
+
+namespace mla {
+namespace hg {
+
+constexpr int kBM = 128;          // M rows per CTA
+constexpr int kBK = 64;           // K per stage (one 128-byte swizzle row)
+constexpr int kStagesHG = 4;
+constexpr int kThreadsHG = 128;
+
+struct GemmArgs {
+  int H, M, K;                    // per-head problem: M x K weights, K-long activations
+  int nb;                         // batch rows (N) in total
+  int n_tile;                     // N per CTA (multiple of 16, <= 256)
+  int stages;                     // ring depth (<= kStagesHG)
+  __nv_bfloat16* out;             // out[n * out_n_stride + h * out_h_stride + m]
+  long long out_n_stride, out_h_stride;
+  // RoPE of the query's position part (absorb only; d_r == 0 otherwise)
+  const __nv_bfloat16* q_rope;    // [B][H][d_r]
+  const int32_t* q_pos;           // [B]
+  int d_r;
+  int rope_col;                   // first output column of the rotated part (d_c)
+  RopeTable rope;                 // base^(-2i/d_r), i < d_r / 2
+};
+
+template <bool kAMN>
+__global__ void __launch_bounds__(kThreadsHG) head_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                                                               const __grid_constant__ CUtensorMap map_b,
+                                                               const GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  const int a_bytes = kBM * kBK * 2;               // 16 KB
+  const int b_bytes = g.n_tile * kBK * 2;          // n_tile x 128 B
+  const int stage_bytes = a_bytes + b_bytes;
+  const int nst = g.stages;
+  const uint32_t bars = sbase + nst * stage_bytes;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  volatile int* abort = &s_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int mt = blockIdx.x, h = blockIdx.y, nt = blockIdx.z;
+  const int m0 = mt * kBM, n0 = nt * g.n_tile;
+  const int nk = g.K / kBK;
+  const uint32_t tmem_cols = g.n_tile <= 32 ? 32 : (g.n_tile <= 64 ? 64 : (g.n_tile <= 128 ? 128 : 256));
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(bars + 8 * i, 1);                    // full
+      mbar_init(bars + 8 * (kStagesHG + i), 1);      // empty
+    }
+    mbar_init(bars + 8 * (2 * kStagesHG), 1);        // accumulator done
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&s_tmem), tmem_cols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    const uint32_t leader = elect_one();
+    for (int k = 0; k < nk; ++k) {
+      const int st = k % nst;
+      if (!warp_wait(bars + 8 * (kStagesHG + st), ((k / nst) & 1) ^ 1, abort)) break;
+      const uint32_t sa = sbase + st * stage_bytes, sb = sa + a_bytes, full = bars + 8 * st;
+      mbar_arrive_expect_tx_if(leader, full, stage_bytes);
+      if (kAMN) {
+        // W_UK rows h*K + [k*64, k*64+64), latent columns [m0, m0+128) as two 64-wide boxes
+        tma_load_2d_if(leader, sa, &map_a, full, m0, h * g.K + k * kBK);
+        tma_load_2d_if(leader, sa + a_bytes / 2, &map_a, full, m0 + 64, h * g.K + k * kBK);
+      } else {
+        // W_UV rows h*M + [m0, m0+128), columns [k*64, k*64+64)
+        tma_load_2d_if(leader, sa, &map_a, full, k * kBK, h * g.M + m0);
+      }
+      tma_load_3d_if(leader, sb, &map_b, full, k * kBK, h, n0);
+    }
+  } else if (warp == 1) {
+    const uint32_t leader = elect_one();
+    const uint32_t idesc = idesc_bf16(kBM, g.n_tile, kAMN, false);
+    for (int k = 0; k < nk; ++k) {
+      const int st = k % nst;
+      if (!warp_wait(bars + 8 * st, (k / nst) & 1, abort)) break;
+      tc_fence_after();
+      const uint32_t sa = sbase + st * stage_bytes, sb = sa + a_bytes;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ad = kAMN ? sdesc_sw128(sa + kk * 16 * 128, a_bytes / 2, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
+        mma_ss_if(leader, tmem, ad, sdesc_sw128(sb + kk * 32, 16, 1024), idesc, (k | kk) != 0);
+      }
+      tc_commit_if(leader, bars + 8 * (kStagesHG + st));
+    }
+    tc_commit_if(leader, bars + 8 * (2 * kStagesHG));
+  } else if (g.d_r > 0 && mt == 0) {
+    // warps 2-3 rotate the query's position part of this head for the CTA's rows
+    const int half = g.d_r / 2;
+    const int n_end = min(n0 + g.n_tile, g.nb);
+    for (int idx = threadIdx.x - 64; idx < (n_end - n0) * half; idx += 64) {
+      const int n = n0 + idx / half, j = idx % half;
+      float sn, cs;
+      rope_sincos(g.q_pos[n], g.rope.theta[j], &sn, &cs);
+      const __nv_bfloat16* qr = g.q_rope + (static_cast<long long>(n) * g.H + h) * g.d_r + 2 * j;
+      const float x0 = __bfloat162float(qr[0]), x1 = __bfloat162float(qr[1]);
+      __nv_bfloat16* dst = g.out + n * g.out_n_stride + h * g.out_h_stride + g.rope_col + 2 * j;
+      dst[0] = __float2bfloat16_rn(x0 * cs - x1 * sn);
+      dst[1] = __float2bfloat16_rn(x0 * sn + x1 * cs);
+    }
+  }
+  __syncwarp();
+
+  // epilogue: warp w holds rows 32w..32w+31 (TMEM lanes), columns = batch rows
+  const bool ok = warp_wait(bars + 8 * (2 * kStagesHG), 0, abort);
+  tc_fence_after();
+  if (ok) {
+    const int m = m0 + warp * 32 + (threadIdx.x & 31);
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    for (int c0 = 0; c0 < g.n_tile; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_off + c0, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int n = n0 + c0 + j;
+        if (n < g.nb && m < g.M) g.out[n * g.out_n_stride + h * g.out_h_stride + m] = __float2bfloat16_rn(__uint_as_float(v[j]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && s_abort) record_error(MLA_ERR_DEVICE_TIMEOUT, kSiteDecodeWait);
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+static bool map_2d(CUtensorMap* m, const void* p, uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [B][H][K] activations as a 3-D map (K, H, B) with a (64, 1, n_tile) box.
+static bool map_act(CUtensorMap* m, const void* p, uint64_t K, uint64_t H, uint64_t B, uint32_t n_tile) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {K, H, B};
+  const cuuint64_t strides[2] = {K * 2, H * K * 2};
+  const cuuint32_t box[3] = {64, 1, n_tile};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int n_tile_for(int B) {
+  int n = B > 256 ? 256 : B;
+  return (n + 15) / 16 * 16;
+}
+
+template <bool kAMN>
+static mla_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& g, int m_tiles, int n_tiles,
+                         cudaStream_t s) {
+  auto k = head_gemm_kernel<kAMN>;
+  const size_t smem = static_cast<size_t>(g.stages) * (kBM * kBK * 2 + g.n_tile * kBK * 2) + 8 * (2 * kStagesHG + 1) + 1024;
+  static size_t done[2] = {0, 0};
+  if (smem > done[kAMN ? 1 : 0]) {
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    done[kAMN ? 1 : 0] = smem;
+  }
+  dim3 grid(m_tiles, g.H, n_tiles);
+  k<<<grid, kThreadsHG, smem, s>>>(ma, mb, g);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace hg
+
+bool headgemm_absorb_supported(int32_t d_k, int32_t d_c, int32_t d_r) {
+  return d_k % 64 == 0 && d_c % 128 == 0 && d_r <= 128;
+}
+
+bool headgemm_out_up_supported(int32_t d_c, int32_t d_v) { return d_c % 64 == 0 && d_v % 128 == 0; }
+
+mla_status launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int32_t* q_pos, const void* w_uk,
+                              void* q_cat, int32_t B, int32_t H, int32_t d_k, int32_t d_c, int32_t d_r,
+                              float rope_base, cudaStream_t s) {
+  using namespace hg;
+  GemmArgs g = {};
+  g.H = H;
+  g.M = d_c;
+  g.K = d_k;
+  g.nb = B;
+  g.n_tile = n_tile_for(B);
+  g.stages = d_k / kBK < kStagesHG ? d_k / kBK : kStagesHG;
+  g.out = static_cast<__nv_bfloat16*>(q_cat);
+  g.out_h_stride = d_c + d_r;
+  g.out_n_stride = static_cast<long long>(H) * (d_c + d_r);
+  g.q_rope = static_cast<const __nv_bfloat16*>(q_rope);
+  g.q_pos = q_pos;
+  g.d_r = d_r;
+  g.rope_col = d_c;
+  g.rope = rope_table(d_r, rope_base);
+  CUtensorMap ma, mb;
+  if (!map_2d(&ma, w_uk, d_c, static_cast<uint64_t>(H) * d_k, 64, 64)) return MLA_ERR_CUDA;
+  if (!map_act(&mb, q_nope, d_k, H, B, g.n_tile)) return MLA_ERR_CUDA;
+  return launch<true>(ma, mb, g, d_c / kBM, (B + g.n_tile - 1) / g.n_tile, s);
+}
+
+mla_status launch_out_up_tc(const void* o_lat, const void* w_uv, void* o, int32_t B, int32_t H, int32_t d_c,
+                            int32_t d_v, cudaStream_t s) {
+  using namespace hg;
+  GemmArgs g = {};
+  g.H = H;
+  g.M = d_v;
+  g.K = d_c;
+  g.nb = B;
+  g.n_tile = n_tile_for(B);
+  g.stages = d_c / kBK < kStagesHG ? d_c / kBK : kStagesHG;
+  g.out = static_cast<__nv_bfloat16*>(o);
+  g.out_h_stride = d_v;
+  g.out_n_stride = static_cast<long long>(H) * d_v;
+  CUtensorMap ma, mb;
+  if (!map_2d(&ma, w_uv, d_c, static_cast<uint64_t>(H) * d_v, 64, 128)) return MLA_ERR_CUDA;
+  if (!map_act(&mb, o_lat, d_c, H, B, g.n_tile)) return MLA_ERR_CUDA;
+  return launch<false>(ma, mb, g, d_v / kBM, (B + g.n_tile - 1) / g.n_tile, s);
+}
+
+}  // namespace mla

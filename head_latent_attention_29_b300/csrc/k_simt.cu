@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(128) cache_append_kernel(T* __restrict__ cache
                                                            const T* __restrict__ c_kv, const T* __restrict__ k_r,
                                                            const int32_t* __restrict__ seq_idx,
                                                            const int32_t* __restrict__ pos, int32_t n_rows,
-                                                           double base, int vec_ok) {
+                                                           const RopeTable rope, int vec_ok) {
   for (int64_t i = blockIdx.x; i < n_rows; i += gridDim.x) {
     const int32_t b = seq_idx[i];
     const int32_t p = pos[i];
@@ -58,15 +58,14 @@ __global__ void __launch_bounds__(128) cache_append_kernel(T* __restrict__ cache
     } else {
       for (int c = threadIdx.x; c < d_c; c += blockDim.x) dst[c] = src[c];
     }
-    // rotate pairs (2j, 2j+1) by pos * base^(-2j/d_r); angle and rotation in fp64
+    // rotate pairs (2j, 2j+1) by pos * theta_j
     const T* kr = k_r + i * d_r;
     for (int j = threadIdx.x; j < d_r / 2; j += blockDim.x) {
-      const double theta = pow(base, -2.0 * j / d_r);
-      double sn, cs;
-      sincos(static_cast<double>(p) * theta, &sn, &cs);
-      const double x0 = ld_elem(kr + 2 * j), x1 = ld_elem(kr + 2 * j + 1);
-      st_elem(dst + d_c + 2 * j, static_cast<float>(x0 * cs - x1 * sn));
-      st_elem(dst + d_c + 2 * j + 1, static_cast<float>(x0 * sn + x1 * cs));
+      float sn, cs;
+      rope_sincos(p, rope.theta[j], &sn, &cs);
+      const float x0 = ld_elem(kr + 2 * j), x1 = ld_elem(kr + 2 * j + 1);
+      st_elem(dst + d_c + 2 * j, fmaf(x0, cs, -x1 * sn));
+      st_elem(dst + d_c + 2 * j + 1, fmaf(x0, sn, x1 * cs));
     }
   }
 }
@@ -81,12 +80,12 @@ mla_status launch_cache_append(const mla_cache& c, const void* c_kv, const void*
     cache_append_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
         static_cast<__nv_bfloat16*>(c.data), c.B, c.N_max, c.d_c, c.d_r, c.row_stride,
         static_cast<const __nv_bfloat16*>(c_kv), static_cast<const __nv_bfloat16*>(k_r), seq_idx, pos, T,
-        static_cast<double>(rope_base), vec_ok);
+        rope_table(c.d_r, rope_base), vec_ok);
   } else {
     cache_append_kernel<float><<<grid, 128, 0, s>>>(static_cast<float*>(c.data), c.B, c.N_max, c.d_c, c.d_r,
                                                     c.row_stride, static_cast<const float*>(c_kv),
                                                     static_cast<const float*>(k_r), seq_idx, pos, T,
-                                                    static_cast<double>(rope_base), vec_ok);
+                                                    rope_table(c.d_r, rope_base), vec_ok);
   }
   return cuda_status(cudaGetLastError());
 }
@@ -103,7 +102,7 @@ template <typename T>
 __global__ void __launch_bounds__(128) absorb_q_kernel(const T* __restrict__ q_nope, const T* __restrict__ q_rope,
                                                        const int32_t* __restrict__ q_pos,
                                                        const T* __restrict__ w_uk, T* __restrict__ q_cat, int B,
-                                                       int H, int d_k, int d_c, int d_r, double base) {
+                                                       int H, int d_k, int d_c, int d_r, const RopeTable rope) {
   extern __shared__ float qs[];  // [kAbsorbBatch][d_k]
   const int h = blockIdx.y;
   const int c = blockIdx.x * 128 + threadIdx.x;
@@ -135,14 +134,13 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(const T* __restrict__ q_n
     const int half = d_r / 2;
     for (int idx = threadIdx.x; idx < B * half; idx += blockDim.x) {
       const int b = idx / half, j = idx - b * half;
-      const double theta = pow(base, -2.0 * j / d_r);
-      double sn, cs;
-      sincos(static_cast<double>(q_pos[b]) * theta, &sn, &cs);
+      float sn, cs;
+      rope_sincos(q_pos[b], rope.theta[j], &sn, &cs);
       const T* qr = q_rope + (static_cast<int64_t>(b) * H + h) * d_r;
-      const double x0 = ld_elem(qr + 2 * j), x1 = ld_elem(qr + 2 * j + 1);
+      const float x0 = ld_elem(qr + 2 * j), x1 = ld_elem(qr + 2 * j + 1);
       T* dst = q_cat + (static_cast<int64_t>(b) * H + h) * R + d_c;
-      st_elem(dst + 2 * j, static_cast<float>(x0 * cs - x1 * sn));
-      st_elem(dst + 2 * j + 1, static_cast<float>(x0 * sn + x1 * cs));
+      st_elem(dst + 2 * j, fmaf(x0, cs, -x1 * sn));
+      st_elem(dst + 2 * j + 1, fmaf(x0, sn, x1 * cs));
     }
   }
 }
@@ -157,13 +155,13 @@ mla_status launch_absorb_q(const void* q_nope, const void* q_rope, const int32_t
     ensure_smem(reinterpret_cast<const void*>(k), smem);
     k<<<grid, 128, smem, s>>>(static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(q_rope),
                               q_pos, static_cast<const __nv_bfloat16*>(w_uk), static_cast<__nv_bfloat16*>(q_cat),
-                              B, H, d_k, d_c, d_r, static_cast<double>(rope_base));
+                              B, H, d_k, d_c, d_r, rope_table(d_r, rope_base));
   } else {
     auto k = absorb_q_kernel<float>;
     ensure_smem(reinterpret_cast<const void*>(k), smem);
     k<<<grid, 128, smem, s>>>(static_cast<const float*>(q_nope), static_cast<const float*>(q_rope), q_pos,
                               static_cast<const float*>(w_uk), static_cast<float*>(q_cat), B, H, d_k, d_c, d_r,
-                              static_cast<double>(rope_base));
+                              rope_table(d_r, rope_base));
   }
   return cuda_status(cudaGetLastError());
 }

@@ -2,4 +2,5 @@
 // so all sources are compiled together.
 #include "k_simt.cu"
 #include "k_decode_tc.cu"
+#include "k_headgemm.cu"
 #include "mla_api.cu"

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstddef>
+#include <cmath>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -35,6 +36,32 @@ __device__ __forceinline__ void st_elem(__nv_bfloat16* p, float v) { *p = __floa
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// RoPE frequencies theta_i = base^(-2i/d_r), i < d_r/2, computed once on the host in
+// double and passed by value to the kernels (d_r <= 128).
+struct RopeTable {
+  double theta[64];
+};
+
+inline RopeTable rope_table(int d_r, double base) {
+  RopeTable t = {};
+  for (int i = 0; i < d_r / 2 && i < 64; ++i) t.theta[i] = pow(base, -2.0 * i / d_r);
+  return t;
+}
+
+// sin/cos of the rotation angle pos * theta: the product and its reduction by 2 pi
+// (split into a head and a tail so that the reduction is exact to double precision
+// for the positions used here) are the only fp64 operations; sin/cos run in fp32
+// on an argument already in [-pi, pi].
+__device__ __forceinline__ void rope_sincos(int pos, double theta, float* s, float* c) {
+  constexpr double kTwoPi = 6.283185307179586232;
+  constexpr double kTwoPiLo = 2.4492935982947064e-16;
+  constexpr double kInvTwoPi = 0.15915494309189534561;
+  const double ang = static_cast<double>(pos) * theta;
+  const double q = rint(ang * kInvTwoPi);
+  const double red = fma(-q, kTwoPiLo, fma(-q, kTwoPi, ang));
+  sincosf(static_cast<float>(red), s, c);
+}
+
 inline mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 
 // ---- host launchers (one per kernel family), defined in the .cu files -------
@@ -47,6 +74,13 @@ mla_status launch_out_up(const void* o_lat, const void* w_uv, void* o, int32_t B
                          int32_t d_v, int32_t dtype, cudaStream_t s);
 mla_status launch_gate(const void* h, const void* w_g, void* o, int32_t B, int32_t d_model, int32_t width,
                        int32_t dtype, cudaStream_t s);
+bool headgemm_absorb_supported(int32_t d_k, int32_t d_c, int32_t d_r);
+bool headgemm_out_up_supported(int32_t d_c, int32_t d_v);
+mla_status launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int32_t* q_pos, const void* w_uk,
+                              void* q_cat, int32_t B, int32_t H, int32_t d_k, int32_t d_c, int32_t d_r,
+                              float rope_base, cudaStream_t s);
+mla_status launch_out_up_tc(const void* o_lat, const void* w_uv, void* o, int32_t B, int32_t H, int32_t d_c,
+                            int32_t d_v, cudaStream_t s);
 mla_status launch_decode_f32(const float* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
                              float scale, float* o_lat, float* lse, cudaStream_t s);
 

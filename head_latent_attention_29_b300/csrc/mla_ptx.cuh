@@ -126,6 +126,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Warp-collective bounded wait: every lane polls, the warp agrees on the outcome.
+template <bool kCluster = false>
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  const bool ok = mbar_wait<kCluster>(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
@@ -144,6 +151,15 @@ __device__ __forceinline__ void tma_load_3d_if(uint32_t pred, uint32_t dst, cons
       "@q cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%1], [%2, {%3, %4, %5}], [%6];\n\t}"
       :: "r"(pred), "r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_if(uint32_t pred, uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                               int x, int y) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+      "@q cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%1], [%2, {%3, %4}], [%5];\n\t}"
+      :: "r"(pred), "r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar) : "memory");
 }
 
 // 3-D tiled TMA load into this CTA's shared memory, completing on `bar`.

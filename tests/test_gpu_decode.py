@@ -207,3 +207,30 @@ def test_step_ragged_long_context_sampled(mla):
         check_bf16(o_lat[b], r_lat, f"o_lat ragged b={b} n={case.lens[b]}")
         check_bf16(o[b], r_o, f"o ragged b={b}")
         np.testing.assert_allclose(lse[b], r_lse, atol=2e-2, rtol=1e-3)
+
+
+# ---------------------------------------------------------------------------
+# Tensor-core per-head GEMMs: batch sizes that are not multiples of the tile and
+# batches spanning several N tiles
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("B", [1, 5, 40, 300])
+def test_absorb_q_batch_shapes(mla, B):
+    H, d_k, d_c, d_r = 16, 128, 512, 64
+    q_nope = W.bf16_bits(W.normal(21, "abs_q", (B, H, d_k)))
+    q_r = W.bf16_bits(W.normal(21, "abs_qr", (B, H, d_r)))
+    w_uk = W.bf16_bits(W.normal(21, "abs_w", (H, d_k, d_c), std=1 / math.sqrt(512)))
+    pos = (np.arange(B, dtype=np.int32) * 97) % 32768
+    q_cat = mla.absorb_q(to_device(q_nope, "bf16"), to_device(q_r, "bf16"), torch.from_numpy(pos).cuda(),
+                         to_device(w_uk, "bf16"))
+    ref = O.absorb_q(W.widen(q_nope, "bf16"), W.widen(q_r, "bf16"), pos, W.widen(w_uk, "bf16"), 1e4)
+    check_bf16(q_cat.float().cpu().numpy(), ref, f"q_cat B={B}")
+
+
+@pytest.mark.parametrize("B", [1, 5, 40, 300])
+def test_out_up_batch_shapes(mla, B):
+    H, d_c, d_v = 16, 512, 128
+    o_lat = W.bf16_bits(W.normal(22, "oup_o", (B, H, d_c)))
+    w_uv = W.bf16_bits(W.normal(22, "oup_w", (H, d_v, d_c), std=1 / math.sqrt(512)))
+    o = mla.out_up(to_device(o_lat, "bf16"), to_device(w_uv, "bf16"))
+    ref = O.out_up(W.widen(o_lat, "bf16"), W.widen(w_uv, "bf16"))
+    check_bf16(o.float().cpu().numpy(), ref, f"o B={B}")
