@@ -24,7 +24,7 @@ import torch
 
 __all__ = [
     "MlaError", "LatentCache", "lib", "cache_append", "absorb_q", "decode_workspace",
-    "decode_attn", "out_up", "gate", "get_device_error", "LIB_PATH",
+    "decode_attn", "decode_attn_noalloc", "out_up", "gate", "get_device_error", "LIB_PATH",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -68,6 +68,9 @@ _SIGS = {
     "mla_gate": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]),
     "mla_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+    "mla_decode_attn_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(_Cache), ctypes.c_void_p,
+                                               ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p]),
 }
 
 
@@ -197,6 +200,21 @@ def decode_attn(q_cat: torch.Tensor, cache: LatentCache, seq_lens: torch.Tensor,
     st = cache.struct()
     _check(lib().mla_decode_attn(_ptr(q_cat), ctypes.byref(st), _ptr(seq_lens), H, float(scale), _ptr(workspace),
                                  workspace.numel(), _ptr(out), _ptr(lse), _stream(q_cat)), "mla_decode_attn")
+    return out, lse
+
+
+def decode_attn_noalloc(q_cat: torch.Tensor, cache: LatentCache, seq_lens: torch.Tensor, scale: float,
+                        out: torch.Tensor, lse: torch.Tensor | None = None):
+    """Same result as decode_attn, for callers that cannot allocate device memory:
+    the split-KV scratch is a buffer built into the library (at most 32 sequences).
+    `out` (and `lse` if wanted) must be preallocated by the caller."""
+    _dev_tensor(q_cat, "q_cat", cache.dtype)
+    _dev_tensor(seq_lens, "seq_lens", torch.int32)
+    _dev_tensor(out, "out", cache.dtype)
+    H = q_cat.shape[1]
+    st = cache.struct()
+    _check(lib().mla_decode_attn_noalloc(_ptr(q_cat), ctypes.byref(st), _ptr(seq_lens), H, float(scale), _ptr(out),
+                                         _ptr(lse), _stream(q_cat)), "mla_decode_attn_noalloc")
     return out, lse
 
 

@@ -643,10 +643,10 @@ struct WsLayout {
   size_t hdr, cum, m, l, o, total;
 };
 
-static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-static WsLayout ws_layout(int B) {
-  WsLayout w;
+constexpr WsLayout ws_layout(int B) {
+  WsLayout w = {};
   const size_t slots = static_cast<size_t>(kMaxPairs) + static_cast<size_t>(B);
   w.hdr = 0;
   w.cum = 256;

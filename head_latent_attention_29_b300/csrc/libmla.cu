@@ -4,3 +4,4 @@
 #include "k_decode_tc.cu"
 #include "k_headgemm.cu"
 #include "mla_api.cu"
+#include "mla_noalloc.cu"

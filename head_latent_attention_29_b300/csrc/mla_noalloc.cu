@@ -1,0 +1,61 @@
+// Allocation-free decode attention.
+//
+// Some callers cannot allocate device memory at the moment they need attention:
+// code running inside a CUDA-graph replay or a capture that forbids new
+// allocations, custom allocators that are not reentrant, or embedders that only
+// own input/output buffers handed to them by a host framework.  For them
+// mla_decode_attn_noalloc runs the same tensor-core decode kernels as
+// mla_decode_attn, but takes its split-KV scratch from a buffer that is part of
+// the library image itself (a file-scope device array), so the call allocates
+// nothing.
+//
+// The buffer holds the workspace of a batch of up to kNoAllocMaxBatch sequences
+// (about 50 MB).  Every GPU that loads the library keeps it until the process
+// exits.  All calls on a device share it, so calls whose kernels could overlap on
+// the GPU (different streams without ordering between them) race on it.  The
+// kernels overwrite every scratch word they later read (run table, partial
+// maxima, sums and outputs), so nothing has to be cleared between calls.
+#include <mutex>
+
+#include "mla_internal.cuh"
+
+namespace mla {
+
+constexpr int kNoAllocMaxBatch = 32;
+constexpr size_t kNoAllocScratchBytes = dtc::ws_layout(kNoAllocMaxBatch).total;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch buffer for the current device, looked up once per
+// device (host code may not use the symbol itself as a device pointer).
+static mla_status noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* ptr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MLA_ERR_CUDA;
+    ptr[dev] = p;
+  }
+  *out = ptr[dev];
+  return MLA_OK;
+}
+
+}  // namespace mla
+
+extern "C" {
+
+MLA_API mla_status mla_decode_attn_noalloc(const void* q_cat, const mla_cache* cache, const int32_t* seq_lens,
+                                           int32_t H, float scale, void* o_lat, float* lse, void* stream) {
+  if (cache == nullptr || q_cat == nullptr || seq_lens == nullptr || o_lat == nullptr) return MLA_ERR_INVALID_ARG;
+  if (cache->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (cache->B > mla::kNoAllocMaxBatch) return MLA_ERR_WORKSPACE;  // beyond the built-in scratch
+  void* ws = nullptr;
+  const mla_status st = mla::noalloc_scratch(&ws);
+  if (st != MLA_OK) return st;
+  return mla_decode_attn(q_cat, cache, seq_lens, H, scale, ws, mla::kNoAllocScratchBytes, o_lat, lse, stream);
+}
+
+}  // extern "C"

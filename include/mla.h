@@ -178,6 +178,27 @@ MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, 
                             int32_t width, int32_t dtype, void* stream);
 
 /*
+ * mla_decode_attn_noalloc -- mla_decode_attn for callers that cannot allocate.
+ *   (No counterpart on the pages this library restates: it is a deployment aid.)
+ *   Some callers cannot hand the library a workspace: code that runs while new
+ *   device allocations are not allowed (inside graph capture or replay, or under an
+ *   allocator that cannot be re-entered) or embedders that only own the input and
+ *   output buffers.  This entry point computes exactly what mla_decode_attn does,
+ *   with the same kernels, but takes the split-KV scratch from a buffer built into
+ *   the library (about 50 MB per GPU that loads the library, held until the
+ *   process exits), so it allocates nothing.
+ *   Arguments are those of mla_decode_attn minus the workspace.  Limits: bf16 cache
+ *   only (MLA_ERR_UNSUPPORTED otherwise) and at most 32 sequences (cache->B > 32
+ *   returns MLA_ERR_WORKSPACE).  The first call on a device looks up the buffer's
+ *   device address; make that first call before any stream capture.  All calls on
+ *   a device share the one buffer: calls whose work could overlap on the GPU
+ *   (unordered streams) race on it and must be serialised by the caller.  Nothing
+ *   in the buffer needs clearing between calls.
+ */
+MLA_API mla_status mla_decode_attn_noalloc(const void* q_cat, const mla_cache* cache, const int32_t* seq_lens,
+                                           int32_t H, float scale, void* o_lat, float* lse, void* stream);
+
+/*
  * mla_get_device_error -- wait for the device, then read and clear the device
  * error word written by the kernels of this library on the current device.
  * Returns MLA_OK if no kernel recorded an error since the last call, otherwise
