@@ -41,7 +41,7 @@ import numpy as np  # noqa: E402
 
 import mla_workloads as W  # noqa: E402
 
-ROTATE = 4  # cache copies rotated between steps
+ROTATE = 4  # default number of cache copies rotated between steps
 
 THROTTLE_BITS = {
     0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
@@ -60,61 +60,98 @@ def _peaks():
 
 # ---------------------------------------------------------------- clocks (NVML)
 class ClockSampler:
+    """SM clock and clock-event reasons during the timed region: NVML when the
+    Python module is present, else an nvidia-smi sampling subprocess; the GPU is
+    selected by UUID (NVML ignores CUDA_VISIBLE_DEVICES)."""
+
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+
     def __init__(self, device_index: int, period_s: float = 0.02):
         self.samples, self.reasons, self.max_mhz = [], 0, None
         self._stop = threading.Event()
         self._period = period_s
-        self._dev = device_index
-        self._ok = False
+        self._mode = None
         self.error = None
+        self._uuid = None
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(device_index).uuid)
+            self._uuid = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception as e:
+            self.error = repr(e)[:200]
         try:
             import pynvml
-            import torch
             pynvml.nvmlInit()
             self._nv = pynvml
-            # NVML numbers GPUs without regard to CUDA_VISIBLE_DEVICES: find ours by UUID
-            try:
-                uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-                self._h = pynvml.nvmlDeviceGetHandleByUUID(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
-            except Exception:
-                self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self._h = pynvml.nvmlDeviceGetHandleByUUID(self._uuid) if self._uuid else \
+                pynvml.nvmlDeviceGetHandleByIndex(device_index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
             self._reasons_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
                 getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
-            self._ok = True
-        except Exception as e:  # reported in the JSON line
+            self._mode = "nvml"
+        except Exception as e:
             self.error = repr(e)[:200]
-            self._ok = False
+            import shutil
+            if shutil.which("nvidia-smi") and self._uuid:
+                self._mode = "smi"
 
-    def _run(self):
+    def _run_nvml(self):
         while not self._stop.is_set():
             try:
                 self.samples.append(self._nv.nvmlDeviceGetClockInfo(self._h, self._nv.NVML_CLOCK_SM))
-            except Exception as e:
-                self.error = repr(e)[:200]
-            try:
                 self.reasons |= int(self._reasons_fn(self._h))
             except Exception as e:
                 self.error = repr(e)[:200]
             time.sleep(self._period)
 
     def __enter__(self):
-        if self._ok:
-            self._t = threading.Thread(target=self._run, daemon=True)
+        if self._mode == "nvml":
+            self._t = threading.Thread(target=self._run_nvml, daemon=True)
             self._t.start()
+        elif self._mode == "smi":
+            import subprocess
+            self._p = subprocess.Popen(["nvidia-smi", "-i", self._uuid, f"--query-gpu={self.SMI_FIELDS}",
+                                        "--format=csv,noheader,nounits", f"-lms={int(self._period * 1000)}"],
+                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         return self
 
     def __exit__(self, *exc):
-        if self._ok:
+        if self._mode == "nvml":
             self._stop.set()
             self._t.join()
+        elif self._mode == "smi":
+            self._p.terminate()
+            out, _ = self._p.communicate(timeout=10)
+            self._smi_lines = out.strip().splitlines()
+            self._parse_smi()
+
+    def _parse_smi(self):
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        self._smi_reasons = set()
+        for line in self._smi_lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                self.samples.append(float(f[0]))
+                self.max_mhz = float(f[1])
+            except ValueError:
+                continue
+            for name, val in zip(names[1:], f[3:7]):
+                if val.lower() in ("active", "1", "yes"):
+                    self._smi_reasons.add(name)
 
     def summary(self):
-        if not self._ok or not self.samples:
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"], "error": self.error}
-        names = [n for bit, n in THROTTLE_BITS.items() if self.reasons & bit]
+        if self._mode == "nvml":
+            names = [n for bit, n in THROTTLE_BITS.items() if self.reasons & bit]
+        else:
+            names = sorted(self._smi_reasons)
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": names,
-                "samples": len(self.samples)}
+                "samples": len(self.samples), "source": self._mode}
 
 
 # ---------------------------------------------------------------- workload
@@ -130,7 +167,7 @@ class DeviceWorkload:
     """Resident inputs of one replica: ROTATE latent caches, each with a captured
     decode-step graph, shared weights and the step's pinned host inputs."""
 
-    def __init__(self, name: str, seed: int, device):
+    def __init__(self, name: str, seed: int, device, rotate: int = ROTATE):
         import torch
         import head_latent_attention_29_b300 as mla
         from head_latent_attention_29_b300.step import DecodeStep
@@ -159,8 +196,9 @@ class DeviceWorkload:
             idx = torch.full((n,), b, dtype=torch.int32, device=device)
             pos = torch.arange(n, dtype=torch.int32, device=device)
             mla.cache_append(c0, up(c), up(k) if d_r else None, idx, pos, rb)
+        self.rotate = rotate
         caches = [c0] + [mla.LatentCache(B, N_max, d_c, d_r, dtype=bf, device=device, data=c0.data.clone())
-                         for _ in range(ROTATE - 1)]
+                         for _ in range(rotate - 1)]
         w_uk, w_uv = W.up_weights(cfg, seed)
         w_uk, w_uv = up(w_uk), up(w_uv)
         self.gated = d_r == 0 and "d_model" in cfg
@@ -196,12 +234,12 @@ class DeviceWorkload:
         s0 = self.steps[0]
         with torch.cuda.graph(self.attn_graph):
             for i in range(10):
-                st = self.steps[i % ROTATE]
+                st = self.steps[i % rotate]
                 mla.decode_attn(st.q_cat, st.cache, seq_lens, cfg["scale"], st.ws, st.o_lat, st.lse)
         self.kernels_per_step = s0.kernels_per_step
 
     def step(self, i: int):
-        self.steps[i % ROTATE].replay()
+        self.steps[i % self.rotate].replay()
 
 
 def run_b300(args, rank, world, device):
@@ -209,7 +247,7 @@ def run_b300(args, rank, world, device):
     import torch.distributed as dist
 
     torch.cuda.set_device(device)
-    wl = DeviceWorkload(args.workload, args.seed + rank, device)
+    wl = DeviceWorkload(args.workload, args.seed + rank, device, args.rotate)
     cfg = wl.cfg
     stream = torch.cuda.current_stream(device)
 
@@ -257,12 +295,12 @@ def run_b300(args, rank, world, device):
     # ---- end to end: pinned inputs in, result out, host waits for every step
     n_e2e = max(20, min(args.steps // 10, 2000))
     for i in range(3):
-        wl.e2e[i % ROTATE].replay()
+        wl.e2e[i % wl.rotate].replay()
     torch.cuda.synchronize(device)
     barrier()
     t0 = time.perf_counter()
     for i in range(n_e2e):
-        wl.e2e[i % ROTATE].replay()
+        wl.e2e[i % wl.rotate].replay()
         torch.cuda.current_stream(device).synchronize()
     barrier()
     e2e_s = (time.perf_counter() - t0) / n_e2e
@@ -298,7 +336,7 @@ def run_b300(args, rank, world, device):
             "workload": args.workload, "B": cfg["B"], "H": cfg["H"], "d_c": cfg["d_c"], "d_r": cfg["d_r"],
             "d_k": cfg["d_k"], "d_v": cfg["d_v"], "tokens_cached": int(np.sum(wl.lens)),
             "parallelism": f"replicas x{world}",
-            "l2": f"{ROTATE} rotating cache copies ({ROTATE * bytes_attn / 1e6:.0f} MB > 126 MB L2)",
+            "l2": f"{wl.rotate} rotating cache copies ({wl.rotate * bytes_attn / 1e6:.0f} MB vs 126 MB L2)",
             "step": "append+absorb_q+decode_attn(split+combine)+out_up" + ("+gate" if wl.gated else ""),
         },
         "gpu_launches": wl.kernels_per_step * args.steps,
@@ -420,6 +458,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rotate", type=int, default=ROTATE, help="cache copies rotated between steps (>= 1)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
