@@ -585,40 +585,82 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 
 // Merge the partials of each sequence: M = max m_s, L = sum l_s 2^(m_s - M),
 // o = sum 2^(m_s - M) O_s / L, lse = (M + log2 L) ln 2.  One block per (32 latent
-// columns, sequence), one thread per head: partial reads are coalesced over heads.
-template <typename TOut>
-__global__ void __launch_bounds__(128) combine_kernel(const Args a, TOut* __restrict__ o_lat,
+// columns, sequence); thread t owns heads 4(t/4)..+3 and columns 8(t%4)..+7, so
+// every partial read is a 16-byte load and a warp reads 4 runs of 128 contiguous
+// bytes.  The merged tile is staged in shared memory ([head][column], padded rows)
+// and written out as 64 contiguous bytes per (sequence, head).
+__global__ void __launch_bounds__(128) combine_kernel(const Args a, __nv_bfloat16* __restrict__ o_lat,
                                                       float* __restrict__ lse) {
-  const int cb32 = blockIdx.x, b = blockIdx.y, h = threadIdx.x;
-  if (h >= a.H) return;
+  constexpr int kPitch = 40;  // staged row: 32 bf16 columns + 16 bytes of padding
+  __shared__ __align__(16) __nv_bfloat16 s_o[kM * kPitch];
+  const int cb32 = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+  const int h0 = (t >> 2) * 4, cq = t & 3;
   const long long T = a.hdr[0], P = a.hdr[1];
   const long long cb = a.cum[b], ce = a.cum[b + 1];
-  TOut* out = o_lat + (static_cast<long long>(b) * a.H + h) * kDC + cb32 * 32;
-  float acc[32];
+  float acc[8][4];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-  float M = -INFINITY, L = 0.f;
-  if (ce > cb && P > 0) {
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
+  float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, L[4] = {0.f, 0.f, 0.f, 0.f};
+  const bool any = ce > cb && P > 0;
+  if (any) {
     // run p covers blocks [p T / P, (p + 1) T / P); run of block g = ceil((g + 1) P / T) - 1
     const long long p_first = ((cb + 1) * P + T - 1) / T - 1;
     const long long p_last = (ce * P + T - 1) / T - 1;
-    for (long long p = p_first; p <= p_last; ++p) M = fmaxf(M, a.part_m[(p + b) * kM + h]);
+    for (long long p = p_first; p <= p_last; ++p) {
+      const float4 m = *reinterpret_cast<const float4*>(a.part_m + (p + b) * kM + h0);
+      M[0] = fmaxf(M[0], m.x);
+      M[1] = fmaxf(M[1], m.y);
+      M[2] = fmaxf(M[2], m.z);
+      M[3] = fmaxf(M[3], m.w);
+    }
     for (long long p = p_first; p <= p_last; ++p) {
       const long long slot = p + b;
-      const float w = exp2f(a.part_m[slot * kM + h] - M);
-      L += w * a.part_l[slot * kM + h];
-      const float* src = a.part_o + slot * (kDC * kM) + static_cast<long long>(cb32 * 32) * kM + h;
+      const float4 m = *reinterpret_cast<const float4*>(a.part_m + slot * kM + h0);
+      const float4 l = *reinterpret_cast<const float4*>(a.part_l + slot * kM + h0);
+      const float* src = a.part_o + slot * (kDC * kM) + static_cast<long long>(cb32 * 32 + cq * 8) * kM + h0;
+      float4 v[8];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = fmaf(w, src[j * kM], acc[j]);
+      for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const float4*>(src + j * kM);
+      const float w[4] = {exp2f(m.x - M[0]), exp2f(m.y - M[1]), exp2f(m.z - M[2]), exp2f(m.w - M[3])};
+      L[0] = fmaf(w[0], l.x, L[0]);
+      L[1] = fmaf(w[1], l.y, L[1]);
+      L[2] = fmaf(w[2], l.z, L[2]);
+      L[3] = fmaf(w[3], l.w, L[3]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc[j][0] = fmaf(w[0], v[j].x, acc[j][0]);
+        acc[j][1] = fmaf(w[1], v[j].y, acc[j][1]);
+        acc[j][2] = fmaf(w[2], v[j].z, acc[j][2]);
+        acc[j][3] = fmaf(w[3], v[j].w, acc[j][3]);
+      }
     }
-    const float inv = 1.f / L;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) acc[j] *= inv;
   }
 #pragma unroll
-  for (int j = 0; j < 32; ++j) st_elem(out + j, acc[j]);
-  if (lse != nullptr && cb32 == 0)
-    lse[static_cast<long long>(b) * a.H + h] = (ce > cb && P > 0) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  for (int i = 0; i < 4; ++i) {
+    const float inv = any ? 1.f / L[i] : 0.f;
+    uint4 pk;
+    pk.x = pack_bf16x2(acc[0][i] * inv, acc[1][i] * inv);
+    pk.y = pack_bf16x2(acc[2][i] * inv, acc[3][i] * inv);
+    pk.z = pack_bf16x2(acc[4][i] * inv, acc[5][i] * inv);
+    pk.w = pack_bf16x2(acc[6][i] * inv, acc[7][i] * inv);
+    *reinterpret_cast<uint4*>(s_o + (h0 + i) * kPitch + cq * 8) = pk;
+  }
+  if (lse != nullptr && cb32 == 0 && cq == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (h0 + i < a.H)
+        lse[static_cast<long long>(b) * a.H + h0 + i] = any ? (M[i] + log2f(L[i])) * 0.69314718055994531f : -INFINITY;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int id = k * 128 + t, row = id >> 2, q = id & 3;
+    if (row < a.H)
+      *reinterpret_cast<uint4*>(o_lat + (static_cast<long long>(b) * a.H + row) * kDC + cb32 * 32 + q * 8) =
+          *reinterpret_cast<const uint4*>(s_o + row * kPitch + q * 8);
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -740,7 +782,7 @@ mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t
   cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel, map, a);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   dim3 grid(kDC / 32, c.B);
-  combine_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(a, static_cast<__nv_bfloat16*>(o_lat), lse);
+  combine_kernel<<<grid, 128, 0, s>>>(a, static_cast<__nv_bfloat16*>(o_lat), lse);
   return cuda_status(cudaGetLastError());
 }
 

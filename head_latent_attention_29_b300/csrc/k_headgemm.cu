@@ -19,7 +19,8 @@ namespace hg {
 
 constexpr int kBM = 128;          // M rows per CTA
 constexpr int kBK = 64;           // K per stage (one 128-byte swizzle row)
-constexpr int kStagesHG = 4;
+constexpr int kStagesHG = 8;         // a whole K = 512 in flight
+constexpr int kSmemBudgetHG = 200 * 1024;
 constexpr int kThreadsHG = 128;
 
 struct GemmArgs {
@@ -109,19 +110,37 @@ __global__ void __launch_bounds__(kThreadsHG) head_gemm_kernel(const __grid_cons
       tc_commit_if(leader, bars + 8 * (kStagesHG + st));
     }
     tc_commit_if(leader, bars + 8 * (2 * kStagesHG));
-  } else if (g.d_r > 0 && mt == 0) {
-    // warps 2-3 rotate the query's position part of this head for the CTA's rows
+  } else if (g.d_r > 0) {
+    // warps 2-3 of every m-tile CTA of this head rotate a share of the query's
+    // position part (rows n0.., pairs j); the loads of four items are issued
+    // before any of them is used
     const int half = g.d_r / 2;
-    const int n_end = min(n0 + g.n_tile, g.nb);
-    for (int idx = threadIdx.x - 64; idx < (n_end - n0) * half; idx += 64) {
-      const int n = n0 + idx / half, j = idx % half;
-      float sn, cs;
-      rope_sincos(g.q_pos[n], g.rope.theta[j], &sn, &cs);
-      const __nv_bfloat16* qr = g.q_rope + (static_cast<long long>(n) * g.H + h) * g.d_r + 2 * j;
-      const float x0 = __bfloat162float(qr[0]), x1 = __bfloat162float(qr[1]);
-      __nv_bfloat16* dst = g.out + n * g.out_n_stride + h * g.out_h_stride + g.rope_col + 2 * j;
-      dst[0] = __float2bfloat16_rn(x0 * cs - x1 * sn);
-      dst[1] = __float2bfloat16_rn(x0 * sn + x1 * cs);
+    const int total = (min(n0 + g.n_tile, g.nb) - n0) * half;
+    const int stride = 64 * gridDim.x;
+    for (int base = mt * 64 + threadIdx.x - 64; base < total; base += 4 * stride) {
+      int pos[4];
+      uint32_t x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = base + u * stride;
+        if (idx < total) {
+          const int n = n0 + idx / half, j = idx % half;
+          pos[u] = g.q_pos[n];
+          x[u] = *reinterpret_cast<const uint32_t*>(g.q_rope + (static_cast<long long>(n) * g.H + h) * g.d_r + 2 * j);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = base + u * stride;
+        if (idx < total) {
+          const int n = n0 + idx / half, j = idx % half;
+          float sn, cs;
+          rope_sincos(pos[u], g.rope.theta[j], &sn, &cs);
+          const float x0 = __uint_as_float(x[u] << 16), x1 = __uint_as_float(x[u] & 0xFFFF0000u);
+          *reinterpret_cast<uint32_t*>(g.out + n * g.out_n_stride + h * g.out_h_stride + g.rope_col + 2 * j) =
+              pack_bf16x2(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+        }
+      }
     }
   }
   __syncwarp();
@@ -199,6 +218,15 @@ static int n_tile_for(int B) {
   return (n + 15) / 16 * 16;
 }
 
+// Ring depth: every K step of the tile in flight when shared memory allows.
+static int stages_for(int nk, int n_tile) {
+  const int per_stage = kBM * kBK * 2 + n_tile * kBK * 2;
+  int st = kSmemBudgetHG / per_stage;
+  if (st > kStagesHG) st = kStagesHG;
+  if (st > nk) st = nk;
+  return st < 1 ? 1 : st;
+}
+
 template <bool kAMN>
 static mla_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& g, int m_tiles, int n_tiles,
                          cudaStream_t s) {
@@ -233,7 +261,7 @@ mla_status launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int3
   g.K = d_k;
   g.nb = B;
   g.n_tile = n_tile_for(B);
-  g.stages = d_k / kBK < kStagesHG ? d_k / kBK : kStagesHG;
+  g.stages = stages_for(d_k / kBK, g.n_tile);
   g.out = static_cast<__nv_bfloat16*>(q_cat);
   g.out_h_stride = d_c + d_r;
   g.out_n_stride = static_cast<long long>(H) * (d_c + d_r);
@@ -257,7 +285,7 @@ mla_status launch_out_up_tc(const void* o_lat, const void* w_uv, void* o, int32_
   g.K = d_c;
   g.nb = B;
   g.n_tile = n_tile_for(B);
-  g.stages = d_c / kBK < kStagesHG ? d_c / kBK : kStagesHG;
+  g.stages = stages_for(d_c / kBK, g.n_tile);
   g.out = static_cast<__nv_bfloat16*>(o);
   g.out_h_stride = d_v;
   g.out_n_stride = static_cast<long long>(H) * d_v;

@@ -6,6 +6,7 @@
 namespace {
 
 using mla::aligned16;
+using mla::aligned4;
 
 bool valid_dtype(int32_t dt) { return dt == MLA_BF16 || dt == MLA_F32; }
 
@@ -65,7 +66,8 @@ MLA_API mla_status mla_absorb_q(const void* q_nope, const void* q_rope, const in
   if (d_r > 0 && q_rope == nullptr) return MLA_ERR_INVALID_ARG;
   if (!(rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
   if (d_r > 128) return MLA_ERR_UNSUPPORTED;
-  if (dtype == MLA_BF16 && mla::headgemm_absorb_supported(d_k, d_c, d_r) && aligned16(q_nope) && aligned16(w_uk))
+  if (dtype == MLA_BF16 && mla::headgemm_absorb_supported(d_k, d_c, d_r) && aligned16(q_nope) && aligned16(w_uk) &&
+      aligned4(q_cat) && (d_r == 0 || aligned4(q_rope)))
     return mla::launch_absorb_q_tc(q_nope, q_rope, q_pos, w_uk, q_cat, B, H, d_k, d_c, d_r, rope_base,
                                    as_stream(stream));
   if (static_cast<size_t>(32) * d_k * sizeof(float) > 200 * 1024) return MLA_ERR_UNSUPPORTED;

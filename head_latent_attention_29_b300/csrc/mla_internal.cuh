@@ -35,6 +35,7 @@ __device__ __forceinline__ void st_elem(float* p, float v) { *p = v; }
 __device__ __forceinline__ void st_elem(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // RoPE frequencies theta_i = base^(-2i/d_r), i < d_r/2, computed once on the host in
 // double and passed by value to the kernels (d_r <= 128).
