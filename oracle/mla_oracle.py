@@ -234,18 +234,20 @@ def gate(h: np.ndarray, w_g: np.ndarray, o_flat: np.ndarray) -> np.ndarray:
 
 
 def prefill_absorbed_rows(q_cat: np.ndarray, rows: np.ndarray, d_c: int, scale: float,
-                          query_positions, causal: bool = True):
-    """Absorbed attention of selected prompt queries against the cache prefix.
+                          query_positions, causal: bool = True, start: int = 0):
+    """Absorbed attention of selected prompt queries against the cache prefix
+    (hotelren.com guide, section 2.1: prefill handles the whole prompt at once;
+    0539edu.com sections 3.1-3.2: the absorbed scores keep their per-position shape).
 
-    q_cat [S, H, R] for all S prompt positions, rows [S, R] the cached rows of the
-    same prompt (positions 0..S-1).  For each selected query position i the keys
-    are j <= i when causal (the diagonal included), else all S.
-    Returns (o_lat [k, H, d_c], lse [k, H]) for the k selected positions."""
+    q_cat [S, H, R] for the S prompt queries, which sit at positions start..start+S-1;
+    rows [start + S, R] the cached rows of the sequence up to the prompt's end.
+    Query i reads rows 0..start+i when causal (its own row included), else all
+    start + S rows.  Returns (o_lat [k, H, d_c], lse [k, H]) for the k selected i."""
     q_cat = np.asarray(q_cat, dtype=np.float64)
     rows = np.asarray(rows, dtype=np.float64)
     outs, lses = [], []
     for i in query_positions:
-        n = i + 1 if causal else rows.shape[0]
+        n = start + i + 1 if causal else start + q_cat.shape[0]
         o, l = decode_absorbed(q_cat[i], rows[:n], d_c, scale)
         outs.append(o)
         lses.append(l)

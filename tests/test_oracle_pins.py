@@ -263,6 +263,30 @@ def test_prefill_rows_match_masked_full_softmax():
     np.testing.assert_allclose(o_rows[0], np.broadcast_to(rows[0, :d_c], (H, d_c)), rtol=1e-15)
 
 
+def test_prefill_in_chunks_equals_one_pass():
+    # A prompt processed as two chunks (the second starting at position S1 over the
+    # rows of both) gives the rows of one pass: the chunk offset is only a shift of
+    # the causal limit.  The non-causal chunk reads every row up to its own end.
+    rng = np.random.default_rng(23)
+    S1, S2, H, R, d_c = 7, 9, 2, 24, 16
+    q_cat, rows = rng.standard_normal((S1 + S2, H, R)), rng.standard_normal((S1 + S2, R))
+    scale = 0.3
+    whole_o, whole_l = O.prefill_absorbed_rows(q_cat, rows, d_c, scale, range(S1 + S2))
+    o1, l1 = O.prefill_absorbed_rows(q_cat[:S1], rows[:S1], d_c, scale, range(S1))
+    o2, l2 = O.prefill_absorbed_rows(q_cat[S1:], rows, d_c, scale, range(S2), start=S1)
+    np.testing.assert_allclose(np.concatenate([o1, o2]), whole_o, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(np.concatenate([l1, l2]), whole_l, rtol=1e-13)
+    # non-causal second chunk: every query reads all S1 + S2 rows (as the last query does)
+    o_nc, l_nc = O.prefill_absorbed_rows(q_cat[S1:], rows, d_c, scale, range(S2), causal=False, start=S1)
+    for i in range(S2):
+        o_ref, l_ref = O.decode_absorbed(q_cat[S1 + i], rows, d_c, scale)
+        np.testing.assert_allclose(o_nc[i], o_ref, rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(l_nc[i], l_ref, rtol=1e-13)
+    # a wrong offset would be visible: the first query of the chunk must see S1 + 1 rows
+    o_wrong, _ = O.decode_absorbed(q_cat[S1], rows[:1], d_c, scale)
+    assert np.max(np.abs(o2[0] - o_wrong)) > 1e-3
+
+
 # ---------------------------------------------------------------------------
 # Magnitudes of the headline workload: unit-variance scores
 # ---------------------------------------------------------------------------
