@@ -360,6 +360,211 @@ def run_b300(args, rank, world, device):
     return out
 
 
+# ---------------------------------------------------------------- prefill
+def prefill_draws(cfg, seed, b):
+    """Seeded prompt inputs of sequence b: c_KV [S, d_c], k_R [S, d_r] (pre-rotation),
+    q_nope [S, H, d_k], q_R [S, H, d_r], bf16 bit patterns."""
+    S, H = cfg["S"], cfg["H"]
+    c, k = W.latent_rows(cfg, seed, b, S)
+    q_nope = W.normal(seed, "prefill_q_nope", (S, H, cfg["d_k"]), index=(b,))
+    q_r = W.normal(seed, "prefill_q_r", (S, H, cfg["d_r"]), index=(b,))
+    return tuple(W.bf16_bits(x) for x in (c, k, q_nope, q_r))
+
+
+def prefill_flops(cfg):
+    """Causal (query, row) pairs x heads x (2 R + 2 d_c)."""
+    S, R = cfg["S"], cfg["d_c"] + cfg["d_r"]
+    pairs = cfg["B"] * S * (S + 1) // 2
+    return pairs * cfg["H"] * (2 * R + 2 * cfg["d_c"]), pairs
+
+
+class PrefillWorkload:
+    """One prompt step over static buffers: append the B x S prompt rows (RoPE at
+    0..S-1), absorb every query at its own position, causal prefill attention,
+    W_UV.  Inputs are far larger than L2."""
+
+    def __init__(self, name, seed, device):
+        import torch
+        import head_latent_attention_29_b300 as mla
+        self.mla, self.torch = mla, torch
+        cfg = dict(W.WORKLOADS[name])
+        self.cfg = cfg
+        B, S, H, d_c, d_r, d_k, d_v = (cfg[k] for k in ("B", "S", "H", "d_c", "d_r", "d_k", "d_v"))
+        self.B, self.S, self.H = B, S, H
+        bf = torch.bfloat16
+        self.base, self.scale = cfg["rope_base"], cfg["scale"]
+        pin = lambda shape: torch.empty(shape, dtype=bf).pin_memory()
+        self.host = {"c_kv": pin((B, S, d_c)), "k_r": pin((B, S, d_r)), "q_nope": pin((B, S, H, d_k)),
+                     "q_rope": pin((B, S, H, d_r))}
+        for b in range(B):
+            for key, x in zip(("c_kv", "k_r", "q_nope", "q_rope"), prefill_draws(cfg, seed, b)):
+                self.host[key][b].copy_(torch.from_numpy(x.view(np.int16)).view(bf))
+        self.dev = {k: v.to(device) for k, v in self.host.items()}
+        w_uk, w_uv = W.up_weights(cfg, seed)
+        up = lambda x: torch.from_numpy(np.ascontiguousarray(W.bf16_bits(x)).view(np.int16)).view(bf).to(device)
+        self.w_uk, self.w_uv = up(w_uk), up(w_uv)
+        self.cache = mla.LatentCache(B, S, d_c, d_r, dtype=bf, device=device)
+        self.seq_idx = torch.arange(B, dtype=torch.int32, device=device).repeat_interleave(S)
+        self.pos = torch.arange(S, dtype=torch.int32, device=device).repeat(B)
+        self.q_start = torch.zeros(B, dtype=torch.int32, device=device)
+        self.q_cat = torch.empty((B, S, H, d_c + d_r), dtype=bf, device=device)
+        self.o_lat = torch.empty((B, S, H, d_c), dtype=bf, device=device)
+        self.lse = torch.empty((B, S, H), dtype=torch.float32, device=device)
+        self.o = torch.empty((B, S, H, d_v), dtype=bf, device=device)
+        self.o_host = torch.empty((B, S, H, d_v), dtype=bf).pin_memory()
+        self.ws = mla.prefill_workspace(B, S, H, d_c, bf, device)
+        self.kernels_per_step = 5  # append, absorb GEMM, split attention, combine, out-up GEMM
+
+    def attn(self):
+        self.mla.prefill_attn(self.q_cat, self.cache, self.q_start, self.scale, True, self.ws, self.o_lat, self.lse)
+
+    def step(self, copy_in=False, copy_out=False):
+        d, mla, BS = self.dev, self.mla, self.B * self.S
+        if copy_in:
+            for k, v in self.host.items():
+                d[k].copy_(v, non_blocking=True)
+        mla.cache_append(self.cache, d["c_kv"].view(BS, -1), d["k_r"].view(BS, -1), self.seq_idx, self.pos,
+                         self.base)
+        mla.absorb_q(d["q_nope"].view(BS, self.H, -1), d["q_rope"].view(BS, self.H, -1), self.pos, self.w_uk,
+                     self.base, out=self.q_cat.view(BS, self.H, -1))
+        self.attn()
+        mla.out_up(self.o_lat.view(BS, self.H, -1), self.w_uv, out=self.o.view(BS, self.H, -1))
+        if copy_out:
+            self.o_host.copy_(self.o, non_blocking=True)
+
+
+def run_b300_prefill(args, rank, world, device):
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(device)
+    wl = PrefillWorkload(args.workload, args.seed + rank, device)
+    cfg = wl.cfg
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize(device)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            wl.step()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier()
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    tokens = wl.B * wl.S * world
+    value = tokens / (ms_step * 1e-3)
+
+    # the attention kernel alone (split + combine), on its stream
+    n_rep = max(3, min(args.steps, 20))
+    wl.attn()
+    torch.cuda.synchronize(device)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(n_rep):
+        wl.attn()
+    a1.record(stream)
+    torch.cuda.synchronize(device)
+    attn_us = a0.elapsed_time(a1) * 1e3 / n_rep
+
+    # end to end: prompt inputs in from pinned memory, o back to pinned memory
+    n_e2e = max(3, min(args.steps, 10))
+    wl.step(True, True)
+    torch.cuda.synchronize(device)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        wl.step(True, True)
+        stream.synchronize()
+    barrier()
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    h2d = sum(v.numel() * v.element_size() for v in wl.host.values())
+    d2h = wl.o_host.numel() * wl.o_host.element_size()
+
+    hbm, tc_burst, tc_sust, peak_kind = _peaks()
+    flops, pairs = prefill_flops(cfg)
+    R = cfg["d_c"] + cfg["d_r"]
+    bytes_alg = cfg["B"] * cfg["S"] * cfg["H"] * (R + cfg["d_c"]) * 2 + cfg["B"] * cfg["S"] * R * 2
+    tflops = flops / (attn_us * 1e-6) / 1e12
+    t_tc = flops / (tc_burst * 1e12)
+    t_mem = bytes_alg / (hbm * 1e9)
+    return {
+        "metric": "MLA causal prefill prompt tokens/s at H=128,d_c=512,B=4,S=8192 bf16; % of roofline",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) latents/keys/queries, N(0,1/512) up-projections)",
+        "config": {"workload": args.workload, "B": cfg["B"], "S": cfg["S"], "H": cfg["H"], "d_c": cfg["d_c"],
+                   "d_r": cfg["d_r"], "causal": True, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (q_cat 4.8 GB, o_lat 4.3 GB per step)",
+                   "step": "append(B*S rows)+absorb_q(B*S queries)+prefill_attn(split+combine)+out_up"},
+        "gpu_launches": wl.kernels_per_step * args.steps,
+        "e2e": {"value": round(tokens / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "roofline": {
+            "bound": "tensor", "kernel": "prefill_attn (split tensor-core kernel + combine)",
+            "achieved": round(tflops, 1), "peak": tc_burst, "unit": "TFLOP/s", "frac": round(tflops / tc_burst, 4),
+            "traffic": None, "peak_source": f"{peak_kind} bf16_tflops (burst)",
+            "frac_sustained": round(tflops / tc_sust, 4) if tc_sust else None,
+            "attn_us": round(attn_us, 1), "algorithmic_flops": flops, "causal_pairs": pairs,
+            "roofline_us": round(max(t_tc, t_mem) * 1e6, 1), "frac_of_roofline": round(max(t_tc, t_mem) * 1e6 / attn_us, 4),
+        },
+        "clocks": clk.summary(),
+    }
+
+
+_PREFILL_ORACLE_STATE = {}
+
+
+def cpu_baseline_prefill(workload: str, seed: int, budget_s: float = 12.0):
+    """Time the float64 oracle's prompt step per query row (absorb at the row's
+    position, attention over rows 0..i, out_up) for query rows spread evenly over
+    the prompt of sequence 0; the per-token cost of an even spread is the mean
+    cost of the whole causal prompt."""
+    from oracle import mla_oracle as O
+    cfg = dict(W.WORKLOADS[workload])
+    S, base = cfg["S"], cfg["rope_base"]
+    key = (workload, seed)
+    if key not in _PREFILL_ORACLE_STATE:  # inputs and the cache rows are resident state, not step work
+        c, k, q_nope, q_r = (W.widen(x, "bf16") for x in prefill_draws(cfg, seed, 0))
+        w_uk, w_uv = (W.widen(W.as_dtype(w, "bf16"), "bf16") for w in W.up_weights(cfg, seed))
+        _PREFILL_ORACLE_STATE[key] = (O.cache_rows(c, k, np.arange(S), base), q_nope, q_r, w_uk, w_uv)
+    rows, q_nope, q_r, w_uk, w_uv = _PREFILL_ORACLE_STATE[key]
+    order = np.random.default_rng(seed).permutation(S)
+    done = 0
+    t0 = time.perf_counter()
+    while done < S:
+        i = int(order[done])
+        q_cat = O.absorb_q(q_nope[i], q_r[i], i, w_uk, base)
+        o_lat, _ = O.decode_absorbed(q_cat, rows[: i + 1], cfg["d_c"], cfg["scale"])
+        O.out_up(o_lat, w_uv)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    try:
+        from threadpoolctl import threadpool_info
+        threads = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+    except Exception:  # pragma: no cover
+        threads = []
+    return {"value": round(done / el, 3), "unit": "tokens/s", "cores": max(threads) if threads else 1,
+            "kind": "oracle", "host_cpus": os.cpu_count(),
+            "sample": f"{done} prompt query rows of sequence 0 at random positions of 0..{S - 1} "
+                      f"(causal prefix each), float64 numpy, {el:.1f} s"}
+
+
 def _ncu_traffic(workload):
     """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, if any."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -425,21 +630,26 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     cfg = W.WORKLOADS[args.workload]
+    prefill = "S" in cfg
+    fn = cpu_baseline_prefill if prefill else cpu_baseline
     steps = []
     for _ in range(max(1, args.warmup)):
-        cpu_baseline(args.workload, args.seed, budget_s=0.5)
+        fn(args.workload, args.seed, budget_s=0.5)
     per = max(1.0, min(10.0, 60.0 / max(args.steps, 1)))
     for _ in range(args.steps):
-        steps.append(cpu_baseline(args.workload, args.seed, budget_s=per))
+        steps.append(fn(args.workload, args.seed, budget_s=per))
     vals = [s["value"] for s in steps]
     v = statistics.median(vals)
     cb = dict(steps[-1])
     cb["value"] = round(v, 3)
+    metric = ("MLA causal prefill prompt tokens/s at H=128,d_c=512,B=4,S=8192 bf16; % of roofline" if prefill
+              else "MLA decode tokens/s at H=128,d_c=512,B=32,N=4K bf16; % of roofline")
+    tokens_per_step = cfg["B"] * cfg.get("S", 1)
     return {
         "impl": "reference",
-        "metric": "MLA decode tokens/s at H=128,d_c=512,B=32,N=4K bf16; % of roofline",
+        "metric": metric,
         "value": round(v, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(1e3 * cfg["B"] / v, 3), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": round(1e3 * tokens_per_step / v, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "B": cfg["B"], "H": cfg["H"], "d_c": cfg["d_c"], "d_r": cfg["d_r"],
                    "parallelism": "host cores (oracle)"},
@@ -480,7 +690,12 @@ def main():
         torch.cuda.set_device(device)
         dist.init_process_group("nccl", device_id=device)
     try:
-        out = run_b300(args, rank, world, device)
+        if "S" in W.WORKLOADS[args.workload]:
+            out = run_b300_prefill(args, rank, world, device)
+            if rank == 0 and not args.no_cpu_baseline:
+                out["cpu_baseline"] = cpu_baseline_prefill(args.workload, args.seed, budget_s=args.cpu_seconds)
+        else:
+            out = run_b300(args, rank, world, device)
         if rank == 0:
             print(json.dumps(out), flush=True)
     finally:

@@ -63,6 +63,11 @@ _SIGS = {
     "mla_decode_attn": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(_Cache), ctypes.c_void_p, ctypes.c_int32,
                                        ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p]),
+    "mla_prefill_workspace_size": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                     ctypes.c_int32]),
+    "mla_prefill_attn": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(_Cache), ctypes.c_void_p, ctypes.c_int32,
+                                        ctypes.c_int32, ctypes.c_float, ctypes.c_int32, ctypes.c_void_p,
+                                        ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "mla_out_up": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]),
     "mla_gate": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
@@ -200,6 +205,36 @@ def decode_attn(q_cat: torch.Tensor, cache: LatentCache, seq_lens: torch.Tensor,
     st = cache.struct()
     _check(lib().mla_decode_attn(_ptr(q_cat), ctypes.byref(st), _ptr(seq_lens), H, float(scale), _ptr(workspace),
                                  workspace.numel(), _ptr(out), _ptr(lse), _stream(q_cat)), "mla_decode_attn")
+    return out, lse
+
+
+def prefill_workspace(B: int, S: int, H: int, d_c: int, dtype=torch.bfloat16, device="cuda") -> torch.Tensor:
+    n = lib().mla_prefill_workspace_size(B, S, H, d_c, _DT[dtype])
+    if n == 0:
+        raise MlaError(2, "mla_prefill_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def prefill_attn(q_cat: torch.Tensor, cache: LatentCache, q_start: torch.Tensor, scale: float, causal: bool = True,
+                 workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                 lse: torch.Tensor | None = None, want_lse: bool = True):
+    """o_lat [B, S, H, d_c] (and lse [B, S, H] fp32) of absorbed prompt attention;
+    query i of sequence b sits at position q_start[b] + i."""
+    _dev_tensor(q_cat, "q_cat", cache.dtype)
+    B, S, H, R = q_cat.shape
+    if B != cache.B or R != cache.d_c + cache.d_r:
+        raise ValueError("q_cat shape does not match the cache")
+    _dev_tensor(q_start, "q_start", torch.int32)
+    if workspace is None:
+        workspace = prefill_workspace(B, S, H, cache.d_c, cache.dtype, q_cat.device)
+    if out is None:
+        out = torch.empty((B, S, H, cache.d_c), dtype=cache.dtype, device=q_cat.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, S, H), dtype=torch.float32, device=q_cat.device)
+    st = cache.struct()
+    _check(lib().mla_prefill_attn(_ptr(q_cat), ctypes.byref(st), _ptr(q_start), S, H, float(scale), int(causal),
+                                  _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse), _stream(q_cat)),
+           "mla_prefill_attn")
     return out, lse
 
 

@@ -28,10 +28,15 @@
 //  * Cache rows stream in through TMA (128-byte swizzled 64x64 chunks, 3-stage
 //    ring per CTA).  The same swizzled chunk is the K-major B operand of
 //    S = Q C^T and the MN-major B operand of O = P C.
-//  * The token stream of all sequences is cut into equal runs of 64-token blocks,
-//    one run per cluster, so every SM pair gets the same work whatever the mix
-//    of lengths; each (run, sequence) overlap leaves an unnormalised partial
-//    (m, l, O) and a combine kernel merges the partials of each sequence.
+//  * A "problem" is one query row group (all heads of one query) against a prefix
+//    of one cached sequence: in decode, sequence b's query against its N_b rows; in
+//    causal prefill, query i of sequence b against rows [0, start_b + i] (the rows
+//    of the prompt itself, already appended).  The blocks of all problems form one
+//    token stream that is cut into equal runs of 64-token blocks, one run per
+//    cluster, so every SM pair gets the same work whatever the mix of lengths.  A
+//    problem that lies inside one run is normalised and written out directly; one
+//    cut by run boundaries leaves an unnormalised partial (m, l, O) per piece, and
+//    a combine kernel merges the pieces.
 #include <cmath>
 
 #include "mla_internal.cuh"
@@ -53,7 +58,7 @@ constexpr int kDC = 512;                    // latent width
 constexpr int kChDC = kDC / 64;             // 8 chunks of 64 columns cover the latent
 constexpr int kChunk = kBN * 128;           // bytes of one [64 tok x 64 col] bf16 chunk
 constexpr int kM = 128;                     // head rows per MMA
-constexpr int kMaxPairs = 160;              // upper bound on clusters per launch
+constexpr int kMaxPairs = 80;               // upper bound on clusters per launch (148 SMs -> 74)
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P stays <= 256
 constexpr int kThreads = 384;               // 12 warps: see the role map in the kernel
 
@@ -109,35 +114,52 @@ struct Misc {                     // at kOffMisc
 };
 static_assert(sizeof(Misc) <= 128, "misc");
 
-struct Args {
-  const __nv_bfloat16* q_cat;  // [B][H][R]
-  const int32_t* seq_lens;     // [B]
-  int B, H, N_max, R, nch;     // nch: 64-column chunks per row (R / 64)
-  float scale_log2;            // scale * log2(e)
-  int32_t* hdr;                // workspace: [0] = total blocks, [1] = runs used
-  int32_t* cum;                // workspace: [B + 1] first block of each sequence
-  float* part_m;               // [slots][128] running max (log2 units)
-  float* part_l;               // [slots][128] running sum
-  float* part_o;               // [slots][512][128] unnormalised output, latent-column major
+__device__ __forceinline__ int clamp_len(int n, int n_max) { return n < 0 ? 0 : (n > n_max ? n_max : n); }
+
+// The problems of a launch and the rows each one reads.
+struct Problems {
+  const int32_t* seq_lens;  // decode: [B] rows of sequence b (one problem per sequence)
+  const int32_t* q_start;   // prefill: [B] position of sequence b's first query; nullptr in decode
+  int S;                    // queries per sequence (1 in decode)
+  int causal;               // prefill: query i reads start + i + 1 rows (else start + S)
+  int n_max;
+  __device__ int raw_len(int pr) const {
+    if (q_start == nullptr) return seq_lens[pr];
+    const int b = pr / S, i = pr - b * S;
+    return q_start[b] + (causal ? i + 1 : S);
+  }
+  __device__ int len(int pr) const { return clamp_len(raw_len(pr), n_max); }
+  __device__ int seq(int pr) const { return q_start == nullptr ? pr : pr / S; }
 };
 
-__device__ __forceinline__ int clamp_len(int n, int n_max) { return n < 0 ? 0 : (n > n_max ? n_max : n); }
+struct Args {
+  const __nv_bfloat16* q_cat;  // [NP][H][R]
+  Problems pb;
+  int NP, H, N_max, R, nch;    // NP problems; nch: 64-column chunks per row (R / 64)
+  float scale_log2;            // scale * log2(e)
+  int32_t* hdr;                // workspace: [0] total blocks, [1] runs used, [2] problems with no rows
+  int32_t* cum;                // workspace: [NP + 1] first block of each problem
+  float* part_m;               // [2 kMaxPairs][128] running max (log2 units)
+  float* part_l;               // [2 kMaxPairs][128] running sum
+  float* part_o;               // [2 kMaxPairs][512][128] unnormalised output, latent-column major
+  __nv_bfloat16* o_lat;        // [NP][H][512]
+  float* lse;                  // [NP][H] natural-log LSE, or nullptr
+};
 
 // Walks the 64-token blocks [lo, hi) of the flattened token stream.
 struct Cursor {
-  const int32_t* seq_lens;
-  int n_max;
+  Problems pbs;
   long long g, lo, hi, cum;
-  int b, len, nblk;
-  __device__ void start(const Misc& m, const int32_t* sl, int nm) {
-    seq_lens = sl;
-    n_max = nm;
+  int b, len, nblk, cs;  // b: problem, cs: its cache sequence
+  __device__ void start(const Misc& m, const Problems& p) {
+    pbs = p;
     g = lo = m.lo;
     hi = m.hi;
     cum = m.cum0;
     b = m.b0;
     len = m.len0;
     nblk = (len + kBN - 1) / kBN;
+    cs = pbs.seq(b);
   }
   __device__ bool ok() const { return g < hi; }
   __device__ void next() {
@@ -145,35 +167,43 @@ struct Cursor {
     while (g < hi && g >= cum + nblk) {
       cum += nblk;
       ++b;
-      len = clamp_len(seq_lens[b], n_max);
+      len = pbs.len(b);
       nblk = (len + kBN - 1) / kBN;
+      cs = pbs.seq(b);
     }
   }
   __device__ int t0() const { return static_cast<int>(g - cum) * kBN; }
   __device__ int rows() const { return min(kBN, len - t0()); }
   __device__ bool first() const { return g == lo || g == cum; }
   __device__ bool last() const { return g == hi - 1 || g == cum + nblk - 1; }
+  __device__ bool whole() const { return cum >= lo && cum + nblk <= hi; }  // problem inside this run
 };
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
 
 // Plan the run of this cluster: total blocks T, runs P = min(clusters, T), this
-// run's [lo, hi), and the sequence that holds block lo.  One warp.
+// run's [lo, hi), and the problem that holds block lo.  One warp.  The writer of
+// the table (one CTA per launch) also checks every length and counts the problems
+// with no rows.
 __device__ void plan_run(const Args& a, Misc* misc, bool write_table) {
   const int lane = threadIdx.x & 31;
   long long T = 0;
-  for (int base = 0; base < a.B; base += 32) {
+  int empties = 0;
+  for (int base = 0; base < a.NP; base += 32) {
     const int b = base + lane;
     int nb = 0;
-    if (b < a.B) {
-      const int n = a.seq_lens[b];
+    if (b < a.NP) {
+      const int n = a.pb.raw_len(b);
       if (write_table && (n < 0 || n > a.N_max)) record_error(MLA_ERR_DEVICE_INDEX, kSiteDecodeLength);
       nb = (clamp_len(n, a.N_max) + kBN - 1) / kBN;
+      empties += nb == 0;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) nb += __shfl_xor_sync(0xffffffffu, nb, off);
     T += nb;
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) empties += __shfl_xor_sync(0xffffffffu, empties, off);
   const long long nclus = nclusters_x();
   const long long P = T < nclus ? T : nclus;
   const long long cid = cluster_id_x();
@@ -187,9 +217,9 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table) {
   if (lo < hi || write_table) {
     long long run = 0;
     bool found = false;
-    for (int base = 0; base < a.B; base += 32) {
+    for (int base = 0; base < a.NP; base += 32) {
       const int b = base + lane;
-      const int n = b < a.B ? clamp_len(a.seq_lens[b], a.N_max) : 0;
+      const int n = b < a.NP ? a.pb.len(b) : 0;
       const int nb = (n + kBN - 1) / kBN;
       int incl = nb;
 #pragma unroll
@@ -198,8 +228,8 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table) {
         if (lane >= off) incl += v;
       }
       const long long excl = run + incl - nb;
-      if (write_table && b < a.B) a.cum[b] = static_cast<int32_t>(excl);
-      const bool hit = !found && b < a.B && nb > 0 && excl <= lo && lo < excl + nb;
+      if (write_table && b < a.NP) a.cum[b] = static_cast<int32_t>(excl);
+      const bool hit = !found && b < a.NP && nb > 0 && excl <= lo && lo < excl + nb;
       const unsigned m = __ballot_sync(0xffffffffu, hit);
       if (m != 0u) {
         const int src = __ffs(m) - 1;
@@ -219,9 +249,10 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table) {
     misc->cum0 = cum0;
     misc->len0 = len0;
     if (write_table) {
-      a.cum[a.B] = static_cast<int32_t>(T);
+      a.cum[a.NP] = static_cast<int32_t>(T);
       a.hdr[0] = static_cast<int32_t>(T);
       a.hdr[1] = static_cast<int32_t>(P);
+      a.hdr[2] = empties;
     }
   }
 }
@@ -288,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     const int nload = score_cta ? nch : kChDC;
     const int nst = score_cta ? kStages : kStagesO;
     Cursor c;
-    c.start(*misc, a.seq_lens, a.N_max);
+    c.start(*misc, a.pb);
     // the score CTA's query goes out before the cache stream floods the memory system
     if (score_cta && c.ok()) warp_wait(bar_addr(sbase, kBarQReady), 0, abort);
     for (int k = 0; c.ok(); c.next(), ++k) {
@@ -299,14 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       for (int ch = 0; ch < nload; ++ch) {
         const uint32_t dst = ch < kChDC ? sbase + kOffStage + st * kStageDC + ch * kChunk
                                         : sbase + kOffRope + st * kChunk;
-        tma_load_3d_if(leader, dst, &map, bar_addr(sbase, kBarFull + st), ch * 64, c.t0(), c.b);
+        tma_load_3d_if(leader, dst, &map, bar_addr(sbase, kBarFull + st), ch * 64, c.t0(), c.cs);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t leader = elect_one();
     Cursor c;
-    c.start(*misc, a.seq_lens, a.N_max);
+    c.start(*misc, a.pb);
     if (score_cta) {
       // S = Q C^T: M = 128 heads, N = 64 tokens, A (the query) from tensor memory
       constexpr uint32_t idesc = idesc_bf16(kM, kBN, false, false);
@@ -381,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     const uint32_t lane_off = static_cast<uint32_t>(r & ~31) << 16;
     float* ref_x = reinterpret_cast<float*>(gbase + kOffX);    // reference exchange between the groups
     Cursor c;
-    c.start(*misc, a.seq_lens, a.N_max);
+    c.start(*misc, a.pb);
     int k = 0, last_mine = -1;
     for (; c.ok(); c.next(), ++k) {
       if ((k & 1) != grp) continue;
@@ -486,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     const int r = threadIdx.x - 128;
     const uint32_t lane_off = static_cast<uint32_t>(r & ~31) << 16;
     Cursor c;
-    c.start(*misc, a.seq_lens, a.N_max);
+    c.start(*misc, a.pb);
     float m = 0.f, l = 0.f;
     int k = 0;
     for (; c.ok(); c.next(), ++k) {
@@ -552,20 +583,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         if (!warp_wait(bar_addr(sbase, kBarODone + pb), (k / kPBufs) & 1, abort)) break;
         if (r == 0) MLA_TRACE_POINT(k, 11);
         tc_fence_after();
-        const long long slot = cluster_id_x() + c.b;
-        float* dst = a.part_o + slot * (kDC * kM) + r;  // [c][h]: a warp stores 128 contiguous bytes
-        for (int cc = 0; cc < 8; ++cc) {
-          uint32_t v[64];
-          tmem_ld64(tmem + lane_off + cc * 64, v);
-          tmem_wait_ld();
-          if (r < a.H) {
+        if (c.whole()) {
+          // the whole problem ran here: o = O / l in bf16, lse = (m + log2 l) ln 2
+          const float inv = 1.f / l;
+          uint4* dst = reinterpret_cast<uint4*>(a.o_lat + (static_cast<long long>(c.b) * a.H + r) * kDC);
+          for (int cc = 0; cc < 8; ++cc) {
+            uint32_t v[64];
+            tmem_ld64(tmem + lane_off + cc * 64, v);
+            tmem_wait_ld();
+            if (r < a.H) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) dst[(cc * 64 + j) * kM] = __uint_as_float(v[j]);
+              for (int q = 0; q < 8; ++q) {
+                uint4 w;
+                w.x = pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
+                w.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
+                w.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
+                w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
+                dst[cc * 8 + q] = w;
+              }
+            }
           }
-        }
-        if (r < a.H) {
-          a.part_m[slot * kM + r] = m;
-          a.part_l[slot * kM + r] = l;
+          if (r < a.H && a.lse != nullptr)
+            a.lse[static_cast<long long>(c.b) * a.H + r] = (m + log2f(l)) * 0.69314718055994531f;
+        } else {
+          // a piece of a problem cut by run boundaries: slot 2 p for the problem that
+          // holds the run's first block, 2 p + 1 for the one cut at the run's end
+          const long long slot = 2 * static_cast<long long>(cluster_id_x()) + (c.b == misc->b0 ? 0 : 1);
+          float* dst = a.part_o + slot * (kDC * kM) + r;  // [c][h]: a warp stores 128 contiguous bytes
+          for (int cc = 0; cc < 8; ++cc) {
+            uint32_t v[64];
+            tmem_ld64(tmem + lane_off + cc * 64, v);
+            tmem_wait_ld();
+            if (r < a.H) {
+#pragma unroll
+              for (int j = 0; j < 64; ++j) dst[(cc * 64 + j) * kM] = __uint_as_float(v[j]);
+            }
+          }
+          if (r < a.H) {
+            a.part_m[slot * kM + r] = m;
+            a.part_l[slot * kM + r] = l;
+          }
         }
         tc_fence_before();
         if (r == 0) MLA_TRACE_POINT(k, 12);
@@ -583,63 +640,94 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
   cluster_sync();  // no remote access into a CTA that has exited
 }
 
-// Merge the partials of each sequence: M = max m_s, L = sum l_s 2^(m_s - M),
-// o = sum 2^(m_s - M) O_s / L, lse = (M + log2 L) ln 2.  One block per (32 latent
-// columns, sequence); thread t owns heads 4(t/4)..+3 and columns 8(t%4)..+7, so
-// every partial read is a 16-byte load and a warp reads 4 runs of 128 contiguous
-// bytes.  The merged tile is staged in shared memory ([head][column], padded rows)
-// and written out as 64 contiguous bytes per (sequence, head).
-__global__ void __launch_bounds__(128) combine_kernel(const Args a, __nv_bfloat16* __restrict__ o_lat,
-                                                      float* __restrict__ lse) {
+// Largest problem pr with cum[pr] <= g for a block g < T; it has rows (an empty
+// problem shares its cum with the next one).
+__device__ __forceinline__ int problem_of_block(const int32_t* cum, int np, long long g) {
+  int lo = 0, hi = np;  // cum[lo] <= g < cum[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cum[mid] <= g) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Merge the pieces of every problem cut by run boundaries: M = max m_s,
+// L = sum l_s 2^(m_s - M), o = sum 2^(m_s - M) O_s / L, lse = (M + log2 L) ln 2.
+// Block (x, p) handles latent columns [32 x, 32 x + 32) of the problem that run
+// boundary p cuts, if p is the first boundary inside it; blocks (x, 0) write the
+// zero output of problems with no rows.  Thread t owns heads 4(t/4)..+3 and columns
+// 8(t%4)..+7, so every partial read is a 16-byte load and a warp reads 4 runs of
+// 128 contiguous bytes.  The merged tile is staged in shared memory ([head][column],
+// padded rows) and written out as 64 contiguous bytes per (problem, head).
+__global__ void __launch_bounds__(128) combine_kernel(const Args a) {
   constexpr int kPitch = 40;  // staged row: 32 bf16 columns + 16 bytes of padding
   __shared__ __align__(16) __nv_bfloat16 s_o[kM * kPitch];
-  const int cb32 = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
-  const int h0 = (t >> 2) * 4, cq = t & 3;
+  const int cb32 = blockIdx.x, p = blockIdx.y, t = threadIdx.x;
   const long long T = a.hdr[0], P = a.hdr[1];
-  const long long cb = a.cum[b], ce = a.cum[b + 1];
+  if (p == 0) {
+    if (a.hdr[2] == 0) return;
+    for (int pr = t; pr < a.NP; pr += blockDim.x) {
+      if (a.cum[pr] != a.cum[pr + 1]) continue;
+      for (int h = 0; h < a.H; ++h) {
+        uint4* dst = reinterpret_cast<uint4*>(a.o_lat + (static_cast<long long>(pr) * a.H + h) * kDC + cb32 * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+        if (a.lse != nullptr && cb32 == 0) a.lse[static_cast<long long>(pr) * a.H + h] = -INFINITY;
+      }
+    }
+    return;
+  }
+  if (p >= P) return;
+  const long long lo_p = p * T / P;
+  const int pr = problem_of_block(a.cum, a.NP, lo_p);
+  const long long cb = a.cum[pr], ce = a.cum[pr + 1];
+  if (cb == lo_p) return;  // the boundary falls between problems
+  // run q covers blocks [q T / P, (q + 1) T / P); run of block g = ceil((g + 1) P / T) - 1
+  const long long p_first = ((cb + 1) * P + T - 1) / T - 1;
+  if (p != p_first + 1) return;  // the block of an earlier boundary merges this problem
+  const long long p_last = (ce * P + T - 1) / T - 1;
+  const long long slot_first = 2 * p_first + (p_first * T / P == cb ? 0 : 1);
+
+  const int h0 = (t >> 2) * 4, cq = t & 3;
   float acc[8][4];
 #pragma unroll
   for (int j = 0; j < 8; ++j)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
   float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, L[4] = {0.f, 0.f, 0.f, 0.f};
-  const bool any = ce > cb && P > 0;
-  if (any) {
-    // run p covers blocks [p T / P, (p + 1) T / P); run of block g = ceil((g + 1) P / T) - 1
-    const long long p_first = ((cb + 1) * P + T - 1) / T - 1;
-    const long long p_last = (ce * P + T - 1) / T - 1;
-    for (long long p = p_first; p <= p_last; ++p) {
-      const float4 m = *reinterpret_cast<const float4*>(a.part_m + (p + b) * kM + h0);
-      M[0] = fmaxf(M[0], m.x);
-      M[1] = fmaxf(M[1], m.y);
-      M[2] = fmaxf(M[2], m.z);
-      M[3] = fmaxf(M[3], m.w);
-    }
-    for (long long p = p_first; p <= p_last; ++p) {
-      const long long slot = p + b;
-      const float4 m = *reinterpret_cast<const float4*>(a.part_m + slot * kM + h0);
-      const float4 l = *reinterpret_cast<const float4*>(a.part_l + slot * kM + h0);
-      const float* src = a.part_o + slot * (kDC * kM) + static_cast<long long>(cb32 * 32 + cq * 8) * kM + h0;
-      float4 v[8];
+  for (long long q = p_first; q <= p_last; ++q) {
+    const long long slot = q == p_first ? slot_first : 2 * q;
+    const float4 m = *reinterpret_cast<const float4*>(a.part_m + slot * kM + h0);
+    M[0] = fmaxf(M[0], m.x);
+    M[1] = fmaxf(M[1], m.y);
+    M[2] = fmaxf(M[2], m.z);
+    M[3] = fmaxf(M[3], m.w);
+  }
+  for (long long q = p_first; q <= p_last; ++q) {
+    const long long slot = q == p_first ? slot_first : 2 * q;
+    const float4 m = *reinterpret_cast<const float4*>(a.part_m + slot * kM + h0);
+    const float4 l = *reinterpret_cast<const float4*>(a.part_l + slot * kM + h0);
+    const float* src = a.part_o + slot * (kDC * kM) + static_cast<long long>(cb32 * 32 + cq * 8) * kM + h0;
+    float4 v[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const float4*>(src + j * kM);
-      const float w[4] = {exp2f(m.x - M[0]), exp2f(m.y - M[1]), exp2f(m.z - M[2]), exp2f(m.w - M[3])};
-      L[0] = fmaf(w[0], l.x, L[0]);
-      L[1] = fmaf(w[1], l.y, L[1]);
-      L[2] = fmaf(w[2], l.z, L[2]);
-      L[3] = fmaf(w[3], l.w, L[3]);
+    for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const float4*>(src + j * kM);
+    const float w[4] = {exp2f(m.x - M[0]), exp2f(m.y - M[1]), exp2f(m.z - M[2]), exp2f(m.w - M[3])};
+    L[0] = fmaf(w[0], l.x, L[0]);
+    L[1] = fmaf(w[1], l.y, L[1]);
+    L[2] = fmaf(w[2], l.z, L[2]);
+    L[3] = fmaf(w[3], l.w, L[3]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        acc[j][0] = fmaf(w[0], v[j].x, acc[j][0]);
-        acc[j][1] = fmaf(w[1], v[j].y, acc[j][1]);
-        acc[j][2] = fmaf(w[2], v[j].z, acc[j][2]);
-        acc[j][3] = fmaf(w[3], v[j].w, acc[j][3]);
-      }
+    for (int j = 0; j < 8; ++j) {
+      acc[j][0] = fmaf(w[0], v[j].x, acc[j][0]);
+      acc[j][1] = fmaf(w[1], v[j].y, acc[j][1]);
+      acc[j][2] = fmaf(w[2], v[j].z, acc[j][2]);
+      acc[j][3] = fmaf(w[3], v[j].w, acc[j][3]);
     }
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float inv = any ? 1.f / L[i] : 0.f;
+    const float inv = 1.f / L[i];
     uint4 pk;
     pk.x = pack_bf16x2(acc[0][i] * inv, acc[1][i] * inv);
     pk.y = pack_bf16x2(acc[2][i] * inv, acc[3][i] * inv);
@@ -647,18 +735,18 @@ __global__ void __launch_bounds__(128) combine_kernel(const Args a, __nv_bfloat1
     pk.w = pack_bf16x2(acc[6][i] * inv, acc[7][i] * inv);
     *reinterpret_cast<uint4*>(s_o + (h0 + i) * kPitch + cq * 8) = pk;
   }
-  if (lse != nullptr && cb32 == 0 && cq == 0) {
+  if (a.lse != nullptr && cb32 == 0 && cq == 0) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
       if (h0 + i < a.H)
-        lse[static_cast<long long>(b) * a.H + h0 + i] = any ? (M[i] + log2f(L[i])) * 0.69314718055994531f : -INFINITY;
+        a.lse[static_cast<long long>(pr) * a.H + h0 + i] = (M[i] + log2f(L[i])) * 0.69314718055994531f;
   }
   __syncthreads();
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int id = k * 128 + t, row = id >> 2, q = id & 3;
     if (row < a.H)
-      *reinterpret_cast<uint4*>(o_lat + (static_cast<long long>(b) * a.H + row) * kDC + cb32 * 32 + q * 8) =
+      *reinterpret_cast<uint4*>(a.o_lat + (static_cast<long long>(pr) * a.H + row) * kDC + cb32 * 32 + q * 8) =
           *reinterpret_cast<const uint4*>(s_o + row * kPitch + q * 8);
   }
 }
@@ -687,12 +775,15 @@ struct WsLayout {
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-constexpr WsLayout ws_layout(int B) {
+// Workspace of a launch over np problems: header, block table, and two partial
+// slots per run (the problem holding the run's first block and the one cut at its
+// end).
+constexpr WsLayout ws_layout(long long np) {
   WsLayout w = {};
-  const size_t slots = static_cast<size_t>(kMaxPairs) + static_cast<size_t>(B);
+  const size_t slots = 2 * static_cast<size_t>(kMaxPairs);
   w.hdr = 0;
   w.cum = 256;
-  w.m = w.cum + align256(sizeof(int32_t) * (B + 1));
+  w.m = w.cum + align256(sizeof(int32_t) * static_cast<size_t>(np + 1));
   w.l = w.m + align256(sizeof(float) * slots * kM);
   w.o = w.l + align256(sizeof(float) * slots * kM);
   w.total = w.o + sizeof(float) * slots * kM * kDC;
@@ -728,11 +819,18 @@ static int pairs_for_device() {
 
 size_t decode_tc_workspace_size(int32_t B) { return dtc::ws_layout(B).total; }
 
-mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
-                            float scale, void* ws, size_t ws_bytes, void* o_lat, float* lse, cudaStream_t s) {
+size_t prefill_tc_workspace_size(int32_t B, int32_t S) {
+  return dtc::ws_layout(static_cast<long long>(B) * S).total;
+}
+
+static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dtc::Problems& pbs, long long np,
+                                 int32_t H, float scale, void* ws, size_t ws_bytes, void* o_lat, float* lse,
+                                 cudaStream_t s) {
   using namespace dtc;
-  const WsLayout w = ws_layout(c.B);
+  const WsLayout w = ws_layout(np);
   if (ws == nullptr || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MLA_ERR_WORKSPACE;
+  // block indices are 32-bit on the device
+  if (np * ((static_cast<long long>(c.N_max) + kBN - 1) / kBN) >= (1ll << 31)) return MLA_ERR_UNSUPPORTED;
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return MLA_ERR_CUDA;
   const int npairs = pairs_for_device();
@@ -754,8 +852,8 @@ mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   Args a;
   a.q_cat = static_cast<const __nv_bfloat16*>(q_cat);
-  a.seq_lens = seq_lens;
-  a.B = c.B;
+  a.pb = pbs;
+  a.NP = static_cast<int>(np);
   a.H = H;
   a.N_max = c.N_max;
   a.R = R;
@@ -766,6 +864,8 @@ mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t
   a.part_m = reinterpret_cast<float*>(wsb + w.m);
   a.part_l = reinterpret_cast<float*>(wsb + w.l);
   a.part_o = reinterpret_cast<float*>(wsb + w.o);
+  a.o_lat = static_cast<__nv_bfloat16*>(o_lat);
+  a.lse = lse;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * npairs, 1, 1);
@@ -781,9 +881,32 @@ mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel, map, a);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
-  dim3 grid(kDC / 32, c.B);
-  combine_kernel<<<grid, 128, 0, s>>>(a, static_cast<__nv_bfloat16*>(o_lat), lse);
+  dim3 grid(kDC / 32, npairs);
+  combine_kernel<<<grid, 128, 0, s>>>(a);
   return cuda_status(cudaGetLastError());
+}
+
+mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
+                            float scale, void* ws, size_t ws_bytes, void* o_lat, float* lse, cudaStream_t s) {
+  dtc::Problems p = {};
+  p.seq_lens = seq_lens;
+  p.q_start = nullptr;
+  p.S = 1;
+  p.causal = 0;
+  p.n_max = c.N_max;
+  return launch_attn_tc(q_cat, c, p, c.B, H, scale, ws, ws_bytes, o_lat, lse, s);
+}
+
+mla_status launch_prefill_tc(const void* q_cat, const mla_cache& c, const int32_t* q_start, int32_t S,
+                             int32_t causal, int32_t H, float scale, void* ws, size_t ws_bytes, void* o_lat,
+                             float* lse, cudaStream_t s) {
+  dtc::Problems p = {};
+  p.seq_lens = nullptr;
+  p.q_start = q_start;
+  p.S = S;
+  p.causal = causal != 0;
+  p.n_max = c.N_max;
+  return launch_attn_tc(q_cat, c, p, static_cast<long long>(c.B) * S, H, scale, ws, ws_bytes, o_lat, lse, s);
 }
 
 }  // namespace mla

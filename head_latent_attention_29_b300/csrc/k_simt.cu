@@ -324,21 +324,25 @@ __device__ __forceinline__ float block_reduce_sum128(float v, float* red) {
 __global__ void __launch_bounds__(128) decode_f32_kernel(const float* __restrict__ q_cat,
                                                          const float* __restrict__ cache, int32_t N_max,
                                                          int32_t d_c, int32_t d_r, int64_t row_stride,
-                                                         const int32_t* __restrict__ seq_lens, int32_t H,
-                                                         float scale, float* __restrict__ o_lat,
-                                                         float* __restrict__ lse) {
+                                                         const int32_t* __restrict__ seq_lens,
+                                                         const int32_t* __restrict__ q_start, int32_t S,
+                                                         int32_t causal, int32_t H, float scale,
+                                                         float* __restrict__ o_lat, float* __restrict__ lse) {
   extern __shared__ float sm[];
   const int R = d_c + d_r;
   float* qs = sm;           // [R]
   float* ps = sm + R;       // [128]
   float* red = ps + 128;    // [4]
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  int n = seq_lens[b];
+  // problem pr: decode sequence pr (q_start == nullptr), or query pr % S of
+  // sequence pr / S reading start + pr % S + 1 rows (causal) or start + S rows
+  const int pr = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int b = q_start == nullptr ? pr : pr / S;
+  int n = q_start == nullptr ? seq_lens[pr] : q_start[b] + (causal ? pr - b * S + 1 : S);
   if (n < 0 || n > N_max) {
     if (tid == 0) record_error(MLA_ERR_DEVICE_INDEX, kSiteDecodeLength);
     n = n < 0 ? 0 : N_max;
   }
-  for (int k = tid; k < R; k += 128) qs[k] = q_cat[(static_cast<int64_t>(b) * H + h) * R + k];
+  for (int k = tid; k < R; k += 128) qs[k] = q_cat[(static_cast<int64_t>(pr) * H + h) * R + k];
   __syncthreads();
   constexpr int kMaxPer = 8;  // d_c <= 1024
   float acc[kMaxPer];
@@ -381,18 +385,28 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const float* __restrict
 #pragma unroll
   for (int i = 0; i < kMaxPer; ++i) {
     const int c = tid + 128 * i;
-    if (c < d_c) o_lat[(static_cast<int64_t>(b) * H + h) * d_c + c] = acc[i] * inv;
+    if (c < d_c) o_lat[(static_cast<int64_t>(pr) * H + h) * d_c + c] = acc[i] * inv;
   }
-  if (lse != nullptr && tid == 0) lse[static_cast<int64_t>(b) * H + h] = n > 0 ? m + logf(l) : -INFINITY;
+  if (lse != nullptr && tid == 0) lse[static_cast<int64_t>(pr) * H + h] = n > 0 ? m + logf(l) : -INFINITY;
 }
 
 mla_status launch_decode_f32(const float* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
                              float scale, float* o_lat, float* lse, cudaStream_t s) {
   const int R = c.d_c + c.d_r;
   const size_t smem = sizeof(float) * (R + 128 + 4);
-  dim3 grid(H, c.B);
+  dim3 grid(c.B, H);
   decode_f32_kernel<<<grid, 128, smem, s>>>(q_cat, static_cast<const float*>(c.data), c.N_max, c.d_c, c.d_r,
-                                            c.row_stride, seq_lens, H, scale, o_lat, lse);
+                                            c.row_stride, seq_lens, nullptr, 1, 0, H, scale, o_lat, lse);
+  return cuda_status(cudaGetLastError());
+}
+
+mla_status launch_prefill_f32(const float* q_cat, const mla_cache& c, const int32_t* q_start, int32_t S,
+                              int32_t causal, int32_t H, float scale, float* o_lat, float* lse, cudaStream_t s) {
+  const int R = c.d_c + c.d_r;
+  const size_t smem = sizeof(float) * (R + 128 + 4);
+  dim3 grid(static_cast<unsigned>(c.B) * S, H);
+  decode_f32_kernel<<<grid, 128, smem, s>>>(q_cat, static_cast<const float*>(c.data), c.N_max, c.d_c, c.d_r,
+                                            c.row_stride, nullptr, q_start, S, causal, H, scale, o_lat, lse);
   return cuda_status(cudaGetLastError());
 }
 

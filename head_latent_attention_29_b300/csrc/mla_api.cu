@@ -100,6 +100,34 @@ MLA_API mla_status mla_decode_attn(const void* q_cat, const mla_cache* cache, co
                                as_stream(stream));
 }
 
+MLA_API size_t mla_prefill_workspace_size(int32_t B, int32_t S, int32_t H, int32_t d_c, int32_t dtype) {
+  if (B <= 0 || S <= 0 || H <= 0 || d_c <= 0) return 0;
+  if (dtype == MLA_F32) return 256;
+  if (dtype == MLA_BF16 && d_c == 512 && H <= 128) return mla::prefill_tc_workspace_size(B, S);
+  return 0;
+}
+
+MLA_API mla_status mla_prefill_attn(const void* q_cat, const mla_cache* cache, const int32_t* q_start, int32_t S,
+                                    int32_t H, float scale, int32_t causal, void* workspace,
+                                    size_t workspace_bytes, void* o_lat, float* lse, void* stream) {
+  mla_status st = check_cache(cache);
+  if (st != MLA_OK) return st;
+  if (q_cat == nullptr || q_start == nullptr || o_lat == nullptr || H <= 0 || S <= 0) return MLA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_cat) || !aligned16(o_lat)) return MLA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) && !(scale < 0.f) && scale != 0.f) return MLA_ERR_INVALID_ARG;  // NaN
+  if (S > cache->N_max) return MLA_ERR_INVALID_ARG;
+  if (static_cast<long long>(cache->B) * S > 0x7fffffffll) return MLA_ERR_UNSUPPORTED;
+  if (cache->dtype == MLA_F32) {
+    if (cache->d_c > 1024 || cache->d_r > 256 || H > 65535) return MLA_ERR_UNSUPPORTED;
+    return mla::launch_prefill_f32(static_cast<const float*>(q_cat), *cache, q_start, S, causal, H, scale,
+                                   static_cast<float*>(o_lat), lse, as_stream(stream));
+  }
+  if (cache->d_c != 512 || (cache->d_r != 0 && cache->d_r != 64) || H > 128) return MLA_ERR_UNSUPPORTED;
+  return mla::launch_prefill_tc(q_cat, *cache, q_start, S, causal, H, scale, workspace, workspace_bytes, o_lat,
+                                lse, as_stream(stream));
+}
+
 MLA_API mla_status mla_out_up(const void* o_lat, const void* w_uv, void* o, int32_t B, int32_t H, int32_t d_c,
                               int32_t d_v, int32_t dtype, void* stream) {
   if (!valid_dtype(dtype)) return MLA_ERR_INVALID_ARG;

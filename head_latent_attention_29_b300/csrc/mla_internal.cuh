@@ -85,9 +85,16 @@ mla_status launch_out_up_tc(const void* o_lat, const void* w_uv, void* o, int32_
 mla_status launch_decode_f32(const float* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
                              float scale, float* o_lat, float* lse, cudaStream_t s);
 
-// tensor-core decode (bf16): sizes and launch
+mla_status launch_prefill_f32(const float* q_cat, const mla_cache& c, const int32_t* q_start, int32_t S,
+                              int32_t causal, int32_t H, float scale, float* o_lat, float* lse, cudaStream_t s);
+
+// tensor-core decode and prefill (bf16): sizes and launch
 size_t decode_tc_workspace_size(int32_t B);
+size_t prefill_tc_workspace_size(int32_t B, int32_t S);
 mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
                             float scale, void* ws, size_t ws_bytes, void* o_lat, float* lse, cudaStream_t s);
+mla_status launch_prefill_tc(const void* q_cat, const mla_cache& c, const int32_t* q_start, int32_t S,
+                             int32_t causal, int32_t H, float scale, void* ws, size_t ws_bytes, void* o_lat,
+                             float* lse, cudaStream_t s);
 
 }  // namespace mla

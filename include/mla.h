@@ -158,6 +158,41 @@ MLA_API mla_status mla_decode_attn(const void* q_cat, const mla_cache* cache,
                                    float* lse, void* stream);
 
 /*
+ * mla_prefill_workspace_size -- bytes of device workspace mla_prefill_attn needs
+ * for B sequences of S queries each (block table and the partials of queries
+ * whose rows are split across the GPU).  Returns 0 if the shape is unsupported.
+ */
+MLA_API size_t mla_prefill_workspace_size(int32_t B, int32_t S, int32_t H, int32_t d_c, int32_t dtype);
+
+/*
+ * mla_prefill_attn -- absorbed attention of a whole prompt over the latent cache.
+ *   Prefill processes every prompt token at once (hotelren.com guide, section 2.1)
+ *   with the absorbed query of each token (0539edu.com sections 3.1-3.2: the
+ *   absorbed query and c_KV keep their [batch, seq, ...] shape).  The prompt's own
+ *   rows must already be in the cache (mla_cache_append).  For sequence b, query i
+ *   (position start = q_start[b] + i) and head h, with
+ *   n = start + 1 rows if causal (rows 0..start: the diagonal is included) and
+ *   n = q_start[b] + S rows otherwise:
+ *     s_t  = scale * ( q_cat[b][i][h] . cache[b][t] ),  t < n
+ *     o_lat[b][i][h] = sum_t softmax_t(s)_t * cache[b][t][0 : d_c]
+ *     lse[b][i][h]   = ln sum_t exp(s_t)
+ *   Every (b, i) is one attention problem with all H heads as the MMA rows; the
+ *   rows of all problems are cut into equal runs across the GPU, exactly as in
+ *   mla_decode_attn.
+ *   q_cat     [B, S, H, d_c + d_r]  dtype = cache->dtype
+ *   q_start   [B] int32 device; 0 <= q_start[b] and q_start[b] + S <= N_max,
+ *             else the lengths are clamped and MLA_ERR_DEVICE_INDEX is recorded.
+ *   causal    1: query i sees rows up to its own position; 0: all q_start[b] + S rows.
+ *   workspace device scratch of at least mla_prefill_workspace_size() bytes,
+ *             256-byte aligned (bf16 path; the f32 path ignores it).
+ *   o_lat     [B, S, H, d_c] dtype (output);  lse [B, S, H] float32 or NULL.
+ *   Shapes as mla_decode_attn; B * S * ceil(N_max / 64) must stay below 2^31.
+ */
+MLA_API mla_status mla_prefill_attn(const void* q_cat, const mla_cache* cache, const int32_t* q_start,
+                                    int32_t S, int32_t H, float scale, int32_t causal, void* workspace,
+                                    size_t workspace_bytes, void* o_lat, float* lse, void* stream);
+
+/*
  * mla_out_up -- apply W_UV after attention, per head:
  *   o[b][h][d] = sum_c o_lat[b][h][c] * W_UV[h][d][c]
  *   (0539edu.com section 3.1, attn v = (attn c_KV) W_UV; weight view [h, d_v, d_c]
@@ -185,7 +220,7 @@ MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, 
  *   allocator that cannot be re-entered) or embedders that only own the input and
  *   output buffers.  This entry point computes exactly what mla_decode_attn does,
  *   with the same kernels, but takes the split-KV scratch from a buffer built into
- *   the library (about 50 MB per GPU that loads the library, held until the
+ *   the library (about 42 MB per GPU that loads the library, held until the
  *   process exits), so it allocates nothing.
  *   Arguments are those of mla_decode_attn minus the workspace.  Limits: bf16 cache
  *   only (MLA_ERR_UNSUPPORTED otherwise) and at most 32 sequences (cache->B > 32
