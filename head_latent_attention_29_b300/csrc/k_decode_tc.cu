@@ -78,8 +78,10 @@ constexpr int kOffRope = kStages * kStageDC;           // score CTA: kStages x 8
 constexpr int kOffX = kOffRope + kStages * kChunk;     // score CTA: reference exchange between groups
 constexpr int kOffP = kStagesO * kStageDC;             // output CTA: kPBufs P tiles
 constexpr int kOffRef = kOffP + kPBufs * kPBytes;      // output CTA: kPBufs x 128 references
-constexpr int kOffBar = (kOffX + kRefBytes > kOffRef + kPBufs * kRefBytes) ? kOffX + kRefBytes
-                                                                            : kOffRef + kPBufs * kRefBytes;
+constexpr int kOffEpi = kOffRef + kPBufs * kRefBytes;  // output CTA: per-row (m, l) for the epilogue helpers
+constexpr int kOffBar = (kOffX + kRefBytes > kOffEpi + 2 * kRefBytes) ? kOffX + kRefBytes : kOffEpi + 2 * kRefBytes;
+constexpr int kQBoxBytes = kM * 128;                   // one 64-column TMA box of the query (128 rows)
+static_assert(9 * kQBoxBytes <= kStages * kStageDC, "the run's first query is staged in the ring");
 static_assert(kOffP % 1024 == 0, "P tiles must sit on 1024-byte boundaries");
 enum : int {
   kBarFull = 0,                       // [kStages] stage landed
@@ -93,7 +95,10 @@ enum : int {
   kBarPvGo = kBarPFull + kPBufs,      // [kPBufs] output: block may be multiplied
   kBarODone = kBarPvGo + kPBufs,      // [kPBufs] output: PV of a block completed
   kBarDrain = kBarODone + kPBufs,     // MMA drain at teardown
-  kNumBars = kBarDrain + 1,
+  kBarQFull = kBarDrain + 1,          // score: the run's first query staged in shared memory by TMA
+  kBarEpiGo = kBarQFull + 1,          // output: (m, l) of a finished problem published to the helper warps
+  kBarEpiDone = kBarEpiGo + 1,        // output: the helpers' half of the output is out of tensor memory
+  kNumBars = kBarEpiDone + 1,
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffMisc + 128;
@@ -139,6 +144,7 @@ struct Args {
   float scale_log2;            // scale * log2(e)
   int32_t* hdr;                // workspace: [0] total blocks, [1] runs used, [2] problems with no rows
   int32_t* cum;                // workspace: [NP + 1] first block of each problem
+  int32_t* bnd;                // workspace: [kMaxPairs][3] problem holding each run's first block, its cum, end
   float* part_m;               // [2 kMaxPairs][128] running max (log2 units)
   float* part_l;               // [2 kMaxPairs][128] running sum
   float* part_o;               // [2 kMaxPairs][512][128] unnormalised output, latent-column major
@@ -185,7 +191,7 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base
 // run's [lo, hi), and the problem that holds block lo.  One warp.  The writer of
 // the table (one CTA per launch) also checks every length and counts the problems
 // with no rows.
-__device__ void plan_run(const Args& a, Misc* misc, bool write_table) {
+__device__ void plan_run(const Args& a, Misc* misc, bool write_table, bool write_bnd) {
   const int lane = threadIdx.x & 31;
   long long T = 0;
   int empties = 0;
@@ -248,6 +254,12 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table) {
     misc->b0 = b0;
     misc->cum0 = cum0;
     misc->len0 = len0;
+    if (write_bnd && lo < hi) {
+      int32_t* e = a.bnd + 3 * cluster_id_x();
+      e[0] = b0;
+      e[1] = static_cast<int32_t>(cum0);
+      e[2] = static_cast<int32_t>(cum0 + (len0 + kBN - 1) / kBN);
+    }
     if (write_table) {
       a.cum[a.NP] = static_cast<int32_t>(T);
       a.hdr[0] = static_cast<int32_t>(T);
@@ -257,10 +269,57 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table) {
   }
 }
 
+// Slot of the piece of problem c.b that ends this run: 2 p for the problem that holds
+// the run's first block (b0), 2 p + 1 for the one cut at the run's end.
+__device__ __forceinline__ long long piece_slot(const Cursor& c, int b0) {
+  return 2 * static_cast<long long>(cluster_id_x()) + (c.b == b0 ? 0 : 1);
+}
+
+// Write latent columns [col0, col0 + 256) of row r of the finished problem c.b from
+// tensor memory: o = O / l in bf16 if the whole problem ran here, else the
+// unnormalised fp32 piece ([column][head] in its slot, a warp storing 128
+// contiguous bytes per column).
+__device__ __forceinline__ void store_output(const Args& a, const Cursor& c, int b0, uint32_t trow, int r, float l,
+                                             int col0) {
+  if (c.whole()) {
+    const float inv = 1.f / l;
+    uint4* dst = reinterpret_cast<uint4*>(a.o_lat + (static_cast<long long>(c.b) * a.H + r) * kDC + col0);
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t v[64];
+      tmem_ld64(trow + col0 + cc * 64, v);
+      tmem_wait_ld();
+      if (r < a.H) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
+          dst[cc * 8 + q] = w;
+        }
+      }
+    }
+  } else {
+    float* dst = a.part_o + piece_slot(c, b0) * (kDC * kM) + static_cast<long long>(col0) * kM + r;
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t v[64];
+      tmem_ld64(trow + col0 + cc * 64, v);
+      tmem_wait_ld();
+      if (r < a.H) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) dst[(cc * 64 + j) * kM] = __uint_as_float(v[j]);
+      }
+    }
+  }
+}
+
 // Role map (12 warps).  Score CTA: warp 0 TMA, warp 1 S MMA, warp 2 run planning,
 // warps 4-7 softmax group A (even blocks), warps 8-11 softmax group B (odd blocks).
-// Output CTA: warp 0 TMA, warp 1 PV MMA, warps 4-7 correction + epilogue.
+// Output CTA: warp 0 TMA, warp 1 PV MMA, warps 4-7 correction + epilogue (latent
+// columns 0..255), warps 8-11 epilogue (columns 256..511).
 __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_constant__ CUtensorMap map,
+                                                                   const __grid_constant__ CUtensorMap qmap,
                                                                    const Args a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -294,21 +353,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     }
     mbar_init(bar_addr(sbase, kBarQReady), 128);
     mbar_init(bar_addr(sbase, kBarDrain), 1);
+    mbar_init(bar_addr(sbase, kBarQFull), 1);
+    mbar_init(bar_addr(sbase, kBarEpiGo), 128);
+    mbar_init(bar_addr(sbase, kBarEpiDone), 128);
     misc->abort = 0;
     if (!score_cta) {  // the first kPBufs P tiles are expected before any is sent
       for (int i = 0; i < kPBufs; ++i) mbar_arrive_expect_tx(bar_addr(sbase, kBarPFull + i), kPTxBytes);
     }
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&map);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map);
+    tma_prefetch_desc(&qmap);
+  }
   if (warp == 1) {
     tmem_alloc(sbase + kOffMisc + offsetof(Misc, tmem), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 2) plan_run(a, misc, cluster_id_x() == 0 && score_cta);
+  if (threadIdx.x == 0) MLA_TRACE_POINT(63, score_cta ? 0 : 2);
+  if (warp == 2) plan_run(a, misc, cluster_id_x() == 0 && score_cta, score_cta);
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // peer barriers initialised before any remote arrive
+  if (threadIdx.x == 0) MLA_TRACE_POINT(63, score_cta ? 1 : 3);
 
   const uint32_t tmem = misc->tmem;
   const int nch = a.nch;
@@ -320,8 +387,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     const int nst = score_cta ? kStages : kStagesO;
     Cursor c;
     c.start(*misc, a.pb);
-    // the score CTA's query goes out before the cache stream floods the memory system
-    if (score_cta && c.ok()) warp_wait(bar_addr(sbase, kBarQReady), 0, abort);
+    // the run's first query goes out before the cache stream floods the memory system:
+    // 64-column boxes of its 128 rows into the (still empty) ring, which the softmax
+    // threads move into tensor memory; the ring is reused once they are done
+    if (score_cta && c.ok()) {
+      mbar_arrive_expect_tx_if(leader, bar_addr(sbase, kBarQFull), nch * kQBoxBytes);
+      for (int ch = 0; ch < nch; ++ch)
+        tma_load_2d_if(leader, sbase + kOffStage + ch * kQBoxBytes, &qmap, bar_addr(sbase, kBarQFull), ch * 64,
+                       c.b * a.H);
+      warp_wait(bar_addr(sbase, kBarQReady), 0, abort);
+    }
     for (int k = 0; c.ok(); c.next(), ++k) {
       const int st = k % nst;
       if (!warp_wait(bar_addr(sbase, kBarEmpty + st), ((k / nst) & 1) ^ 1, abort)) break;
@@ -421,9 +496,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         // the previous block's S product (other group, older query) must be finished
         if (k > 0 && !warp_wait(bar_addr(sbase, kBarSFull + (k - 1) % kSBufs), ((k - 1) / kSBufs) & 1, abort)) break;
         if (r == 0) MLA_TRACE_POINT(k, 9);
-        // query of this sequence into tensor memory (rows >= H are zero)
+        if (k == 0) {
+          // the run's first query, staged by TMA (128-byte swizzle: piece j of row r at
+          // r * 128 + ((j ^ r % 8) * 16), so a warp's reads hit distinct banks)
+          if (!warp_wait(bar_addr(sbase, kBarQFull), 0, abort)) break;
+          const uint8_t* qrow = gbase + kOffStage + r * 128;
+          for (int j0 = 0; j0 < nch; ++j0) {
+            uint32_t v[32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint4 x = *reinterpret_cast<const uint4*>(qrow + j0 * kQBoxBytes + ((u ^ (r & 7)) << 4));
+              v[4 * u] = x.x;
+              v[4 * u + 1] = x.y;
+              v[4 * u + 2] = x.z;
+              v[4 * u + 3] = x.w;
+            }
+            tmem_st32(tmem + lane_off + kColQ + j0 * 32, v);
+          }
+        }
+        // a later query of the run, read straight from global memory (rows >= H are zero)
         const uint4* src = reinterpret_cast<const uint4*>(a.q_cat + (static_cast<long long>(c.b) * a.H + r) * a.R);
-        for (int j0 = 0; j0 < nch; j0 += 3) {  // three 128-byte pieces of the row in flight at once
+        for (int j0 = (k == 0 ? nch : 0); j0 < nch; j0 += 3) {  // three 128-byte pieces of the row in flight at once
           uint4 x[24];
 #pragma unroll
           for (int u = 0; u < 24; ++u) {
@@ -519,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     Cursor c;
     c.start(*misc, a.pb);
     float m = 0.f, l = 0.f;
-    int k = 0;
+    int k = 0, n_epi = 0;
     for (; c.ok(); c.next(), ++k) {
       const int pb = k % kPBufs, st = k % kStagesO;
       if (!warp_wait<true>(bar_addr(sbase, kBarPFull + pb), (k / kPBufs) & 1, abort)) break;
@@ -582,51 +675,48 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       if (c.last()) {
         if (!warp_wait(bar_addr(sbase, kBarODone + pb), (k / kPBufs) & 1, abort)) break;
         if (r == 0) MLA_TRACE_POINT(k, 11);
+        // the row's (m, l) to the helper warps, which write latent columns 256..511
+        float* epi = reinterpret_cast<float*>(gbase + kOffEpi);
+        epi[r] = m;
+        epi[kM + r] = l;
+        mbar_arrive(bar_addr(sbase, kBarEpiGo));
         tc_fence_after();
-        if (c.whole()) {
-          // the whole problem ran here: o = O / l in bf16, lse = (m + log2 l) ln 2
-          const float inv = 1.f / l;
-          uint4* dst = reinterpret_cast<uint4*>(a.o_lat + (static_cast<long long>(c.b) * a.H + r) * kDC);
-          for (int cc = 0; cc < 8; ++cc) {
-            uint32_t v[64];
-            tmem_ld64(tmem + lane_off + cc * 64, v);
-            tmem_wait_ld();
-            if (r < a.H) {
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                uint4 w;
-                w.x = pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
-                w.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
-                w.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
-                w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
-                dst[cc * 8 + q] = w;
-              }
-            }
-          }
-          if (r < a.H && a.lse != nullptr)
-            a.lse[static_cast<long long>(c.b) * a.H + r] = (m + log2f(l)) * 0.69314718055994531f;
-        } else {
-          // a piece of a problem cut by run boundaries: slot 2 p for the problem that
-          // holds the run's first block, 2 p + 1 for the one cut at the run's end
-          const long long slot = 2 * static_cast<long long>(cluster_id_x()) + (c.b == misc->b0 ? 0 : 1);
-          float* dst = a.part_o + slot * (kDC * kM) + r;  // [c][h]: a warp stores 128 contiguous bytes
-          for (int cc = 0; cc < 8; ++cc) {
-            uint32_t v[64];
-            tmem_ld64(tmem + lane_off + cc * 64, v);
-            tmem_wait_ld();
-            if (r < a.H) {
-#pragma unroll
-              for (int j = 0; j < 64; ++j) dst[(cc * 64 + j) * kM] = __uint_as_float(v[j]);
-            }
-          }
-          if (r < a.H) {
+        store_output(a, c, misc->b0, tmem + lane_off, r, l, 0);
+        if (r < a.H) {
+          if (c.whole()) {
+            if (a.lse != nullptr) a.lse[static_cast<long long>(c.b) * a.H + r] = (m + log2f(l)) * 0.69314718055994531f;
+          } else {
+            const long long slot = piece_slot(c, misc->b0);
             a.part_m[slot * kM + r] = m;
             a.part_l[slot * kM + r] = l;
           }
         }
         tc_fence_before();
+        // O is overwritten by the next problem's first PV only after both halves are out
+        if (!warp_wait(bar_addr(sbase, kBarEpiDone), n_epi & 1, abort)) break;
+        ++n_epi;
         if (r == 0) MLA_TRACE_POINT(k, 12);
       }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ output CTA: epilogue helpers
+    // Warps 8-11 see the same TMEM lanes as warps 4-7 and write the upper half of the
+    // latent columns of every finished problem.
+    const int r = threadIdx.x - 256;
+    const uint32_t lane_off = static_cast<uint32_t>(r & ~31) << 16;
+    const float* epi = reinterpret_cast<const float*>(gbase + kOffEpi);
+    Cursor c;
+    c.start(*misc, a.pb);
+    int n_epi = 0;
+    for (; c.ok(); c.next()) {
+      if (!c.last()) continue;
+      if (!warp_wait(bar_addr(sbase, kBarEpiGo), n_epi & 1, abort)) break;
+      const float l = epi[kM + r];
+      tc_fence_after();
+      store_output(a, c, misc->b0, tmem + lane_off, r, l, kDC / 2);
+      tc_fence_before();
+      mbar_arrive(bar_addr(sbase, kBarEpiDone));
+      ++n_epi;
     }
   }
 
@@ -638,18 +728,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     tmem_dealloc(tmem, kTmemCols);
   }
   cluster_sync();  // no remote access into a CTA that has exited
-}
-
-// Largest problem pr with cum[pr] <= g for a block g < T; it has rows (an empty
-// problem shares its cum with the next one).
-__device__ __forceinline__ int problem_of_block(const int32_t* cum, int np, long long g) {
-  int lo = 0, hi = np;  // cum[lo] <= g < cum[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (cum[mid] <= g) lo = mid;
-    else hi = mid;
-  }
-  return lo;
 }
 
 // Merge the pieces of every problem cut by run boundaries: M = max m_s,
@@ -680,8 +758,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const Args a) {
   }
   if (p >= P) return;
   const long long lo_p = p * T / P;
-  const int pr = problem_of_block(a.cum, a.NP, lo_p);
-  const long long cb = a.cum[pr], ce = a.cum[pr + 1];
+  const int pr = a.bnd[3 * p];  // the problem that holds run p's first block, its first block and end
+  const long long cb = a.bnd[3 * p + 1], ce = a.bnd[3 * p + 2];
   if (cb == lo_p) return;  // the boundary falls between problems
   // run q covers blocks [q T / P, (q + 1) T / P); run of block g = ceil((g + 1) P / T) - 1
   const long long p_first = ((cb + 1) * P + T - 1) / T - 1;
@@ -770,7 +848,7 @@ static EncodeTiledFn encode_fn() {
 }
 
 struct WsLayout {
-  size_t hdr, cum, m, l, o, total;
+  size_t hdr, bnd, cum, m, l, o, total;
 };
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -782,7 +860,8 @@ constexpr WsLayout ws_layout(long long np) {
   WsLayout w = {};
   const size_t slots = 2 * static_cast<size_t>(kMaxPairs);
   w.hdr = 0;
-  w.cum = 256;
+  w.bnd = 256;
+  w.cum = w.bnd + align256(sizeof(int32_t) * 3 * kMaxPairs);
   w.m = w.cum + align256(sizeof(int32_t) * static_cast<size_t>(np + 1));
   w.l = w.m + align256(sizeof(float) * slots * kM);
   w.o = w.l + align256(sizeof(float) * slots * kM);
@@ -849,6 +928,17 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return MLA_ERR_INVALID_ARG;
 
+  // the queries as [NP * H rows][R] for the TMA staging of each run's first query
+  CUtensorMap qmap;
+  const cuuint64_t qdim[2] = {static_cast<cuuint64_t>(R), static_cast<cuuint64_t>(np) * static_cast<cuuint64_t>(H)};
+  const cuuint64_t qstride[1] = {static_cast<cuuint64_t>(R) * 2};
+  const cuuint32_t qbox[2] = {64, static_cast<cuuint32_t>(kM)};
+  const cuuint32_t qes[2] = {1, 1};
+  if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q_cat), qdim, qstride, qbox, qes,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MLA_ERR_INVALID_ARG;
+
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   Args a;
   a.q_cat = static_cast<const __nv_bfloat16*>(q_cat);
@@ -861,6 +951,7 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   a.scale_log2 = scale * 1.4426950408889634f;
   a.hdr = reinterpret_cast<int32_t*>(wsb + w.hdr);
   a.cum = reinterpret_cast<int32_t*>(wsb + w.cum);
+  a.bnd = reinterpret_cast<int32_t*>(wsb + w.bnd);
   a.part_m = reinterpret_cast<float*>(wsb + w.m);
   a.part_l = reinterpret_cast<float*>(wsb + w.l);
   a.part_o = reinterpret_cast<float*>(wsb + w.o);
@@ -879,7 +970,7 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel, map, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel, map, qmap, a);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   dim3 grid(kDC / 32, npairs);
   combine_kernel<<<grid, 128, 0, s>>>(a);
