@@ -501,7 +501,8 @@ def run_b300_prefill(args, rank, world, device):
     t_tc = flops / (tc_burst * 1e12)
     t_mem = bytes_alg / (hbm * 1e9)
     return {
-        "metric": "MLA causal prefill prompt tokens/s at H=128,d_c=512,B=4,S=8192 bf16; % of roofline",
+        "metric": f"MLA causal prefill prompt tokens/s at H={cfg['H']},d_c={cfg['d_c']},B={cfg['B']},S={cfg['S']} bf16; "
+                  "% of roofline",
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
@@ -642,7 +643,8 @@ def run_reference(args, rank, world):
     v = statistics.median(vals)
     cb = dict(steps[-1])
     cb["value"] = round(v, 3)
-    metric = ("MLA causal prefill prompt tokens/s at H=128,d_c=512,B=4,S=8192 bf16; % of roofline" if prefill
+    metric = (f"MLA causal prefill prompt tokens/s at H={cfg['H']},d_c={cfg['d_c']},B={cfg['B']},S={cfg['S']} bf16; "
+              "% of roofline" if prefill
               else "MLA decode tokens/s at H=128,d_c=512,B=32,N=4K bf16; % of roofline")
     tokens_per_step = cfg["B"] * cfg.get("S", 1)
     return {

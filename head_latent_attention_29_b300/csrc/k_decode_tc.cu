@@ -79,9 +79,13 @@ constexpr int kOffX = kOffRope + kStages * kChunk;     // score CTA: reference e
 constexpr int kOffP = kStagesO * kStageDC;             // output CTA: kPBufs P tiles
 constexpr int kOffRef = kOffP + kPBufs * kPBytes;      // output CTA: kPBufs x 128 references
 constexpr int kOffEpi = kOffRef + kPBufs * kRefBytes;  // output CTA: per-row (m, l) for the epilogue helpers
+constexpr int kStgPitch = 80;                          // output CTA: staged bf16 output rows (32 columns + pad)
+constexpr int kStgBytes = kM * kStgPitch;
+constexpr int kOffStg = kOffEpi + 2 * kRefBytes;       // output CTA: two staging tiles (one per epilogue group)
 constexpr int kOffBar = (kOffX + kRefBytes > kOffEpi + 2 * kRefBytes) ? kOffX + kRefBytes : kOffEpi + 2 * kRefBytes;
 constexpr int kQBoxBytes = kM * 128;                   // one 64-column TMA box of the query (128 rows)
 static_assert(9 * kQBoxBytes <= kStages * kStageDC, "the run's first query is staged in the ring");
+static_assert(kOffStg + 2 * kStgBytes <= kOffBar && kOffStg % 16 == 0, "output staging tiles");
 static_assert(kOffP % 1024 == 0, "P tiles must sit on 1024-byte boundaries");
 enum : int {
   kBarFull = 0,                       // [kStages] stage landed
@@ -280,25 +284,38 @@ __device__ __forceinline__ long long piece_slot(const Cursor& c, int b0) {
 // unnormalised fp32 piece ([column][head] in its slot, a warp storing 128
 // contiguous bytes per column).
 __device__ __forceinline__ void store_output(const Args& a, const Cursor& c, int b0, uint32_t trow, int r, float l,
-                                             int col0) {
+                                             int col0, uint8_t* smem_gen) {
   if (c.whole()) {
+    // o = O / l in bf16 through a shared-memory tile per 32 columns, so that a warp
+    // writes 8 runs of 64 contiguous bytes (row r of the tile: 80-byte pitch, so the
+    // 16-byte writes of 8 consecutive rows hit distinct banks)
     const float inv = 1.f / l;
-    uint4* dst = reinterpret_cast<uint4*>(a.o_lat + (static_cast<long long>(c.b) * a.H + r) * kDC + col0);
-    for (int cc = 0; cc < 4; ++cc) {
-      uint32_t v[64];
-      tmem_ld64(trow + col0 + cc * 64, v);
+    uint8_t* stg = smem_gen + kOffStg + (col0 != 0 ? kStgBytes : 0);
+    const uint32_t bar_id = col0 != 0 ? 2u : 1u;
+    __nv_bfloat16* orow = a.o_lat + static_cast<long long>(c.b) * a.H * kDC + col0;
+    for (int cc = 0; cc < 8; ++cc) {
+      uint32_t v[32];
+      tmem_ld32(trow + col0 + cc * 32, v);
       tmem_wait_ld();
-      if (r < a.H) {
+      uint4* srow = reinterpret_cast<uint4*>(stg + r * kStgPitch);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
-          dst[cc * 8 + q] = w;
-        }
+      for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
+        w.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
+        w.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
+        w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
+        srow[q] = w;
       }
+      named_sync(bar_id, 128);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int id = k * 128 + r, row = id >> 2, q = id & 3;
+        if (row < a.H)
+          *reinterpret_cast<uint4*>(orow + static_cast<long long>(row) * kDC + cc * 32 + q * 8) =
+              *reinterpret_cast<const uint4*>(stg + row * kStgPitch + q * 16);
+      }
+      named_sync(bar_id, 128);
     }
   } else {
     float* dst = a.part_o + piece_slot(c, b0) * (kDC * kM) + static_cast<long long>(col0) * kM + r;
@@ -399,6 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     }
     for (int k = 0; c.ok(); c.next(), ++k) {
       const int st = k % nst;
+      // while a problem streams, the next problem's query moves into L2 (it is read
+      // from global memory when that problem starts mid-run)
+      if (score_cta && c.first() && c.b + 1 < a.NP)
+        prefetch_l2_bulk_if(leader, a.q_cat + static_cast<long long>(c.b + 1) * a.H * a.R,
+                            static_cast<uint32_t>(a.H * a.R * 2));
       if (!warp_wait(bar_addr(sbase, kBarEmpty + st), ((k / nst) & 1) ^ 1, abort)) break;
       MLA_TRACE_POINT(k, score_cta ? 8 : 7);
       mbar_arrive_expect_tx_if(leader, bar_addr(sbase, kBarFull + st), nload * kChunk);
@@ -624,18 +646,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         const int kp = k - 1;  // PV of the previous block has to be complete
         if (!warp_wait(bar_addr(sbase, kBarODone + kp % kPBufs), (kp / kPBufs) & 1, abort)) break;
         tc_fence_after();
-        for (int cc = 0; cc < 8; ++cc) {
-          uint32_t v[64];
-          tmem_ld64(tmem + lane_off + cc * 64, v);
+        for (int cc = 0; cc < 16; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + cc * 32, v);
           tmem_wait_ld();
-          uint32_t lo32[32], hi32[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            lo32[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-            hi32[j] = __float_as_uint(__uint_as_float(v[32 + j]) * alpha);
-          }
-          tmem_st32(tmem + lane_off + cc * 64, lo32);
-          tmem_st32(tmem + lane_off + cc * 64 + 32, hi32);
+          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+          tmem_st32(tmem + lane_off + cc * 32, v);
         }
         tmem_wait_st();
       }
@@ -681,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         epi[kM + r] = l;
         mbar_arrive(bar_addr(sbase, kBarEpiGo));
         tc_fence_after();
-        store_output(a, c, misc->b0, tmem + lane_off, r, l, 0);
+        store_output(a, c, misc->b0, tmem + lane_off, r, l, 0, gbase);
         if (r < a.H) {
           if (c.whole()) {
             if (a.lse != nullptr) a.lse[static_cast<long long>(c.b) * a.H + r] = (m + log2f(l)) * 0.69314718055994531f;
@@ -713,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       if (!warp_wait(bar_addr(sbase, kBarEpiGo), n_epi & 1, abort)) break;
       const float l = epi[kM + r];
       tc_fence_after();
-      store_output(a, c, misc->b0, tmem + lane_off, r, l, kDC / 2);
+      store_output(a, c, misc->b0, tmem + lane_off, r, l, kDC / 2, gbase);
       tc_fence_before();
       mbar_arrive(bar_addr(sbase, kBarEpiDone));
       ++n_epi;
@@ -774,33 +791,46 @@ __global__ void __launch_bounds__(128) combine_kernel(const Args a) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
   float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, L[4] = {0.f, 0.f, 0.f, 0.f};
-  for (long long q = p_first; q <= p_last; ++q) {
-    const long long slot = q == p_first ? slot_first : 2 * q;
-    const float4 m = *reinterpret_cast<const float4*>(a.part_m + slot * kM + h0);
-    M[0] = fmaxf(M[0], m.x);
-    M[1] = fmaxf(M[1], m.y);
-    M[2] = fmaxf(M[2], m.z);
-    M[3] = fmaxf(M[3], m.w);
-  }
-  for (long long q = p_first; q <= p_last; ++q) {
-    const long long slot = q == p_first ? slot_first : 2 * q;
-    const float4 m = *reinterpret_cast<const float4*>(a.part_m + slot * kM + h0);
-    const float4 l = *reinterpret_cast<const float4*>(a.part_l + slot * kM + h0);
-    const float* src = a.part_o + slot * (kDC * kM) + static_cast<long long>(cb32 * 32 + cq * 8) * kM + h0;
-    float4 v[8];
+  // pieces are merged two at a time (online: the running sums are rescaled to the new
+  // maximum), with the loads of both pieces in flight together
+  for (long long q = p_first; q <= p_last; q += 2) {
+    const bool two = q + 1 <= p_last;
+    const long long s0 = q == p_first ? slot_first : 2 * q, s1 = 2 * (q + 1);
+    const float* src0 = a.part_o + s0 * (kDC * kM) + static_cast<long long>(cb32 * 32 + cq * 8) * kM + h0;
+    const float* src1 = a.part_o + s1 * (kDC * kM) + static_cast<long long>(cb32 * 32 + cq * 8) * kM + h0;
+    const float4 m0 = *reinterpret_cast<const float4*>(a.part_m + s0 * kM + h0);
+    const float4 l0 = *reinterpret_cast<const float4*>(a.part_l + s0 * kM + h0);
+    float4 v0[8], v1[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const float4*>(src + j * kM);
-    const float w[4] = {exp2f(m.x - M[0]), exp2f(m.y - M[1]), exp2f(m.z - M[2]), exp2f(m.w - M[3])};
-    L[0] = fmaf(w[0], l.x, L[0]);
-    L[1] = fmaf(w[1], l.y, L[1]);
-    L[2] = fmaf(w[2], l.z, L[2]);
-    L[3] = fmaf(w[3], l.w, L[3]);
+    for (int j = 0; j < 8; ++j) v0[j] = *reinterpret_cast<const float4*>(src0 + j * kM);
+    float4 m1 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), l1 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (two) {
+      m1 = *reinterpret_cast<const float4*>(a.part_m + s1 * kM + h0);
+      l1 = *reinterpret_cast<const float4*>(a.part_l + s1 * kM + h0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v1[j] = *reinterpret_cast<const float4*>(src1 + j * kM);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float mm0[4] = {m0.x, m0.y, m0.z, m0.w}, mm1[4] = {m1.x, m1.y, m1.z, m1.w};
+    const float ll0[4] = {l0.x, l0.y, l0.z, l0.w}, ll1[4] = {l1.x, l1.y, l1.z, l1.w};
+    float al[4], w0[4], w1[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float mn = fmaxf(M[i], fmaxf(mm0[i], mm1[i]));
+      al[i] = exp2f(M[i] - mn);  // 0 while nothing has been merged (M = -inf)
+      w0[i] = exp2f(mm0[i] - mn);
+      w1[i] = two ? exp2f(mm1[i] - mn) : 0.f;
+      L[i] = fmaf(w1[i], ll1[i], fmaf(w0[i], ll0[i], L[i] * al[i]));
+      M[i] = mn;
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      acc[j][0] = fmaf(w[0], v[j].x, acc[j][0]);
-      acc[j][1] = fmaf(w[1], v[j].y, acc[j][1]);
-      acc[j][2] = fmaf(w[2], v[j].z, acc[j][2]);
-      acc[j][3] = fmaf(w[3], v[j].w, acc[j][3]);
+      acc[j][0] = fmaf(w1[0], v1[j].x, fmaf(w0[0], v0[j].x, acc[j][0] * al[0]));
+      acc[j][1] = fmaf(w1[1], v1[j].y, fmaf(w0[1], v0[j].y, acc[j][1] * al[1]));
+      acc[j][2] = fmaf(w1[2], v1[j].z, fmaf(w0[2], v0[j].z, acc[j][2] * al[2]));
+      acc[j][3] = fmaf(w1[3], v1[j].w, fmaf(w0[3], v0[j].w, acc[j][3] * al[3]));
     }
   }
 #pragma unroll

@@ -35,13 +35,65 @@ struct GemmArgs {
   const int32_t* q_pos;           // [B]
   int d_r;
   int rope_col;                   // first output column of the rotated part (d_c)
-  RopeTable rope;                 // base^(-2i/d_r), i < d_r / 2
+  RopeTable rope;                 // turns per position of each RoPE pair, i < d_r / 2
 };
+
+// The query's position part, q_cat[n][h][d_c + 2j, +1] = RoPE(q_rope[n][h][2j, 2j+1],
+// q_pos[n]), for the rows of n-tile n0 of head h, done by the kRopeThreads idle
+// threads (warps 2-3) of each of the `parts` m-tile blocks of the head while their
+// TMA loads and MMAs are in flight.  When the pair count divides the thread count,
+// every thread keeps one pair j (its frequency read once: a kernel parameter read at
+// a per-thread index is serialised) and walks rows part * step + t / half,
+// + step * parts, ...; the loads of eight rows are issued before any is used.
+constexpr int kRopeThreads = 64;
+__device__ __forceinline__ void rope_rows(const GemmArgs& g, int h, int n0, int part, int parts, int t) {
+  const int half = g.d_r / 2;
+  const int n_end = min(n0 + g.n_tile, g.nb);
+  constexpr int kU = 8;
+  if (kRopeThreads % half == 0) {
+    const int j = t % half, step = kRopeThreads / half, stride = step * parts;
+    const float u_hi = g.rope.u_hi[j], u_lo = g.rope.u_lo[j];
+    for (int nb = n0 + part * step + t / half; nb < n_end; nb += kU * stride) {
+      int pos[kU];
+      uint32_t x[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int n = nb + u * stride;
+        if (n < n_end) {
+          pos[u] = g.q_pos[n];
+          x[u] = *reinterpret_cast<const uint32_t*>(g.q_rope + (static_cast<long long>(n) * g.H + h) * g.d_r + 2 * j);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int n = nb + u * stride;
+        if (n < n_end) {
+          float sn, cs;
+          rope_sincos(pos[u], u_hi, u_lo, &sn, &cs);
+          const float x0 = __uint_as_float(x[u] << 16), x1 = __uint_as_float(x[u] & 0xFFFF0000u);
+          *reinterpret_cast<uint32_t*>(g.out + n * g.out_n_stride + h * g.out_h_stride + g.rope_col + 2 * j) =
+              pack_bf16x2(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+        }
+      }
+    }
+    return;
+  }
+  for (int idx = part * kRopeThreads + t; idx < (n_end - n0) * half; idx += parts * kRopeThreads) {
+    const int n = n0 + idx / half, j = idx % half;
+    float sn, cs;
+    rope_sincos(g.q_pos[n], g.rope.u_hi[j], g.rope.u_lo[j], &sn, &cs);
+    const uint32_t x = *reinterpret_cast<const uint32_t*>(g.q_rope + (static_cast<long long>(n) * g.H + h) * g.d_r + 2 * j);
+    const float x0 = __uint_as_float(x << 16), x1 = __uint_as_float(x & 0xFFFF0000u);
+    *reinterpret_cast<uint32_t*>(g.out + n * g.out_n_stride + h * g.out_h_stride + g.rope_col + 2 * j) =
+        pack_bf16x2(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+  }
+}
 
 template <bool kAMN>
 __global__ void __launch_bounds__(kThreadsHG) head_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                                                                const __grid_constant__ CUtensorMap map_b,
-                                                               const GemmArgs g) {
+                                                               const __grid_constant__ CUtensorMap map_out,
+                                                               const __grid_constant__ GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -49,7 +101,8 @@ __global__ void __launch_bounds__(kThreadsHG) head_gemm_kernel(const __grid_cons
   const int b_bytes = g.n_tile * kBK * 2;          // n_tile x 128 B
   const int stage_bytes = a_bytes + b_bytes;
   const int nst = g.stages;
-  const uint32_t bars = sbase + nst * stage_bytes;
+  const int tile_bytes = g.n_tile * kBM * 2;       // the transposed output tile reuses the stages
+  const uint32_t bars = sbase + (nst * stage_bytes > tile_bytes ? nst * stage_bytes : tile_bytes);
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   volatile int* abort = &s_abort;
@@ -110,57 +163,34 @@ __global__ void __launch_bounds__(kThreadsHG) head_gemm_kernel(const __grid_cons
       tc_commit_if(leader, bars + 8 * (kStagesHG + st));
     }
     tc_commit_if(leader, bars + 8 * (2 * kStagesHG));
-  } else if (g.d_r > 0) {
-    // warps 2-3 of every m-tile CTA of this head rotate a share of the query's
-    // position part (rows n0.., pairs j); the loads of four items are issued
-    // before any of them is used
-    const int half = g.d_r / 2;
-    const int total = (min(n0 + g.n_tile, g.nb) - n0) * half;
-    const int stride = 64 * gridDim.x;
-    for (int base = mt * 64 + threadIdx.x - 64; base < total; base += 4 * stride) {
-      int pos[4];
-      uint32_t x[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int idx = base + u * stride;
-        if (idx < total) {
-          const int n = n0 + idx / half, j = idx % half;
-          pos[u] = g.q_pos[n];
-          x[u] = *reinterpret_cast<const uint32_t*>(g.q_rope + (static_cast<long long>(n) * g.H + h) * g.d_r + 2 * j);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int idx = base + u * stride;
-        if (idx < total) {
-          const int n = n0 + idx / half, j = idx % half;
-          float sn, cs;
-          rope_sincos(pos[u], g.rope.theta[j], &sn, &cs);
-          const float x0 = __uint_as_float(x[u] << 16), x1 = __uint_as_float(x[u] & 0xFFFF0000u);
-          *reinterpret_cast<uint32_t*>(g.out + n * g.out_n_stride + h * g.out_h_stride + g.rope_col + 2 * j) =
-              pack_bf16x2(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
-        }
-      }
-    }
+  } else if (kAMN && g.d_r > 0) {
+    rope_rows(g, h, n0, mt, gridDim.x, threadIdx.x - 64);
   }
   __syncwarp();
 
-  // epilogue: warp w holds rows 32w..32w+31 (TMEM lanes), columns = batch rows
+  // epilogue: warp w holds rows 32w..32w+31 (TMEM lanes), columns = batch rows.  The
+  // tile is transposed into the idle stage memory as [n][128 rows] bf16 and leaves
+  // in one TMA store (rows n >= nb fall outside the tensor and are clipped).
   const bool ok = warp_wait(bars + 8 * (2 * kStagesHG), 0, abort);
   tc_fence_after();
   if (ok) {
-    const int m = m0 + warp * 32 + (threadIdx.x & 31);
+    __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(smem_raw + (sbase - raw));
+    const int ml = warp * 32 + (threadIdx.x & 31);
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     for (int c0 = 0; c0 < g.n_tile; c0 += 32) {
       uint32_t v[32];
       tmem_ld32(tmem + lane_off + c0, v);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int n = n0 + c0 + j;
-        if (n < g.nb && m < g.M) g.out[n * g.out_n_stride + h * g.out_h_stride + m] = __float2bfloat16_rn(__uint_as_float(v[j]));
-      }
+      for (int j = 0; j < 32; ++j) tile[(c0 + j) * kBM + ml] = __float2bfloat16_rn(__uint_as_float(v[j]));
     }
+    fence_proxy_async_cta();
+  }
+  __syncthreads();
+  if (ok && threadIdx.x == 0) {
+    tma_store_3d(&map_out, sbase, m0, h, n0);
+    bulk_commit();
+    bulk_wait_read0();
   }
   tc_fence_before();
   __syncthreads();
@@ -200,6 +230,20 @@ static bool map_2d(CUtensorMap* m, const void* p, uint64_t inner, uint64_t rows,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [B][H][X] output as a 3-D map (X, H, B) with a (128, 1, n_tile) box, no swizzle
+// (the staged tile is plain [n][128] bf16).
+static bool map_out3d(CUtensorMap* m, void* p, uint64_t X, uint64_t H, uint64_t B, uint32_t n_tile) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {X, H, B};
+  const cuuint64_t strides[2] = {X * 2, H * X * 2};
+  const cuuint32_t box[3] = {128, 1, n_tile};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 // [B][H][K] activations as a 3-D map (K, H, B) with a (64, 1, n_tile) box.
 static bool map_act(CUtensorMap* m, const void* p, uint64_t K, uint64_t H, uint64_t B, uint32_t n_tile) {
   EncodeTiledFn enc = encode_fn();
@@ -228,10 +272,12 @@ static int stages_for(int nk, int n_tile) {
 }
 
 template <bool kAMN>
-static mla_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& g, int m_tiles, int n_tiles,
-                         cudaStream_t s) {
+static mla_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const GemmArgs& g,
+                         int m_tiles, int n_tiles, cudaStream_t s) {
   auto k = head_gemm_kernel<kAMN>;
-  const size_t smem = static_cast<size_t>(g.stages) * (kBM * kBK * 2 + g.n_tile * kBK * 2) + 8 * (2 * kStagesHG + 1) + 1024;
+  const size_t ring = static_cast<size_t>(g.stages) * (kBM * kBK * 2 + g.n_tile * kBK * 2);
+  const size_t tile = static_cast<size_t>(g.n_tile) * kBM * 2;
+  const size_t smem = (ring > tile ? ring : tile) + 8 * (2 * kStagesHG + 1) + 1024;
   static size_t done[2] = {0, 0};
   if (smem > done[kAMN ? 1 : 0]) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
@@ -239,14 +285,14 @@ static mla_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const Gem
     done[kAMN ? 1 : 0] = smem;
   }
   dim3 grid(m_tiles, g.H, n_tiles);
-  k<<<grid, kThreadsHG, smem, s>>>(ma, mb, g);
+  k<<<grid, kThreadsHG, smem, s>>>(ma, mb, mo, g);
   return cuda_status(cudaGetLastError());
 }
 
 }  // namespace hg
 
 bool headgemm_absorb_supported(int32_t d_k, int32_t d_c, int32_t d_r) {
-  return d_k % 64 == 0 && d_c % 128 == 0 && d_r <= 128;
+  return d_k % 64 == 0 && d_c % 128 == 0 && d_r <= 128 && (d_c + d_r) % 8 == 0;  // 16-byte output rows
 }
 
 bool headgemm_out_up_supported(int32_t d_c, int32_t d_v) { return d_c % 64 == 0 && d_v % 128 == 0; }
@@ -273,7 +319,9 @@ mla_status launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int3
   CUtensorMap ma, mb;
   if (!map_2d(&ma, w_uk, d_c, static_cast<uint64_t>(H) * d_k, 64, 64)) return MLA_ERR_CUDA;
   if (!map_act(&mb, q_nope, d_k, H, B, g.n_tile)) return MLA_ERR_CUDA;
-  return launch<true>(ma, mb, g, d_c / kBM, (B + g.n_tile - 1) / g.n_tile, s);
+  CUtensorMap mo;
+  if (!map_out3d(&mo, q_cat, d_c + d_r, H, B, g.n_tile)) return MLA_ERR_CUDA;
+  return launch<true>(ma, mb, mo, g, d_c / kBM, (B + g.n_tile - 1) / g.n_tile, s);
 }
 
 mla_status launch_out_up_tc(const void* o_lat, const void* w_uv, void* o, int32_t B, int32_t H, int32_t d_c,
@@ -292,7 +340,9 @@ mla_status launch_out_up_tc(const void* o_lat, const void* w_uv, void* o, int32_
   CUtensorMap ma, mb;
   if (!map_2d(&ma, w_uv, d_c, static_cast<uint64_t>(H) * d_v, 64, 128)) return MLA_ERR_CUDA;
   if (!map_act(&mb, o_lat, d_c, H, B, g.n_tile)) return MLA_ERR_CUDA;
-  return launch<false>(ma, mb, g, d_v / kBM, (B + g.n_tile - 1) / g.n_tile, s);
+  CUtensorMap mo;
+  if (!map_out3d(&mo, o, d_v, H, B, g.n_tile)) return MLA_ERR_CUDA;
+  return launch<false>(ma, mb, mo, g, d_v / kBM, (B + g.n_tile - 1) / g.n_tile, s);
 }
 
 }  // namespace mla

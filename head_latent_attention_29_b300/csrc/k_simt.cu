@@ -40,7 +40,9 @@ __global__ void __launch_bounds__(128) cache_append_kernel(T* __restrict__ cache
                                                            const T* __restrict__ c_kv, const T* __restrict__ k_r,
                                                            const int32_t* __restrict__ seq_idx,
                                                            const int32_t* __restrict__ pos, int32_t n_rows,
-                                                           const RopeTable rope, int vec_ok) {
+                                                           const __grid_constant__ RopeTable rope, int vec_ok) {
+  __shared__ float s_hi[64], s_lo[64];
+  rope_table_to_smem(rope, d_r / 2, s_hi, s_lo);
   for (int64_t i = blockIdx.x; i < n_rows; i += gridDim.x) {
     const int32_t b = seq_idx[i];
     const int32_t p = pos[i];
@@ -62,7 +64,7 @@ __global__ void __launch_bounds__(128) cache_append_kernel(T* __restrict__ cache
     const T* kr = k_r + i * d_r;
     for (int j = threadIdx.x; j < d_r / 2; j += blockDim.x) {
       float sn, cs;
-      rope_sincos(p, rope.theta[j], &sn, &cs);
+      rope_sincos(p, s_hi[j], s_lo[j], &sn, &cs);
       const float x0 = ld_elem(kr + 2 * j), x1 = ld_elem(kr + 2 * j + 1);
       st_elem(dst + d_c + 2 * j, fmaf(x0, cs, -x1 * sn));
       st_elem(dst + d_c + 2 * j + 1, fmaf(x0, sn, x1 * cs));
@@ -102,8 +104,11 @@ template <typename T>
 __global__ void __launch_bounds__(128) absorb_q_kernel(const T* __restrict__ q_nope, const T* __restrict__ q_rope,
                                                        const int32_t* __restrict__ q_pos,
                                                        const T* __restrict__ w_uk, T* __restrict__ q_cat, int B,
-                                                       int H, int d_k, int d_c, int d_r, const RopeTable rope) {
+                                                       int H, int d_k, int d_c, int d_r,
+                                                       const __grid_constant__ RopeTable rope) {
   extern __shared__ float qs[];  // [kAbsorbBatch][d_k]
+  __shared__ float s_hi[64], s_lo[64];
+  rope_table_to_smem(rope, d_r / 2, s_hi, s_lo);
   const int h = blockIdx.y;
   const int c = blockIdx.x * 128 + threadIdx.x;
   const int R = d_c + d_r;
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(const T* __restrict__ q_n
     for (int idx = threadIdx.x; idx < B * half; idx += blockDim.x) {
       const int b = idx / half, j = idx - b * half;
       float sn, cs;
-      rope_sincos(q_pos[b], rope.theta[j], &sn, &cs);
+      rope_sincos(q_pos[b], s_hi[j], s_lo[j], &sn, &cs);
       const T* qr = q_rope + (static_cast<int64_t>(b) * H + h) * d_r;
       const float x0 = ld_elem(qr + 2 * j), x1 = ld_elem(qr + 2 * j + 1);
       T* dst = q_cat + (static_cast<int64_t>(b) * H + h) * R + d_c;

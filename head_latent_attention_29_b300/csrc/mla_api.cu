@@ -67,7 +67,7 @@ MLA_API mla_status mla_absorb_q(const void* q_nope, const void* q_rope, const in
   if (!(rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
   if (d_r > 128) return MLA_ERR_UNSUPPORTED;
   if (dtype == MLA_BF16 && mla::headgemm_absorb_supported(d_k, d_c, d_r) && aligned16(q_nope) && aligned16(w_uk) &&
-      aligned4(q_cat) && (d_r == 0 || aligned4(q_rope)))
+      aligned16(q_cat) && (d_r == 0 || aligned4(q_rope)))
     return mla::launch_absorb_q_tc(q_nope, q_rope, q_pos, w_uk, q_cat, B, H, d_k, d_c, d_r, rope_base,
                                    as_stream(stream));
   if (static_cast<size_t>(32) * d_k * sizeof(float) > 200 * 1024) return MLA_ERR_UNSUPPORTED;
@@ -133,7 +133,8 @@ MLA_API mla_status mla_out_up(const void* o_lat, const void* w_uv, void* o, int3
   if (!valid_dtype(dtype)) return MLA_ERR_INVALID_ARG;
   if (o_lat == nullptr || w_uv == nullptr || o == nullptr) return MLA_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || d_c <= 0 || d_v <= 0) return MLA_ERR_INVALID_ARG;
-  if (dtype == MLA_BF16 && mla::headgemm_out_up_supported(d_c, d_v) && aligned16(o_lat) && aligned16(w_uv))
+  if (dtype == MLA_BF16 && mla::headgemm_out_up_supported(d_c, d_v) && aligned16(o_lat) && aligned16(w_uv) &&
+      aligned16(o))
     return mla::launch_out_up_tc(o_lat, w_uv, o, B, H, d_c, d_v, as_stream(stream));
   if (d_c > 1024) return MLA_ERR_UNSUPPORTED;
   return mla::launch_out_up(o_lat, w_uv, o, B, H, d_c, d_v, dtype, as_stream(stream));

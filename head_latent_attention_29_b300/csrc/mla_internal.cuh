@@ -39,28 +39,54 @@ inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3
 
 // RoPE frequencies theta_i = base^(-2i/d_r), i < d_r/2, computed once on the host in
 // double and passed by value to the kernels (d_r <= 128).
+// RoPE frequencies as turns per position: u_i = theta_i / (2 pi), theta_i =
+// base^(-2i/d_r), held as an unevaluated fp32 sum u_hi + u_lo (about 48 bits).
 struct RopeTable {
-  double theta[64];
+  float u_hi[64];
+  float u_lo[64];
 };
 
 inline RopeTable rope_table(int d_r, double base) {
   RopeTable t = {};
-  for (int i = 0; i < d_r / 2 && i < 64; ++i) t.theta[i] = pow(base, -2.0 * i / d_r);
+  const double two_pi = 6.283185307179586476925;
+  for (int i = 0; i < d_r / 2 && i < 64; ++i) {
+    const double u = pow(base, -2.0 * i / d_r) / two_pi;
+    t.u_hi[i] = static_cast<float>(u);
+    t.u_lo[i] = static_cast<float>(u - static_cast<double>(t.u_hi[i]));
+  }
   return t;
 }
 
-// sin/cos of the rotation angle pos * theta: the product and its reduction by 2 pi
-// (split into a head and a tail so that the reduction is exact to double precision
-// for the positions used here) are the only fp64 operations; sin/cos run in fp32
-// on an argument already in [-pi, pi].
-__device__ __forceinline__ void rope_sincos(int pos, double theta, float* s, float* c) {
-  constexpr double kTwoPi = 6.283185307179586232;
-  constexpr double kTwoPiLo = 2.4492935982947064e-16;
-  constexpr double kInvTwoPi = 0.15915494309189534561;
-  const double ang = static_cast<double>(pos) * theta;
-  const double q = rint(ang * kInvTwoPi);
-  const double red = fma(-q, kTwoPiLo, fma(-q, kTwoPi, ang));
-  sincosf(static_cast<float>(red), s, c);
+// Copy the first `half` entries of the table into shared memory: reading a kernel
+// parameter at a per-thread index serialises on the constant cache, a shared-memory
+// read does not.  Every thread of the block calls it (it ends in __syncthreads).
+__device__ __forceinline__ void rope_table_to_smem(const RopeTable& t, int half, float* s_hi, float* s_lo) {
+  for (int i = threadIdx.x; i < half && i < 64; i += blockDim.x) {
+    s_hi[i] = t.u_hi[i];
+    s_lo[i] = t.u_lo[i];
+  }
+  __syncthreads();
+}
+
+// sin/cos of the rotation angle pos * theta, all in fp32: the number of turns
+// pos * u is formed exactly enough with FMA-based two-product (Dekker's exact
+// product, here hi = p u_hi rounded and err = fma(p, u_hi, -hi) exact), whole
+// turns are dropped (x - rint(x) is exact in fp32 by Sterbenz's lemma), and only
+// the fractional turn, at most half a turn, is scaled by 2 pi for sincosf.  The
+// position is split into a multiple of 4096 and a remainder so that both parts
+// convert to fp32 exactly for any int32 position.  Angle error ~1e-6 rad.
+__device__ __forceinline__ float rope_turn_part(float p, float u_hi, float u_lo) {
+  const float hi = p * u_hi;
+  const float err = fmaf(p, u_hi, -hi);
+  const float lo = fmaf(p, u_lo, err);
+  return (hi - rintf(hi)) + lo;
+}
+
+__device__ __forceinline__ void rope_sincos(int pos, float u_hi, float u_lo, float* s, float* c) {
+  const float p_hi = static_cast<float>(pos & ~4095), p_lo = static_cast<float>(pos & 4095);
+  float f = rope_turn_part(p_hi, u_hi, u_lo) + rope_turn_part(p_lo, u_hi, u_lo);
+  f -= rintf(f);
+  sincosf(f * 6.2831853071795865f, s, c);
 }
 
 inline mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }

@@ -201,6 +201,16 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
 }
 
 // ---------------------------------------------------------------- proxies
+// TMA store of a 3-D box from shared memory (bulk-group completion).  Boxes that
+// reach past the tensor's extent are clipped; coordinates must be non-negative.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+               :: "l"(map), "r"(src), "r"(x), "r"(y), "r"(z) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_cta() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -257,6 +267,12 @@ __device__ __forceinline__ void bulk_copy_to_cluster_if(uint32_t pred, uint32_t 
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
+
+// Bulk prefetch of `bytes` (multiple of 16) contiguous bytes into L2; p 16-byte aligned.
+__device__ __forceinline__ void prefetch_l2_bulk_if(uint32_t pred, const void* p, uint32_t bytes) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t@q cp.async.bulk.prefetch.L2.global [%1], %2;\n\t}"
+               :: "r"(pred), "l"(p), "r"(bytes) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05

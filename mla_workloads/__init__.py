@@ -50,6 +50,12 @@ WORKLOADS: dict[str, dict] = {
         dtype="bf16", rope_base=10000.0, w_std=1.0 / math.sqrt(512.0),
         scale=1.0 / math.sqrt(192.0),
     ),
+    # a small causal prefill of the same shape per token (profiling-sized case)
+    "prefill_h128_b1_s2048": dict(
+        B=1, H=128, d_c=512, d_r=64, d_k=128, d_v=128, S=2048,
+        dtype="bf16", rope_base=10000.0, w_std=1.0 / math.sqrt(512.0),
+        scale=1.0 / math.sqrt(192.0),
+    ),
     # gated MLA without RoPE: 64 heads, 131072 cached tokens, full-rank gate
     "gated_h64_b16_n131072": dict(
         B=16, H=64, d_c=512, d_r=0, d_k=128, d_v=128, N=131072, d_model=4096,
