@@ -27,7 +27,9 @@
 //    no redundant work.
 //  * Cache rows stream in through TMA (128-byte swizzled 64x64 chunks, 3-stage
 //    ring per CTA).  The same swizzled chunk is the K-major B operand of
-//    S = Q C^T and the MN-major B operand of O = P C.
+//    S = Q C^T and the MN-major B operand of O = P C.  The score CTA's ring also
+//    carries each problem's query (two slots of 64 rows) on its way to tensor
+//    memory, so a new problem costs two ring loads instead of per-thread reads.
 //  * A "problem" is one query row group (all heads of one query) against a prefix
 //    of one cached sequence: in decode, sequence b's query against its N_b rows; in
 //    causal prefill, query i of sequence b against rows [0, start_b + i] (the rows
@@ -79,12 +81,9 @@ constexpr int kOffX = kOffRope + kStages * kChunk;     // score CTA: reference e
 constexpr int kOffP = kStagesO * kStageDC;             // output CTA: kPBufs P tiles
 constexpr int kOffRef = kOffP + kPBufs * kPBytes;      // output CTA: kPBufs x 128 references
 constexpr int kOffEpi = kOffRef + kPBufs * kRefBytes;  // output CTA: per-row (m, l) for the epilogue helpers
-constexpr int kStgPitch = 80;                          // output CTA: staged bf16 output rows (32 columns + pad)
-constexpr int kStgBytes = kM * kStgPitch;
+constexpr int kStgBytes = kM * 64;                     // output CTA: one [128 rows][32 columns] bf16 output tile
 constexpr int kOffStg = kOffEpi + 2 * kRefBytes;       // output CTA: two staging tiles (one per epilogue group)
 constexpr int kOffBar = (kOffX + kRefBytes > kOffEpi + 2 * kRefBytes) ? kOffX + kRefBytes : kOffEpi + 2 * kRefBytes;
-constexpr int kQBoxBytes = kM * 128;                   // one 64-column TMA box of the query (128 rows)
-static_assert(9 * kQBoxBytes <= kStages * kStageDC, "the run's first query is staged in the ring");
 static_assert(kOffStg + 2 * kStgBytes <= kOffBar && kOffStg % 16 == 0, "output staging tiles");
 static_assert(kOffP % 1024 == 0, "P tiles must sit on 1024-byte boundaries");
 enum : int {
@@ -99,8 +98,7 @@ enum : int {
   kBarPvGo = kBarPFull + kPBufs,      // [kPBufs] output: block may be multiplied
   kBarODone = kBarPvGo + kPBufs,      // [kPBufs] output: PV of a block completed
   kBarDrain = kBarODone + kPBufs,     // MMA drain at teardown
-  kBarQFull = kBarDrain + 1,          // score: the run's first query staged in shared memory by TMA
-  kBarEpiGo = kBarQFull + 1,          // output: (m, l) of a finished problem published to the helper warps
+  kBarEpiGo = kBarDrain + 1,          // output: (m, l) of a finished problem published to the helper warps
   kBarEpiDone = kBarEpiGo + 1,        // output: the helpers' half of the output is out of tensor memory
   kNumBars = kBarEpiDone + 1,
 };
@@ -190,6 +188,12 @@ struct Cursor {
 };
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
+
+// Shared address of 64-column chunk ch (8 KB: 64 rows x 128 bytes, 128-byte swizzle)
+// of ring slot st: chunks 0-7 in the slot's latent area, chunk 8 in its RoPE area.
+__device__ __forceinline__ uint32_t ring_chunk(uint32_t base, int st, int ch) {
+  return ch < kChDC ? base + kOffStage + st * kStageDC + ch * kChunk : base + kOffRope + st * kChunk;
+}
 
 // Plan the run of this cluster: total blocks T, runs P = min(clusters, T), this
 // run's [lo, hi), and the problem that holds block lo.  One warp.  The writer of
@@ -283,39 +287,45 @@ __device__ __forceinline__ long long piece_slot(const Cursor& c, int b0) {
 // tensor memory: o = O / l in bf16 if the whole problem ran here, else the
 // unnormalised fp32 piece ([column][head] in its slot, a warp storing 128
 // contiguous bytes per column).
-__device__ __forceinline__ void store_output(const Args& a, const Cursor& c, int b0, uint32_t trow, int r, float l,
-                                             int col0, uint8_t* smem_gen) {
+__device__ __forceinline__ void store_output(const Args& a, const CUtensorMap* omap, const Cursor& c, int b0,
+                                             uint32_t trow, int r, float l, int col0, uint8_t* smem_gen,
+                                             uint32_t sbase) {
   if (c.whole()) {
-    // o = O / l in bf16 through a shared-memory tile per 32 columns, so that a warp
-    // writes 8 runs of 64 contiguous bytes (row r of the tile: 80-byte pitch, so the
-    // 16-byte writes of 8 consecutive rows hit distinct banks)
+    // o = O / l in bf16, 32 columns at a time: each thread packs its row into a
+    // [H rows][32 columns] tile in shared memory (64-byte rows) and one thread writes
+    // the tile out with a TMA store (rows past H are outside the box).  The next
+    // chunk's tensor-memory load is in flight while a chunk is handed over.
     const float inv = 1.f / l;
-    uint8_t* stg = smem_gen + kOffStg + (col0 != 0 ? kStgBytes : 0);
-    const uint32_t bar_id = col0 != 0 ? 2u : 1u;
-    __nv_bfloat16* orow = a.o_lat + static_cast<long long>(c.b) * a.H * kDC + col0;
+    const int grp = col0 != 0 ? 1 : 0;
+    uint8_t* stg = smem_gen + kOffStg + grp * kStgBytes;
+    const uint32_t stg_s = sbase + kOffStg + grp * kStgBytes;
+    const uint32_t bar_id = 1u + grp;
+    uint32_t v[32];
+    tmem_ld32(trow + col0, v);
     for (int cc = 0; cc < 8; ++cc) {
-      uint32_t v[32];
-      tmem_ld32(trow + col0 + cc * 32, v);
       tmem_wait_ld();
-      uint4* srow = reinterpret_cast<uint4*>(stg + r * kStgPitch);
+      uint4 w[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
-        w.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
-        w.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
-        w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
-        srow[q] = w;
+        w[q].x = pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
+        w[q].y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
+        w[q].z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
+        w[q].w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
       }
+      if (cc + 1 < 8) tmem_ld32(trow + col0 + (cc + 1) * 32, v);
+      if (r == 0) bulk_wait_read0();  // the previous store has read the tile
       named_sync(bar_id, 128);
+      if (r < a.H) {
+        uint4* srow = reinterpret_cast<uint4*>(stg + r * 64);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int id = k * 128 + r, row = id >> 2, q = id & 3;
-        if (row < a.H)
-          *reinterpret_cast<uint4*>(orow + static_cast<long long>(row) * kDC + cc * 32 + q * 8) =
-              *reinterpret_cast<const uint4*>(stg + row * kStgPitch + q * 16);
+        for (int q = 0; q < 4; ++q) srow[q] = w[q];
       }
+      fence_proxy_async_cta();
       named_sync(bar_id, 128);
+      if (r == 0) {
+        tma_store_2d(omap, stg_s, col0 + cc * 32, c.b * a.H);
+        bulk_commit();
+      }
     }
   } else {
     float* dst = a.part_o + piece_slot(c, b0) * (kDC * kM) + static_cast<long long>(col0) * kM + r;
@@ -337,6 +347,7 @@ __device__ __forceinline__ void store_output(const Args& a, const Cursor& c, int
 // columns 0..255), warps 8-11 epilogue (columns 256..511).
 __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_constant__ CUtensorMap map,
                                                                    const __grid_constant__ CUtensorMap qmap,
+                                                                   const __grid_constant__ CUtensorMap omap,
                                                                    const Args a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -370,7 +381,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     }
     mbar_init(bar_addr(sbase, kBarQReady), 128);
     mbar_init(bar_addr(sbase, kBarDrain), 1);
-    mbar_init(bar_addr(sbase, kBarQFull), 1);
     mbar_init(bar_addr(sbase, kBarEpiGo), 128);
     mbar_init(bar_addr(sbase, kBarEpiDone), 128);
     misc->abort = 0;
@@ -404,31 +414,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     const int nst = score_cta ? kStages : kStagesO;
     Cursor c;
     c.start(*misc, a.pb);
-    // the run's first query goes out before the cache stream floods the memory system:
-    // 64-column boxes of its 128 rows into the (still empty) ring, which the softmax
-    // threads move into tensor memory; the ring is reused once they are done
-    if (score_cta && c.ok()) {
-      mbar_arrive_expect_tx_if(leader, bar_addr(sbase, kBarQFull), nch * kQBoxBytes);
-      for (int ch = 0; ch < nch; ++ch)
-        tma_load_2d_if(leader, sbase + kOffStage + ch * kQBoxBytes, &qmap, bar_addr(sbase, kBarQFull), ch * 64,
-                       c.b * a.H);
-      warp_wait(bar_addr(sbase, kBarQReady), 0, abort);
-    }
+    int li = 0;  // ring load index: the score CTA's ring also carries each problem's query
     for (int k = 0; c.ok(); c.next(), ++k) {
-      const int st = k % nst;
-      // while a problem streams, the next problem's query moves into L2 (it is read
-      // from global memory when that problem starts mid-run)
-      if (score_cta && c.first() && c.b + 1 < a.NP)
-        prefetch_l2_bulk_if(leader, a.q_cat + static_cast<long long>(c.b + 1) * a.H * a.R,
-                            static_cast<uint32_t>(a.H * a.R * 2));
-      if (!warp_wait(bar_addr(sbase, kBarEmpty + st), ((k / nst) & 1) ^ 1, abort)) break;
+      if (score_cta && c.first()) {
+        // the problem's query, rows 0..63 and 64..127, as 64 x 64 boxes into two ring
+        // slots (latent area: 8 boxes, RoPE area: the ninth); the softmax threads move
+        // it into tensor memory and the MMA warp releases the slots
+        for (int part = 0; part < 2; ++part, ++li) {
+          const int st = li % kStages;
+          if (!warp_wait(bar_addr(sbase, kBarEmpty + st), ((li / kStages) & 1) ^ 1, abort)) break;
+          mbar_arrive_expect_tx_if(leader, bar_addr(sbase, kBarFull + st), nch * kChunk);
+          for (int ch = 0; ch < nch; ++ch)
+            tma_load_2d_if(leader, ring_chunk(sbase, st, ch), &qmap, bar_addr(sbase, kBarFull + st), ch * 64,
+                           c.b * a.H + part * kBN);
+        }
+        // meanwhile the next problem's query moves into L2
+        if (c.b + 1 < a.NP)
+          prefetch_l2_bulk_if(leader, a.q_cat + static_cast<long long>(c.b + 1) * a.H * a.R,
+                              static_cast<uint32_t>(a.H * a.R * 2));
+      }
+      const int st = (score_cta ? li : k) % nst;
+      const int ph = (score_cta ? li : k) / nst;
+      ++li;
+      if (!warp_wait(bar_addr(sbase, kBarEmpty + st), (ph & 1) ^ 1, abort)) break;
       MLA_TRACE_POINT(k, score_cta ? 8 : 7);
       mbar_arrive_expect_tx_if(leader, bar_addr(sbase, kBarFull + st), nload * kChunk);
-      for (int ch = 0; ch < nload; ++ch) {
-        const uint32_t dst = ch < kChDC ? sbase + kOffStage + st * kStageDC + ch * kChunk
-                                        : sbase + kOffRope + st * kChunk;
-        tma_load_3d_if(leader, dst, &map, bar_addr(sbase, kBarFull + st), ch * 64, c.t0(), c.cs);
-      }
+      for (int ch = 0; ch < nload; ++ch)
+        tma_load_3d_if(leader, ring_chunk(sbase, st, ch), &map, bar_addr(sbase, kBarFull + st), ch * 64, c.t0(), c.cs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -438,31 +450,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     if (score_cta) {
       // S = Q C^T: M = 128 heads, N = 64 tokens, A (the query) from tensor memory
       constexpr uint32_t idesc = idesc_bf16(kM, kBN, false, false);
-      int seg = 0;
+      int seg = 0, li = 0;
       for (int k = 0; c.ok(); c.next(), ++k) {
         if (c.first()) {
+          // the query left its two ring slots for tensor memory: release them
           if (!warp_wait(bar_addr(sbase, kBarQReady), seg & 1, abort)) break;
           ++seg;
+          if (leader) {
+            mbar_arrive(bar_addr(sbase, kBarEmpty + li % kStages));
+            mbar_arrive(bar_addr(sbase, kBarEmpty + (li + 1) % kStages));
+          }
+          li += 2;
         }
-        const int st = k % kStages, sb = k % kSBufs;
-        if (!warp_wait(bar_addr(sbase, kBarFull + st), (k / kStages) & 1, abort)) break;
+        const int st = li % kStages, sb = k % kSBufs;
+        if (!warp_wait(bar_addr(sbase, kBarFull + st), (li / kStages) & 1, abort)) break;
+        ++li;
         if (!warp_wait(bar_addr(sbase, kBarSEmpty + sb), ((k / kSBufs) & 1) ^ 1, abort)) break;
         MLA_TRACE_POINT(k, 0);
         tc_fence_after();
         const uint32_t d = tmem + kColS + sb * kBN;
-        const uint32_t stage = sbase + kOffStage + st * kStageDC;
 #pragma unroll
         for (int ch = 0; ch < kChDC; ++ch) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts_if(leader, d, tmem + kColQ + ch * 32 + kk * 8, sdesc_sw128(stage + ch * kChunk + kk * 32, 16, 1024),
+            mma_ts_if(leader, d, tmem + kColQ + ch * 32 + kk * 8, sdesc_sw128(ring_chunk(sbase, st, ch) + kk * 32, 16, 1024),
                       idesc, (ch | kk) != 0);
         }
         if (nch > kChDC) {  // the RoPE chunk
-          const uint32_t rope = sbase + kOffRope + st * kChunk;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts_if(leader, d, tmem + kColQ + kChDC * 32 + kk * 8, sdesc_sw128(rope + kk * 32, 16, 1024), idesc, 1u);
+            mma_ts_if(leader, d, tmem + kColQ + kChDC * 32 + kk * 8,
+                      sdesc_sw128(ring_chunk(sbase, st, kChDC) + kk * 32, 16, 1024), idesc, 1u);
         }
         tc_commit_if(leader, bar_addr(sbase, kBarEmpty + st));
         tc_commit_if(leader, bar_addr(sbase, kBarSFull + sb));
@@ -510,55 +528,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     float* ref_x = reinterpret_cast<float*>(gbase + kOffX);    // reference exchange between the groups
     Cursor c;
     c.start(*misc, a.pb);
-    int k = 0, last_mine = -1;
+    int k = 0, last_mine = -1, li = 0;  // li: the score ring's load index, as the producer counts it
     for (; c.ok(); c.next(), ++k) {
+      const bool first = c.first();
+      const int qli = li;  // a problem's query occupies ring loads qli, qli + 1
+      li += first ? 3 : 1;
       if ((k & 1) != grp) continue;
       last_mine = k;
-      if (c.first()) {
+      if (first) {
         // the previous block's S product (other group, older query) must be finished
         if (k > 0 && !warp_wait(bar_addr(sbase, kBarSFull + (k - 1) % kSBufs), ((k - 1) / kSBufs) & 1, abort)) break;
         if (r == 0) MLA_TRACE_POINT(k, 9);
-        if (k == 0) {
-          // the run's first query, staged by TMA (128-byte swizzle: piece j of row r at
-          // r * 128 + ((j ^ r % 8) * 16), so a warp's reads hit distinct banks)
-          if (!warp_wait(bar_addr(sbase, kBarQFull), 0, abort)) break;
-          const uint8_t* qrow = gbase + kOffStage + r * 128;
-          for (int j0 = 0; j0 < nch; ++j0) {
-            uint32_t v[32];
+        if (!warp_wait(bar_addr(sbase, kBarFull + qli % kStages), (qli / kStages) & 1, abort)) break;
+        if (!warp_wait(bar_addr(sbase, kBarFull + (qli + 1) % kStages), ((qli + 1) / kStages) & 1, abort)) break;
+        // row r of the query from its slot (rows 0-63, then 64-127); 128-byte swizzle:
+        // piece j of a row at row * 128 + ((j ^ row % 8) * 16), so a warp's reads hit
+        // distinct banks
+        const int qst = (qli + (r >> 6)) % kStages;
+        for (int ch = 0; ch < nch; ++ch) {
+          const uint8_t* qrow = gbase + (ring_chunk(sbase, qst, ch) - sbase) + (r & 63) * 128;
+          uint32_t v[32];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint4 x = *reinterpret_cast<const uint4*>(qrow + j0 * kQBoxBytes + ((u ^ (r & 7)) << 4));
-              v[4 * u] = x.x;
-              v[4 * u + 1] = x.y;
-              v[4 * u + 2] = x.z;
-              v[4 * u + 3] = x.w;
-            }
-            tmem_st32(tmem + lane_off + kColQ + j0 * 32, v);
+          for (int u = 0; u < 8; ++u) {
+            const uint4 x = *reinterpret_cast<const uint4*>(qrow + ((u ^ (r & 7)) << 4));
+            v[4 * u] = x.x;
+            v[4 * u + 1] = x.y;
+            v[4 * u + 2] = x.z;
+            v[4 * u + 3] = x.w;
           }
-        }
-        // a later query of the run, read straight from global memory (rows >= H are zero)
-        const uint4* src = reinterpret_cast<const uint4*>(a.q_cat + (static_cast<long long>(c.b) * a.H + r) * a.R);
-        for (int j0 = (k == 0 ? nch : 0); j0 < nch; j0 += 3) {  // three 128-byte pieces of the row in flight at once
-          uint4 x[24];
-#pragma unroll
-          for (int u = 0; u < 24; ++u) {
-            const int j = j0 + (u >> 3);
-            x[u] = (r < a.H && j < nch) ? __ldg(src + j * 8 + (u & 7)) : make_uint4(0u, 0u, 0u, 0u);
-          }
-#pragma unroll
-          for (int jj = 0; jj < 3; ++jj) {
-            if (j0 + jj < nch) {
-              uint32_t v[32];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                v[4 * u] = x[jj * 8 + u].x;
-                v[4 * u + 1] = x[jj * 8 + u].y;
-                v[4 * u + 2] = x[jj * 8 + u].z;
-                v[4 * u + 3] = x[jj * 8 + u].w;
-              }
-              tmem_st32(tmem + lane_off + kColQ + (j0 + jj) * 32, v);
-            }
-          }
+          tmem_st32(tmem + lane_off + kColQ + ch * 32, v);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -698,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         epi[kM + r] = l;
         mbar_arrive(bar_addr(sbase, kBarEpiGo));
         tc_fence_after();
-        store_output(a, c, misc->b0, tmem + lane_off, r, l, 0, gbase);
+        store_output(a, &omap, c, misc->b0, tmem + lane_off, r, l, 0, gbase, sbase);
         if (r < a.H) {
           if (c.whole()) {
             if (a.lse != nullptr) a.lse[static_cast<long long>(c.b) * a.H + r] = (m + log2f(l)) * 0.69314718055994531f;
@@ -730,13 +728,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       if (!warp_wait(bar_addr(sbase, kBarEpiGo), n_epi & 1, abort)) break;
       const float l = epi[kM + r];
       tc_fence_after();
-      store_output(a, c, misc->b0, tmem + lane_off, r, l, kDC / 2, gbase);
+      store_output(a, &omap, c, misc->b0, tmem + lane_off, r, l, kDC / 2, gbase, sbase);
       tc_fence_before();
       mbar_arrive(bar_addr(sbase, kBarEpiDone));
       ++n_epi;
     }
   }
 
+  if (!score_cta && (threadIdx.x == 128 || threadIdx.x == 256)) bulk_wait0();  // output tile stores complete
   __syncthreads();
   if (threadIdx.x == 0 && *abort) record_error(MLA_ERR_DEVICE_TIMEOUT, kSiteDecodeWait);
   if (warp == 1) {
@@ -958,15 +957,26 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return MLA_ERR_INVALID_ARG;
 
-  // the queries as [NP * H rows][R] for the TMA staging of each run's first query
+  // the queries as [NP * H rows][R]: each problem's query is staged through the score
+  // CTA's ring as 64 x 64 boxes
   CUtensorMap qmap;
   const cuuint64_t qdim[2] = {static_cast<cuuint64_t>(R), static_cast<cuuint64_t>(np) * static_cast<cuuint64_t>(H)};
   const cuuint64_t qstride[1] = {static_cast<cuuint64_t>(R) * 2};
-  const cuuint32_t qbox[2] = {64, static_cast<cuuint32_t>(kM)};
+  const cuuint32_t qbox[2] = {64, static_cast<cuuint32_t>(kBN)};
   const cuuint32_t qes[2] = {1, 1};
   if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q_cat), qdim, qstride, qbox, qes,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MLA_ERR_INVALID_ARG;
+
+  // o_lat as [NP * H rows][512] for the TMA stores of whole problems: H rows x 32 columns
+  CUtensorMap omap;
+  const cuuint64_t odim[2] = {static_cast<cuuint64_t>(kDC), static_cast<cuuint64_t>(np) * static_cast<cuuint64_t>(H)};
+  const cuuint64_t ostride[1] = {static_cast<cuuint64_t>(kDC) * 2};
+  const cuuint32_t obox[2] = {32, static_cast<cuuint32_t>(H)};
+  if (enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o_lat, odim, ostride, obox, qes, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+      CUDA_SUCCESS)
     return MLA_ERR_INVALID_ARG;
 
   uint8_t* wsb = static_cast<uint8_t*>(ws);
@@ -1000,7 +1010,7 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel, map, qmap, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel, map, qmap, omap, a);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   dim3 grid(kDC / 32, npairs);
   combine_kernel<<<grid, 128, 0, s>>>(a);
