@@ -62,6 +62,7 @@ constexpr int kChunk = kBN * 128;           // bytes of one [64 tok x 64 col] bf
 constexpr int kM = 128;                     // head rows per MMA
 constexpr int kMaxPairs = 80;               // upper bound on clusters per launch (148 SMs -> 74)
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P stays <= 256
+constexpr int kSwitchCost = 4;              // fixed cost of a problem (query in, output out), in blocks
 constexpr int kThreads = 384;               // 12 warps: see the role map in the kernel
 
 constexpr int kStages = 3;                  // score CTA TMA ring depth (HBM stream)
@@ -146,7 +147,8 @@ struct Args {
   float scale_log2;            // scale * log2(e)
   int32_t* hdr;                // workspace: [0] total blocks, [1] runs used, [2] problems with no rows
   int32_t* cum;                // workspace: [NP + 1] first block of each problem
-  int32_t* bnd;                // workspace: [kMaxPairs][3] problem holding each run's first block, its cum, end
+  int32_t* bnd;                // workspace: [kMaxPairs][4] per run: problem holding its first block, that
+                               //   problem's first block and end, the run's first block
   float* part_m;               // [2 kMaxPairs][128] running max (log2 units)
   float* part_l;               // [2 kMaxPairs][128] running sum
   float* part_o;               // [2 kMaxPairs][512][128] unnormalised output, latent-column major
@@ -195,10 +197,14 @@ __device__ __forceinline__ uint32_t ring_chunk(uint32_t base, int st, int ch) {
   return ch < kChDC ? base + kOffStage + st * kStageDC + ch * kChunk : base + kOffRope + st * kChunk;
 }
 
-// Plan the run of this cluster: total blocks T, runs P = min(clusters, T), this
-// run's [lo, hi), and the problem that holds block lo.  One warp.  The writer of
-// the table (one CTA per launch) also checks every length and counts the problems
-// with no rows.
+// Plan the run of this cluster.  Every problem costs its blocks plus a fixed
+// kSwitchCost (its query staging and output write, in block units); the total cost
+// C is cut into P equal runs, P = min(clusters, T, C / (kSwitchCost + 1)) so that
+// every run holds at least one block.  A run starts at the first block whose cost
+// position (problem start + kSwitchCost + block offset) reaches p C / P.  One warp.
+// The writer of the table (one CTA per launch) also checks every length, fills the
+// block prefix table and counts the problems with no rows; each run records its
+// first block and the problem holding it for the combine.
 __device__ void plan_run(const Args& a, Misc* misc, bool write_table, bool write_bnd) {
   const int lane = threadIdx.x & 31;
   long long T = 0;
@@ -218,42 +224,56 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table, bool write
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) empties += __shfl_xor_sync(0xffffffffu, empties, off);
+  const long long C = T + static_cast<long long>(kSwitchCost) * (a.NP - empties);
   const long long nclus = nclusters_x();
-  const long long P = T < nclus ? T : nclus;
+  long long P = T < nclus ? T : nclus;
+  if (P > C / (kSwitchCost + 1)) P = C / (kSwitchCost + 1);
+  if (T > 0 && P < 1) P = 1;
   const long long cid = cluster_id_x();
-  long long lo = 0, hi = 0;
-  if (cid < P) {
-    lo = cid * T / P;
-    hi = (cid + 1) * T / P;
-  }
+  const bool active = cid < P;
+  const long long x_lo = active ? cid * C / P : 0, x_hi = active ? (cid + 1) * C / P : 0;
+  long long lo = 0, hi = active ? T : 0, cum0 = 0;
   int b0 = 0, len0 = 0;
-  long long cum0 = 0;
-  if (lo < hi || write_table) {
-    long long run = 0;
-    bool found = false;
+  if (active || write_table) {
+    long long run = 0, crun = 0;  // blocks and cost of the problems before this group of 32
+    bool found_lo = !active, found_hi = !active || x_hi >= C;
     for (int base = 0; base < a.NP; base += 32) {
       const int b = base + lane;
       const int n = b < a.NP ? a.pb.len(b) : 0;
       const int nb = (n + kBN - 1) / kBN;
-      int incl = nb;
+      const int cost = nb > 0 ? nb + kSwitchCost : 0;
+      int incl = nb, cincl = cost;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
+        const int cv = __shfl_up_sync(0xffffffffu, cincl, off);
+        if (lane >= off) {
+          incl += v;
+          cincl += cv;
+        }
       }
-      const long long excl = run + incl - nb;
+      const long long excl = run + incl - nb, cexcl = crun + cincl - cost;
       if (write_table && b < a.NP) a.cum[b] = static_cast<int32_t>(excl);
-      const bool hit = !found && b < a.NP && nb > 0 && excl <= lo && lo < excl + nb;
-      const unsigned m = __ballot_sync(0xffffffffu, hit);
-      if (m != 0u) {
-        const int src = __ffs(m) - 1;
+      const unsigned mlo = __ballot_sync(0xffffffffu, !found_lo && cost > 0 && cexcl <= x_lo && x_lo < cexcl + cost);
+      if (mlo != 0u) {
+        const int src = __ffs(mlo) - 1;
         b0 = base + src;
         cum0 = __shfl_sync(0xffffffffu, excl, src);
         len0 = __shfl_sync(0xffffffffu, n, src);
-        found = true;
+        const long long into = x_lo - __shfl_sync(0xffffffffu, cexcl, src) - kSwitchCost;
+        lo = cum0 + (into > 0 ? into : 0);
+        found_lo = true;
+      }
+      const unsigned mhi = __ballot_sync(0xffffffffu, !found_hi && cost > 0 && cexcl <= x_hi && x_hi < cexcl + cost);
+      if (mhi != 0u) {
+        const int src = __ffs(mhi) - 1;
+        const long long into = x_hi - __shfl_sync(0xffffffffu, cexcl, src) - kSwitchCost;
+        hi = __shfl_sync(0xffffffffu, excl, src) + (into > 0 ? into : 0);
+        found_hi = true;
       }
       run += __shfl_sync(0xffffffffu, incl, 31);
-      if (found && !write_table) break;
+      crun += __shfl_sync(0xffffffffu, cincl, 31);
+      if (found_lo && found_hi && !write_table) break;
     }
   }
   if (lane == 0) {
@@ -262,11 +282,12 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table, bool write
     misc->b0 = b0;
     misc->cum0 = cum0;
     misc->len0 = len0;
-    if (write_bnd && lo < hi) {
-      int32_t* e = a.bnd + 3 * cluster_id_x();
+    if (write_bnd && active) {
+      int32_t* e = a.bnd + 4 * cluster_id_x();
       e[0] = b0;
       e[1] = static_cast<int32_t>(cum0);
       e[2] = static_cast<int32_t>(cum0 + (len0 + kBN - 1) / kBN);
+      e[3] = static_cast<int32_t>(lo);
     }
     if (write_table) {
       a.cum[a.NP] = static_cast<int32_t>(T);
@@ -758,7 +779,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const Args a) {
   constexpr int kPitch = 40;  // staged row: 32 bf16 columns + 16 bytes of padding
   __shared__ __align__(16) __nv_bfloat16 s_o[kM * kPitch];
   const int cb32 = blockIdx.x, p = blockIdx.y, t = threadIdx.x;
-  const long long T = a.hdr[0], P = a.hdr[1];
+  const long long P = a.hdr[1];
   if (p == 0) {
     if (a.hdr[2] == 0) return;
     for (int pr = t; pr < a.NP; pr += blockDim.x) {
@@ -773,15 +794,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const Args a) {
     return;
   }
   if (p >= P) return;
-  const long long lo_p = p * T / P;
-  const int pr = a.bnd[3 * p];  // the problem that holds run p's first block, its first block and end
-  const long long cb = a.bnd[3 * p + 1], ce = a.bnd[3 * p + 2];
-  if (cb == lo_p) return;  // the boundary falls between problems
-  // run q covers blocks [q T / P, (q + 1) T / P); run of block g = ceil((g + 1) P / T) - 1
-  const long long p_first = ((cb + 1) * P + T - 1) / T - 1;
-  if (p != p_first + 1) return;  // the block of an earlier boundary merges this problem
-  const long long p_last = (ce * P + T - 1) / T - 1;
-  const long long slot_first = 2 * p_first + (p_first * T / P == cb ? 0 : 1);
+  const int32_t* e = a.bnd + 4 * p;  // the problem holding run p's first block, its first block and end
+  const int pr = e[0];
+  const long long cb = e[1], ce = e[2], lo_p = e[3];
+  if (cb == lo_p) return;                     // the boundary falls between problems
+  if (a.bnd[4 * (p - 1) + 3] > cb) return;    // an earlier boundary cuts this problem and merges it
+  const long long p_first = p - 1;
+  long long p_last = p;                       // the run holding the problem's last block
+  while (p_last + 1 < P && a.bnd[4 * (p_last + 1) + 3] < ce) ++p_last;
+  const long long slot_first = 2 * p_first + (a.bnd[4 * p_first + 3] == cb ? 0 : 1);
 
   const int h0 = (t >> 2) * 4, cq = t & 3;
   float acc[8][4];
@@ -890,7 +911,7 @@ constexpr WsLayout ws_layout(long long np) {
   const size_t slots = 2 * static_cast<size_t>(kMaxPairs);
   w.hdr = 0;
   w.bnd = 256;
-  w.cum = w.bnd + align256(sizeof(int32_t) * 3 * kMaxPairs);
+  w.cum = w.bnd + align256(sizeof(int32_t) * 4 * kMaxPairs);
   w.m = w.cum + align256(sizeof(int32_t) * static_cast<size_t>(np + 1));
   w.l = w.m + align256(sizeof(float) * slots * kM);
   w.o = w.l + align256(sizeof(float) * slots * kM);
