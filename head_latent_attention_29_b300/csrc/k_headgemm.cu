@@ -36,6 +36,7 @@ struct GemmArgs {
   int d_r;
   int rope_col;                   // first output column of the rotated part (d_c)
   RopeTable rope;                 // turns per position of each RoPE pair, i < d_r / 2
+  int gate;                       // epilogue: out[n][m] *= sigmoid(D[m][n]) instead of storing D
 };
 
 // The query's position part, q_cat[n][h][d_c + 2j, +1] = RoPE(q_rope[n][h][2j, 2j+1],
@@ -173,7 +174,27 @@ __global__ void __launch_bounds__(kThreadsHG) head_gemm_kernel(const __grid_cons
   // in one TMA store (rows n >= nb fall outside the tensor and are clipped).
   const bool ok = warp_wait(bars + 8 * (2 * kStagesHG), 0, abort);
   tc_fence_after();
-  if (ok) {
+  if (g.gate) {
+    // gate: thread m scales out[n][m] for the tile's batch rows by sigmoid(D[m][n])
+    // (a warp reads and writes 64 contiguous bytes per row n)
+    if (ok) {
+      const int m = m0 + warp * 32 + (threadIdx.x & 31);
+      const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+      for (int c0 = 0; c0 < g.n_tile; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int n = n0 + c0 + j;
+          if (c0 + j < g.n_tile && n < g.nb) {
+            __nv_bfloat16* op = g.out + n * g.out_n_stride + m;
+            *op = __float2bfloat16_rn(__bfloat162float(*op) / (1.f + expf(-__uint_as_float(v[j]))));
+          }
+        }
+      }
+    }
+  } else if (ok) {
     __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(smem_raw + (sbase - raw));
     const int ml = warp * 32 + (threadIdx.x & 31);
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
@@ -187,7 +208,7 @@ __global__ void __launch_bounds__(kThreadsHG) head_gemm_kernel(const __grid_cons
     fence_proxy_async_cta();
   }
   __syncthreads();
-  if (ok && threadIdx.x == 0) {
+  if (ok && !g.gate && threadIdx.x == 0) {
     tma_store_3d(&map_out, sbase, m0, h, n0);
     bulk_commit();
     bulk_wait_read0();
@@ -297,6 +318,8 @@ bool headgemm_absorb_supported(int32_t d_k, int32_t d_c, int32_t d_r) {
 
 bool headgemm_out_up_supported(int32_t d_c, int32_t d_v) { return d_c % 64 == 0 && d_v % 128 == 0; }
 
+bool headgemm_gate_supported(int32_t d_model, int32_t width) { return d_model % 64 == 0 && width % 128 == 0; }
+
 mla_status launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int32_t* q_pos, const void* w_uk,
                               void* q_cat, int32_t B, int32_t H, int32_t d_k, int32_t d_c, int32_t d_r,
                               float rope_base, cudaStream_t s) {
@@ -343,6 +366,30 @@ mla_status launch_out_up_tc(const void* o_lat, const void* w_uv, void* o, int32_
   CUtensorMap mo;
   if (!map_out3d(&mo, o, d_v, H, B, g.n_tile)) return MLA_ERR_CUDA;
   return launch<false>(ma, mb, mo, g, d_v / kBM, (B + g.n_tile - 1) / g.n_tile, s);
+}
+
+// Gate (tahou.com sections 2.6 and 3.2): z[b][j] = sum_i h[b][i] W_g[i][j] computed
+// as D[j][b] with W_g^T as the MN-major A operand (one "head", M = width, K = d_model),
+// and o[b][j] *= sigmoid(z) in the epilogue.
+mla_status launch_gate_tc(const void* h, const void* w_g, void* o, int32_t B, int32_t d_model, int32_t width,
+                          cudaStream_t s) {
+  using namespace hg;
+  GemmArgs g = {};
+  g.H = 1;
+  g.M = width;
+  g.K = d_model;
+  g.nb = B;
+  g.n_tile = n_tile_for(B);
+  g.stages = stages_for(d_model / kBK, g.n_tile);
+  g.out = static_cast<__nv_bfloat16*>(o);
+  g.out_h_stride = 0;
+  g.out_n_stride = width;
+  g.gate = 1;
+  CUtensorMap ma, mb, mo;
+  if (!map_2d(&ma, w_g, width, d_model, 64, 64)) return MLA_ERR_CUDA;
+  if (!map_act(&mb, h, d_model, 1, B, g.n_tile)) return MLA_ERR_CUDA;
+  if (!map_out3d(&mo, o, width, 1, B, g.n_tile)) return MLA_ERR_CUDA;  // unused by the gate epilogue
+  return launch<true>(ma, mb, mo, g, width / kBM, (B + g.n_tile - 1) / g.n_tile, s);
 }
 
 }  // namespace mla

@@ -145,6 +145,9 @@ MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, 
   if (!valid_dtype(dtype)) return MLA_ERR_INVALID_ARG;
   if (h == nullptr || w_g == nullptr || o == nullptr) return MLA_ERR_INVALID_ARG;
   if (B <= 0 || d_model <= 0 || width <= 0) return MLA_ERR_INVALID_ARG;
+  if (dtype == MLA_BF16 && mla::headgemm_gate_supported(d_model, width) && aligned16(h) && aligned16(w_g) &&
+      aligned16(o))
+    return mla::launch_gate_tc(h, w_g, o, B, d_model, width, as_stream(stream));
   return mla::launch_gate(h, w_g, o, B, d_model, width, dtype, as_stream(stream));
 }
 

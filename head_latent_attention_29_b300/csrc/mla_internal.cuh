@@ -106,6 +106,9 @@ bool headgemm_out_up_supported(int32_t d_c, int32_t d_v);
 mla_status launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int32_t* q_pos, const void* w_uk,
                               void* q_cat, int32_t B, int32_t H, int32_t d_k, int32_t d_c, int32_t d_r,
                               float rope_base, cudaStream_t s);
+bool headgemm_gate_supported(int32_t d_model, int32_t width);
+mla_status launch_gate_tc(const void* h, const void* w_g, void* o, int32_t B, int32_t d_model, int32_t width,
+                          cudaStream_t s);
 mla_status launch_out_up_tc(const void* o_lat, const void* w_uv, void* o, int32_t B, int32_t H, int32_t d_c,
                             int32_t d_v, cudaStream_t s);
 mla_status launch_decode_f32(const float* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
