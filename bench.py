@@ -155,6 +155,24 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- workload
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest value of x over all ranks (the slowest replica sets the job's
+    time); no collective for a single process."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, seconds_per_step: float) -> float:
+    """Whole-job rate: the units all replicas processed in one step over the
+    slowest replica's step time."""
+    return units_per_rank * world / seconds_per_step
+
+
 def workload_bytes_flops(cfg, lens):
     R = cfg["d_c"] + cfg["d_r"]
     tokens = int(np.sum(lens))
@@ -270,14 +288,10 @@ def run_b300(args, rank, world, device):
         e1.record(stream)
         torch.cuda.synchronize(device)
         barrier()
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world, device)
     ms_step = ms_total / args.steps
     tokens_per_step = wl.B * world
-    value = tokens_per_step / (ms_step * 1e-3)
+    value = job_throughput(wl.B, world, ms_step * 1e-3)
 
     # ---- dominant op (attention: split-KV kernel + combine), timed alone on its stream
     n_rep = max(5, min(args.steps // 10, 200))
@@ -303,11 +317,7 @@ def run_b300(args, rank, world, device):
         wl.e2e[i % wl.rotate].replay()
         torch.cuda.current_stream(device).synchronize()
     barrier()
-    e2e_s = (time.perf_counter() - t0) / n_e2e
-    if world > 1:
-        t = torch.tensor([e2e_s], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world, device)
     h2d = sum(v.numel() * v.element_size() for v in wl.host.values())
     d2h = wl.o_host.numel() * wl.o_host.element_size()
 
@@ -458,14 +468,10 @@ def run_b300_prefill(args, rank, world, device):
         e1.record(stream)
         torch.cuda.synchronize(device)
         barrier()
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world, device)
     ms_step = ms_total / args.steps
     tokens = wl.B * wl.S * world
-    value = tokens / (ms_step * 1e-3)
+    value = job_throughput(wl.B * wl.S, world, ms_step * 1e-3)
 
     # the attention kernel alone (split + combine), on its stream
     n_rep = max(3, min(args.steps, 20))
@@ -489,7 +495,7 @@ def run_b300_prefill(args, rank, world, device):
         wl.step(True, True)
         stream.synchronize()
     barrier()
-    e2e_s = (time.perf_counter() - t0) / n_e2e
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world, device)
     h2d = sum(v.numel() * v.element_size() for v in wl.host.values())
     d2h = wl.o_host.numel() * wl.o_host.element_size()
 

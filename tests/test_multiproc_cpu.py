@@ -1,0 +1,69 @@
+"""The N > 1 host path on CPU: two gloo ranks (replicas) agree on the slowest
+replica's time, the job rate counts every replica's units, and the oracle arm runs
+on rank 0 only."""
+from __future__ import annotations
+
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank: int, world: int, port: int, q):
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r took (r + 1) ms per step: every rank must see the slowest, 2 ms
+        t = bench.max_over_ranks(float(rank + 1), world, torch.device("cpu"))
+        rate = bench.job_throughput(32, world, t * 1e-3)
+
+        class Args:
+            workload = "decode_h128_b32_n4096"
+            seed = 0
+            steps = 1
+            warmup = 3
+
+        ref = bench.run_reference(Args(), rank, world) if rank != 0 else "skipped"
+        q.put((rank, t, rate, ref))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_replicas_agree_on_the_slowest_time():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    results = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, t, rate, ref in results:
+        assert t == pytest.approx(2.0)
+        assert rate == pytest.approx(32 * 2 / 2e-3)  # both replicas' tokens over the slowest step
+        if rank != 0:
+            assert ref is None  # the oracle arm runs (and prints) on rank 0 only
+
+
+def test_single_process_needs_no_collective():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5, 1, None) == 3.5
+    assert bench.job_throughput(32, 1, 1e-4) == pytest.approx(320000.0)
