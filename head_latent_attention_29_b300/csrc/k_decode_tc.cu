@@ -419,6 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     tmem_relinquish();
   }
   if (threadIdx.x == 0) MLA_TRACE_POINT(63, score_cta ? 0 : 2);
+  griddep_launch();
+  // the workspace, o_lat and q_cat may still be in use by the previous kernels
+  griddep_wait();
   if (warp == 2) plan_run(a, misc, cluster_id_x() == 0 && score_cta, score_cta);
   __syncthreads();
   tc_fence_after();
@@ -778,6 +781,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 __global__ void __launch_bounds__(128) combine_kernel(const Args a) {
   constexpr int kPitch = 40;  // staged row: 32 bf16 columns + 16 bytes of padding
   __shared__ __align__(16) __nv_bfloat16 s_o[kM * kPitch];
+  griddep_launch();
+  griddep_wait();  // the pieces of the split kernel
   const int cb32 = blockIdx.x, p = blockIdx.y, t = threadIdx.x;
   const long long P = a.hdr[1];
   if (p == 0) {
@@ -1024,18 +1029,18 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemAlloc;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel, map, qmap, omap, a);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
-  dim3 grid(kDC / 32, npairs);
-  combine_kernel<<<grid, 128, 0, s>>>(a);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_pdl(combine_kernel, dim3(kDC / 32, npairs), dim3(128), 0, s, a));
 }
 
 mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,

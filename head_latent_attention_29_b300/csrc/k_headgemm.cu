@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(kThreadsHG) head_gemm_kernel(const __grid_cons
   const int nk = g.K / kBK;
   const uint32_t tmem_cols = g.n_tile <= 32 ? 32 : (g.n_tile <= 64 ? 64 : (g.n_tile <= 128 ? 128 : 256));
 
+  griddep_launch();
   if (threadIdx.x == 0) {
     for (int i = 0; i < nst; ++i) {
       mbar_init(bars + 8 * i, 1);                    // full
@@ -133,10 +134,8 @@ __global__ void __launch_bounds__(kThreadsHG) head_gemm_kernel(const __grid_cons
 
   if (warp == 0) {
     const uint32_t leader = elect_one();
-    for (int k = 0; k < nk; ++k) {
-      const int st = k % nst;
-      if (!warp_wait(bars + 8 * (kStagesHG + st), ((k / nst) & 1) ^ 1, abort)) break;
-      const uint32_t sa = sbase + st * stage_bytes, sb = sa + a_bytes, full = bars + 8 * st;
+    auto load_weights = [&](int k, int st) {
+      const uint32_t sa = sbase + st * stage_bytes, full = bars + 8 * st;
       mbar_arrive_expect_tx_if(leader, full, stage_bytes);
       if (kAMN) {
         // W_UK rows h*K + [k*64, k*64+64), latent columns [m0, m0+128) as two 64-wide boxes
@@ -146,7 +145,22 @@ __global__ void __launch_bounds__(kThreadsHG) head_gemm_kernel(const __grid_cons
         // W_UV rows h*M + [m0, m0+128), columns [k*64, k*64+64)
         tma_load_2d_if(leader, sa, &map_a, full, k * kBK, h * g.M + m0);
       }
-      tma_load_3d_if(leader, sb, &map_b, full, k * kBK, h, n0);
+    };
+    auto load_act = [&](int k, int st) {
+      const uint32_t sb = sbase + st * stage_bytes + a_bytes;
+      tma_load_3d_if(leader, sb, &map_b, bars + 8 * st, k * kBK, h, n0);
+    };
+    // the weights of the first ring pass are read while the previous kernel drains
+    // (no kernel writes them); the activations only after it has completed
+    const int first = nk < nst ? nk : nst;
+    for (int k = 0; k < first; ++k) load_weights(k, k);
+    griddep_wait();
+    for (int k = 0; k < first; ++k) load_act(k, k);
+    for (int k = first; k < nk; ++k) {
+      const int st = k % nst;
+      if (!warp_wait(bars + 8 * (kStagesHG + st), ((k / nst) & 1) ^ 1, abort)) break;
+      load_weights(k, st);
+      load_act(k, st);
     }
   } else if (warp == 1) {
     const uint32_t leader = elect_one();
@@ -165,6 +179,7 @@ __global__ void __launch_bounds__(kThreadsHG) head_gemm_kernel(const __grid_cons
     }
     tc_commit_if(leader, bars + 8 * (2 * kStagesHG));
   } else if (kAMN && g.d_r > 0) {
+    griddep_wait();  // q_cat may still be read by the previous kernel
     rope_rows(g, h, n0, mt, gridDim.x, threadIdx.x - 64);
   }
   __syncwarp();
@@ -174,6 +189,7 @@ __global__ void __launch_bounds__(kThreadsHG) head_gemm_kernel(const __grid_cons
   // in one TMA store (rows n >= nb fall outside the tensor and are clipped).
   const bool ok = warp_wait(bars + 8 * (2 * kStagesHG), 0, abort);
   tc_fence_after();
+  griddep_wait();  // the outputs may still be read (or, for the gate, written) by the previous kernel
   if (g.gate) {
     // gate: thread m scales out[n][m] for the tile's batch rows by sigmoid(D[m][n])
     // (a warp reads and writes 64 contiguous bytes per row n)
@@ -305,9 +321,7 @@ static mla_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
       return MLA_ERR_CUDA;
     done[kAMN ? 1 : 0] = smem;
   }
-  dim3 grid(m_tiles, g.H, n_tiles);
-  k<<<grid, kThreadsHG, smem, s>>>(ma, mb, mo, g);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_pdl(k, dim3(m_tiles, g.H, n_tiles), dim3(kThreadsHG), smem, s, ma, mb, mo, g));
 }
 
 }  // namespace hg

@@ -7,6 +7,7 @@
 #include <cmath>
 
 #include "mla_internal.cuh"
+#include "mla_ptx.cuh"
 
 namespace mla {
 
@@ -42,7 +43,9 @@ __global__ void __launch_bounds__(128) cache_append_kernel(T* __restrict__ cache
                                                            const int32_t* __restrict__ pos, int32_t n_rows,
                                                            const __grid_constant__ RopeTable rope, int vec_ok) {
   __shared__ float s_hi[64], s_lo[64];
+  griddep_launch();
   rope_table_to_smem(rope, d_r / 2, s_hi, s_lo);
+  griddep_wait();  // the rows written here may still be read by the previous kernel
   for (int64_t i = blockIdx.x; i < n_rows; i += gridDim.x) {
     const int32_t b = seq_idx[i];
     const int32_t p = pos[i];
@@ -79,10 +82,12 @@ mla_status launch_cache_append(const mla_cache& c, const void* c_kv, const void*
   const int vec_ok = ((c.d_c * esz) % 16 == 0) && ((c.row_stride * esz) % 16 == 0) && aligned16(c_kv) &&
                      aligned16(c.data);
   if (c.dtype == MLA_BF16) {
-    cache_append_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
-        static_cast<__nv_bfloat16*>(c.data), c.B, c.N_max, c.d_c, c.d_r, c.row_stride,
-        static_cast<const __nv_bfloat16*>(c_kv), static_cast<const __nv_bfloat16*>(k_r), seq_idx, pos, T,
-        rope_table(c.d_r, rope_base), vec_ok);
+    const cudaError_t e = launch_pdl(cache_append_kernel<__nv_bfloat16>, dim3(grid), dim3(128), 0, s,
+                                     static_cast<__nv_bfloat16*>(c.data), c.B, c.N_max, c.d_c, c.d_r,
+                                     static_cast<int64_t>(c.row_stride), static_cast<const __nv_bfloat16*>(c_kv),
+                                     static_cast<const __nv_bfloat16*>(k_r), seq_idx, pos, T,
+                                     rope_table(c.d_r, rope_base), vec_ok);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
   } else {
     cache_append_kernel<float><<<grid, 128, 0, s>>>(static_cast<float*>(c.data), c.B, c.N_max, c.d_c, c.d_r,
                                                     c.row_stride, static_cast<const float*>(c_kv),

@@ -91,6 +91,24 @@ __device__ __forceinline__ void rope_sincos(int pos, float u_hi, float u_lo, flo
 
 inline mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 
+// Launch with programmatic stream serialisation (the kernel may start while the
+// previous kernel in the stream drains; it synchronises with griddep_wait()).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ---- host launchers (one per kernel family), defined in the .cu files -------
 mla_status launch_cache_append(const mla_cache& c, const void* c_kv, const void* k_r, const int32_t* seq_idx,
                                const int32_t* pos, int32_t T, float rope_base, cudaStream_t s);

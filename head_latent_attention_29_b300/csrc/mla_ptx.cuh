@@ -281,6 +281,17 @@ __device__ __forceinline__ void prefetch_l2_bulk_if(uint32_t pred, const void* p
                :: "r"(pred), "l"(p), "r"(bytes) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start before the
+// previous kernel in the stream has finished.  griddep_wait() blocks until that
+// kernel has completed and its memory is visible; griddep_launch() lets the next
+// kernel be scheduled once every block of this grid has issued it.  Every kernel of
+// this library that is launched this way waits before it touches memory an earlier
+// kernel may still be writing or reading, and before it exits, so that a grid's
+// completion still implies the completion of everything before it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
