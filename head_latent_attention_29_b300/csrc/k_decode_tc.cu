@@ -62,7 +62,12 @@ constexpr int kChunk = kBN * 128;           // bytes of one [64 tok x 64 col] bf
 constexpr int kM = 128;                     // head rows per MMA
 constexpr int kMaxPairs = 80;               // upper bound on clusters per launch (148 SMs -> 74)
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P stays <= 256
-constexpr int kSwitchCost = 4;              // fixed cost of a problem (query in, output out), in blocks
+// Fixed cost of a problem (query in, output out) in 64-row blocks, for the run
+// planner.  Prompt problems follow each other closely, so each one's output write
+// stalls the pipeline; a decode run holds at most a couple of problems and hides
+// part of it behind the blocks already in flight.
+constexpr int kSwitchCostPrefill = 4;
+constexpr int kSwitchCostDecode = 2;
 constexpr int kThreads = 384;               // 12 warps: see the role map in the kernel
 
 constexpr int kStages = 3;                  // score CTA TMA ring depth (HBM stream)
@@ -145,6 +150,7 @@ struct Args {
   Problems pb;
   int NP, H, N_max, R, nch;    // NP problems; nch: 64-column chunks per row (R / 64)
   float scale_log2;            // scale * log2(e)
+  int switch_cost;             // fixed cost of a problem for the run planner, in blocks
   int32_t* hdr;                // workspace: [0] total blocks, [1] runs used, [2] problems with no rows
   int32_t* cum;                // workspace: [NP + 1] first block of each problem
   int32_t* bnd;                // workspace: [kMaxPairs][4] per run: problem holding its first block, that
@@ -198,15 +204,16 @@ __device__ __forceinline__ uint32_t ring_chunk(uint32_t base, int st, int ch) {
 }
 
 // Plan the run of this cluster.  Every problem costs its blocks plus a fixed
-// kSwitchCost (its query staging and output write, in block units); the total cost
-// C is cut into P equal runs, P = min(clusters, T, C / (kSwitchCost + 1)) so that
-// every run holds at least one block.  A run starts at the first block whose cost
-// position (problem start + kSwitchCost + block offset) reaches p C / P.  One warp.
+// sw = a.switch_cost (its query staging and output write, in block units); the total
+// cost C is cut into P equal runs, P = min(clusters, T, C / (sw + 1)) so that every
+// run holds at least one block.  A run starts at the first block whose cost position
+// (problem start + sw + block offset) reaches p C / P.  One warp.
 // The writer of the table (one CTA per launch) also checks every length, fills the
 // block prefix table and counts the problems with no rows; each run records its
 // first block and the problem holding it for the combine.
 __device__ void plan_run(const Args& a, Misc* misc, bool write_table, bool write_bnd) {
   const int lane = threadIdx.x & 31;
+  const int sw = a.switch_cost;
   long long T = 0;
   int empties = 0;
   for (int base = 0; base < a.NP; base += 32) {
@@ -224,10 +231,10 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table, bool write
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) empties += __shfl_xor_sync(0xffffffffu, empties, off);
-  const long long C = T + static_cast<long long>(kSwitchCost) * (a.NP - empties);
+  const long long C = T + static_cast<long long>(sw) * (a.NP - empties);
   const long long nclus = nclusters_x();
   long long P = T < nclus ? T : nclus;
-  if (P > C / (kSwitchCost + 1)) P = C / (kSwitchCost + 1);
+  if (P > C / (sw + 1)) P = C / (sw + 1);
   if (T > 0 && P < 1) P = 1;
   const long long cid = cluster_id_x();
   const bool active = cid < P;
@@ -241,7 +248,7 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table, bool write
       const int b = base + lane;
       const int n = b < a.NP ? a.pb.len(b) : 0;
       const int nb = (n + kBN - 1) / kBN;
-      const int cost = nb > 0 ? nb + kSwitchCost : 0;
+      const int cost = nb > 0 ? nb + sw : 0;
       int incl = nb, cincl = cost;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -260,14 +267,14 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table, bool write
         b0 = base + src;
         cum0 = __shfl_sync(0xffffffffu, excl, src);
         len0 = __shfl_sync(0xffffffffu, n, src);
-        const long long into = x_lo - __shfl_sync(0xffffffffu, cexcl, src) - kSwitchCost;
+        const long long into = x_lo - __shfl_sync(0xffffffffu, cexcl, src) - sw;
         lo = cum0 + (into > 0 ? into : 0);
         found_lo = true;
       }
       const unsigned mhi = __ballot_sync(0xffffffffu, !found_hi && cost > 0 && cexcl <= x_hi && x_hi < cexcl + cost);
       if (mhi != 0u) {
         const int src = __ffs(mhi) - 1;
-        const long long into = x_hi - __shfl_sync(0xffffffffu, cexcl, src) - kSwitchCost;
+        const long long into = x_hi - __shfl_sync(0xffffffffu, cexcl, src) - sw;
         hi = __shfl_sync(0xffffffffu, excl, src) + (into > 0 ? into : 0);
         found_hi = true;
       }
@@ -696,13 +703,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       fence_proxy_async_cta();  // P arrived through st.async; zeroed rows through generic stores
       tc_fence_before();
       mbar_arrive(bar_addr(sbase, kBarPvGo + pb));
-      // off the critical path (the MMA only reads the tile too): the row sum of the
-      // P tile as stored, i.e. of the values the MMA multiplies
+      // the row sum of the P tile as stored, i.e. of the values the MMA multiplies
+      // (the MMA only reads the tile too).  The eight 16-byte pieces of a row are read
+      // in swizzled order (piece cc ^ r % 8): the order does not matter to the sum,
+      // and the 8 rows of a quarter warp then hit 8 distinct bank groups
       const uint8_t* prow = gbase + kOffP + pb * kPBytes + (r >> 3) * 1024 + (r & 7) * 128;
       float ps = 0.f;
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
-        const uint4 v = *reinterpret_cast<const uint4*>(prow + cc * 16);
+        const uint4 v = *reinterpret_cast<const uint4*>(prow + ((cc ^ (r & 7)) << 4));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) ps += __uint_as_float(w[i] << 16) + __uint_as_float(w[i] & 0xFFFF0000u);
@@ -1015,6 +1024,7 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   a.R = R;
   a.nch = R / 64;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.switch_cost = pbs.q_start == nullptr ? kSwitchCostDecode : kSwitchCostPrefill;
   a.hdr = reinterpret_cast<int32_t*>(wsb + w.hdr);
   a.cum = reinterpret_cast<int32_t*>(wsb + w.cum);
   a.bnd = reinterpret_cast<int32_t*>(wsb + w.bnd);
