@@ -63,11 +63,11 @@ constexpr int kM = 128;                     // head rows per MMA
 constexpr int kMaxPairs = 80;               // upper bound on clusters per launch (148 SMs -> 74)
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P stays <= 256
 // Fixed cost of a problem (query in, output out) in 64-row blocks, for the run
-// planner.  Prompt problems follow each other closely, so each one's output write
-// stalls the pipeline; a decode run holds at most a couple of problems and hides
-// part of it behind the blocks already in flight.
-constexpr int kSwitchCostPrefill = 4;
-constexpr int kSwitchCostDecode = 2;
+// planner.  With more problems than runs they follow each other closely and each
+// one's output write stalls the pipeline; with fewer, a run holds at most a couple
+// of problems and hides part of it behind the blocks already in flight.
+constexpr int kSwitchCostMany = 4;
+constexpr int kSwitchCostFew = 2;
 constexpr int kThreads = 384;               // 12 warps: see the role map in the kernel
 
 constexpr int kStages = 3;                  // score CTA TMA ring depth (HBM stream)
@@ -781,22 +781,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 
 // Merge the pieces of every problem cut by run boundaries: M = max m_s,
 // L = sum l_s 2^(m_s - M), o = sum 2^(m_s - M) O_s / L, lse = (M + log2 L) ln 2.
-// Block (x, p) handles latent columns [32 x, 32 x + 32) of the problem that run
-// boundary p cuts, if p is the first boundary inside it; blocks (x, 0) write the
-// zero output of problems with no rows.  Thread t owns heads 4(t/4)..+3 and columns
-// 8(t%4)..+7, so every partial read is a 16-byte load and a warp reads 4 runs of
-// 128 contiguous bytes.  The merged tile is staged in shared memory ([head][column],
-// padded rows) and written out as 64 contiguous bytes per (problem, head).
-__global__ void __launch_bounds__(128) combine_kernel(const Args a) {
+// Work item (x, p) is latent columns [32 x, 32 x + 32) of the problem that run
+// boundary p cuts, if p is the first boundary inside it; items (x, 0) write the zero
+// output of problems with no rows.  One block per item.  Thread t
+// owns heads 2(t % 64), +1 and columns 8(t / 64)..+7: a warp reads 256 contiguous
+// bytes per column of a piece, and up to kCombinePieces pieces are in flight at once
+// (their maximum first, then one weighted sum).  The merged tile is staged in shared
+// memory ([head][column], padded rows) and written out as 64-byte runs.
+constexpr int kCombineThreads = 256;
+constexpr int kCombinePieces = 4;
+
+__device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, long long P, __nv_bfloat16* s_o) {
   constexpr int kPitch = 40;  // staged row: 32 bf16 columns + 16 bytes of padding
-  __shared__ __align__(16) __nv_bfloat16 s_o[kM * kPitch];
-  griddep_launch();
-  griddep_wait();  // the pieces of the split kernel
-  const int cb32 = blockIdx.x, p = blockIdx.y, t = threadIdx.x;
-  const long long P = a.hdr[1];
+  const int t = threadIdx.x;
   if (p == 0) {
     if (a.hdr[2] == 0) return;
-    for (int pr = t; pr < a.NP; pr += blockDim.x) {
+    for (int pr = t; pr < a.NP; pr += kCombineThreads) {
       if (a.cum[pr] != a.cum[pr + 1]) continue;
       for (int h = 0; h < a.H; ++h) {
         uint4* dst = reinterpret_cast<uint4*>(a.o_lat + (static_cast<long long>(pr) * a.H + h) * kDC + cb32 * 32);
@@ -807,90 +807,101 @@ __global__ void __launch_bounds__(128) combine_kernel(const Args a) {
     }
     return;
   }
-  if (p >= P) return;
   const int32_t* e = a.bnd + 4 * p;  // the problem holding run p's first block, its first block and end
   const int pr = e[0];
   const long long cb = e[1], ce = e[2], lo_p = e[3];
   if (cb == lo_p) return;                     // the boundary falls between problems
   if (a.bnd[4 * (p - 1) + 3] > cb) return;    // an earlier boundary cuts this problem and merges it
-  const long long p_first = p - 1;
-  long long p_last = p;                       // the run holding the problem's last block
+  const int p_first = p - 1;
+  int p_last = p;                             // the run holding the problem's last block
   while (p_last + 1 < P && a.bnd[4 * (p_last + 1) + 3] < ce) ++p_last;
   const long long slot_first = 2 * p_first + (a.bnd[4 * p_first + 3] == cb ? 0 : 1);
 
-  const int h0 = (t >> 2) * 4, cq = t & 3;
-  float acc[8][4];
+  const int h0 = (t & 63) * 2, c0 = cb32 * 32 + (t >> 6) * 8;
+  float acc[8][2];
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
+  for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = 0.f;
+  float M[2] = {-INFINITY, -INFINITY}, L[2] = {0.f, 0.f};
+  for (int q0 = p_first; q0 <= p_last; q0 += kCombinePieces) {
+    float2 m[kCombinePieces], l[kCombinePieces], v[kCombinePieces][8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
-  float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, L[4] = {0.f, 0.f, 0.f, 0.f};
-  // pieces are merged two at a time (online: the running sums are rescaled to the new
-  // maximum), with the loads of both pieces in flight together
-  for (long long q = p_first; q <= p_last; q += 2) {
-    const bool two = q + 1 <= p_last;
-    const long long s0 = q == p_first ? slot_first : 2 * q, s1 = 2 * (q + 1);
-    const float* src0 = a.part_o + s0 * (kDC * kM) + static_cast<long long>(cb32 * 32 + cq * 8) * kM + h0;
-    const float* src1 = a.part_o + s1 * (kDC * kM) + static_cast<long long>(cb32 * 32 + cq * 8) * kM + h0;
-    const float4 m0 = *reinterpret_cast<const float4*>(a.part_m + s0 * kM + h0);
-    const float4 l0 = *reinterpret_cast<const float4*>(a.part_l + s0 * kM + h0);
-    float4 v0[8], v1[8];
+    for (int u = 0; u < kCombinePieces; ++u) {
+      const int q = q0 + u;
+      if (q <= p_last) {
+        const long long slot = q == p_first ? slot_first : 2 * static_cast<long long>(q);
+        m[u] = *reinterpret_cast<const float2*>(a.part_m + slot * kM + h0);
+        l[u] = *reinterpret_cast<const float2*>(a.part_l + slot * kM + h0);
+        const float* src = a.part_o + slot * (kDC * kM) + static_cast<long long>(c0) * kM + h0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v0[j] = *reinterpret_cast<const float4*>(src0 + j * kM);
-    float4 m1 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), l1 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (two) {
-      m1 = *reinterpret_cast<const float4*>(a.part_m + s1 * kM + h0);
-      l1 = *reinterpret_cast<const float4*>(a.part_l + s1 * kM + h0);
+        for (int j = 0; j < 8; ++j) v[u][j] = *reinterpret_cast<const float2*>(src + j * kM);
+      } else {
+        m[u] = make_float2(-INFINITY, -INFINITY);
+        l[u] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v1[j] = *reinterpret_cast<const float4*>(src1 + j * kM);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < 8; ++j) v[u][j] = make_float2(0.f, 0.f);
+      }
     }
-    const float mm0[4] = {m0.x, m0.y, m0.z, m0.w}, mm1[4] = {m1.x, m1.y, m1.z, m1.w};
-    const float ll0[4] = {l0.x, l0.y, l0.z, l0.w}, ll1[4] = {l1.x, l1.y, l1.z, l1.w};
-    float al[4], w0[4], w1[4];
+    float mn[2] = {M[0], M[1]};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float mn = fmaxf(M[i], fmaxf(mm0[i], mm1[i]));
-      al[i] = exp2f(M[i] - mn);  // 0 while nothing has been merged (M = -inf)
-      w0[i] = exp2f(mm0[i] - mn);
-      w1[i] = two ? exp2f(mm1[i] - mn) : 0.f;
-      L[i] = fmaf(w1[i], ll1[i], fmaf(w0[i], ll0[i], L[i] * al[i]));
-      M[i] = mn;
+    for (int u = 0; u < kCombinePieces; ++u) {
+      mn[0] = fmaxf(mn[0], m[u].x);
+      mn[1] = fmaxf(mn[1], m[u].y);
     }
+    const float al0 = exp2f(M[0] - mn[0]), al1 = exp2f(M[1] - mn[1]);  // 0 before the first round
+    L[0] *= al0;
+    L[1] *= al1;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      acc[j][0] = fmaf(w1[0], v1[j].x, fmaf(w0[0], v0[j].x, acc[j][0] * al[0]));
-      acc[j][1] = fmaf(w1[1], v1[j].y, fmaf(w0[1], v0[j].y, acc[j][1] * al[1]));
-      acc[j][2] = fmaf(w1[2], v1[j].z, fmaf(w0[2], v0[j].z, acc[j][2] * al[2]));
-      acc[j][3] = fmaf(w1[3], v1[j].w, fmaf(w0[3], v0[j].w, acc[j][3] * al[3]));
+      acc[j][0] *= al0;
+      acc[j][1] *= al1;
     }
-  }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+    for (int u = 0; u < kCombinePieces; ++u) {
+      const float w0 = exp2f(m[u].x - mn[0]), w1 = exp2f(m[u].y - mn[1]);  // 0 for absent pieces
+      L[0] = fmaf(w0, l[u].x, L[0]);
+      L[1] = fmaf(w1, l[u].y, L[1]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc[j][0] = fmaf(w0, v[u][j].x, acc[j][0]);
+        acc[j][1] = fmaf(w1, v[u][j].y, acc[j][1]);
+      }
+    }
+    M[0] = mn[0];
+    M[1] = mn[1];
+  }
+  __syncthreads();  // the previous item's tile has been written out
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
     const float inv = 1.f / L[i];
     uint4 pk;
     pk.x = pack_bf16x2(acc[0][i] * inv, acc[1][i] * inv);
     pk.y = pack_bf16x2(acc[2][i] * inv, acc[3][i] * inv);
     pk.z = pack_bf16x2(acc[4][i] * inv, acc[5][i] * inv);
     pk.w = pack_bf16x2(acc[6][i] * inv, acc[7][i] * inv);
-    *reinterpret_cast<uint4*>(s_o + (h0 + i) * kPitch + cq * 8) = pk;
+    *reinterpret_cast<uint4*>(s_o + (h0 + i) * kPitch + (t >> 6) * 8) = pk;
   }
-  if (a.lse != nullptr && cb32 == 0 && cq == 0) {
+  if (a.lse != nullptr && cb32 == 0 && t < 64) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 2; ++i)
       if (h0 + i < a.H)
         a.lse[static_cast<long long>(pr) * a.H + h0 + i] = (M[i] + log2f(L[i])) * 0.69314718055994531f;
   }
   __syncthreads();
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int id = k * 128 + t, row = id >> 2, q = id & 3;
+  for (int k = 0; k < 2; ++k) {
+    const int id = k * kCombineThreads + t, row = id >> 2, q = id & 3;
     if (row < a.H)
       *reinterpret_cast<uint4*>(a.o_lat + (static_cast<long long>(pr) * a.H + row) * kDC + cb32 * 32 + q * 8) =
           *reinterpret_cast<const uint4*>(s_o + row * kPitch + q * 8);
   }
+}
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Args a) {
+  __shared__ __align__(16) __nv_bfloat16 s_o[kM * 40];
+  griddep_launch();
+  griddep_wait();  // the pieces of the split kernel
+  const long long P = a.hdr[1];
+  if (static_cast<long long>(blockIdx.y) < (P > 0 ? P : 1)) combine_item(a, blockIdx.x, blockIdx.y, P, s_o);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1024,7 +1035,7 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   a.R = R;
   a.nch = R / 64;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.switch_cost = pbs.q_start == nullptr ? kSwitchCostDecode : kSwitchCostPrefill;
+  a.switch_cost = np > npairs ? kSwitchCostMany : kSwitchCostFew;
   a.hdr = reinterpret_cast<int32_t*>(wsb + w.hdr);
   a.cum = reinterpret_cast<int32_t*>(wsb + w.cum);
   a.bnd = reinterpret_cast<int32_t*>(wsb + w.bnd);
@@ -1050,7 +1061,7 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel, map, qmap, omap, a);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
-  return cuda_status(launch_pdl(combine_kernel, dim3(kDC / 32, npairs), dim3(128), 0, s, a));
+  return cuda_status(launch_pdl(combine_kernel, dim3(kDC / 32, npairs), dim3(kCombineThreads), 0, s, a));
 }
 
 mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
