@@ -791,7 +791,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 constexpr int kCombineThreads = 256;
 constexpr int kCombinePieces = 4;
 
-__device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, long long P, __nv_bfloat16* s_o) {
+__device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, long long P, __nv_bfloat16* s_o,
+                                             const int32_t* bnd) {
   constexpr int kPitch = 40;  // staged row: 32 bf16 columns + 16 bytes of padding
   const int t = threadIdx.x;
   if (p == 0) {
@@ -807,15 +808,15 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
     }
     return;
   }
-  const int32_t* e = a.bnd + 4 * p;  // the problem holding run p's first block, its first block and end
+  const int32_t* e = bnd + 4 * p;  // the problem holding run p's first block, its first block and end
   const int pr = e[0];
   const long long cb = e[1], ce = e[2], lo_p = e[3];
-  if (cb == lo_p) return;                     // the boundary falls between problems
-  if (a.bnd[4 * (p - 1) + 3] > cb) return;    // an earlier boundary cuts this problem and merges it
+  if (cb == lo_p) return;                   // the boundary falls between problems
+  if (bnd[4 * (p - 1) + 3] > cb) return;    // an earlier boundary cuts this problem and merges it
   const int p_first = p - 1;
-  int p_last = p;                             // the run holding the problem's last block
-  while (p_last + 1 < P && a.bnd[4 * (p_last + 1) + 3] < ce) ++p_last;
-  const long long slot_first = 2 * p_first + (a.bnd[4 * p_first + 3] == cb ? 0 : 1);
+  int p_last = p;                           // the run holding the problem's last block
+  while (p_last + 1 < P && bnd[4 * (p_last + 1) + 3] < ce) ++p_last;
+  const long long slot_first = 2 * p_first + (bnd[4 * p_first + 3] == cb ? 0 : 1);
 
   const int h0 = (t & 63) * 2, c0 = cb32 * 32 + (t >> 6) * 8;
   float acc[8][2];
@@ -896,12 +897,42 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
   }
 }
 
+// Block (x, j) merges columns [32 x, 32 x + 32) of the j-th problem that needs a
+// merge (found from the run table: boundary p cuts a problem and is the first
+// boundary inside it); the last row of blocks writes the problems with no rows.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Args a) {
   __shared__ __align__(16) __nv_bfloat16 s_o[kM * 40];
+  __shared__ int32_t s_bnd[4 * kMaxPairs];
+  __shared__ int s_p;
   griddep_launch();
   griddep_wait();  // the pieces of the split kernel
-  const long long P = a.hdr[1];
-  if (static_cast<long long>(blockIdx.y) < (P > 0 ? P : 1)) combine_item(a, blockIdx.x, blockIdx.y, P, s_o);
+  // the run table in one round of loads (entries past the run count are not used)
+  for (int i = threadIdx.x; i < 4 * kMaxPairs; i += kCombineThreads) s_bnd[i] = a.bnd[i];
+  if (threadIdx.x == 0) s_p = 0;
+  const int P = a.hdr[1];
+  __syncthreads();
+  if (blockIdx.y == gridDim.y - 1) {
+    combine_item(a, blockIdx.x, 0, P, s_o, s_bnd);
+    return;
+  }
+  // boundary p (1 <= p < P) needs a merge if it cuts a problem that starts in run p - 1
+  static_assert(kMaxPairs <= 96, "three warps rank the boundaries");
+  if (threadIdx.x < 96) {  // whole warps 0..2
+    const int p = threadIdx.x;
+    const bool need = p >= 1 && p < P && p < kMaxPairs && s_bnd[4 * p + 1] != s_bnd[4 * p + 3] &&
+                      s_bnd[4 * (p - 1) + 3] <= s_bnd[4 * p + 1];
+    const unsigned m0 = __ballot_sync(0xffffffffu, need);
+    const int w = threadIdx.x >> 5;
+    __shared__ unsigned s_masks[4];
+    if ((threadIdx.x & 31) == 0) s_masks[w] = m0;
+    asm volatile("bar.sync 1, 96;" ::: "memory");
+    // rank of this boundary among those that need a merge
+    int rank = __popc(m0 & ((1u << (threadIdx.x & 31)) - 1u));
+    for (int v = 0; v < w; ++v) rank += __popc(s_masks[v]);
+    if (need && rank == static_cast<int>(blockIdx.y)) s_p = p;
+  }
+  __syncthreads();
+  if (s_p > 0) combine_item(a, blockIdx.x, s_p, P, s_o, s_bnd);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1061,7 +1092,10 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel, map, qmap, omap, a);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
-  return cuda_status(launch_pdl(combine_kernel, dim3(kDC / 32, npairs), dim3(kCombineThreads), 0, s, a));
+  // at most min(runs - 1, problems) problems need a merge; one more row for empty problems
+  const long long ncut = np < npairs - 1 ? np : npairs - 1;
+  const unsigned rows = static_cast<unsigned>(ncut > 0 ? ncut : 0) + 1u;
+  return cuda_status(launch_pdl(combine_kernel, dim3(kDC / 32, rows), dim3(kCombineThreads), 0, s, a));
 }
 
 mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
