@@ -226,6 +226,26 @@ def test_absorb_q_batch_shapes(mla, B):
     check_bf16(q_cat.float().cpu().numpy(), ref, f"q_cat B={B}")
 
 
+@pytest.mark.parametrize("d_r", [0, 8, 128])
+def test_absorb_q_rope_widths_and_far_positions(mla, d_r):
+    # the query rotation for every pair count the tensor-core path takes, at positions
+    # up to 2^20 (large angles: the fp32 turn reduction against the float64 oracle)
+    B, H, d_k, d_c = 33, 8, 128, 512
+    q_nope = W.bf16_bits(W.normal(23, "abs_q", (B, H, d_k)))
+    q_r = W.bf16_bits(W.normal(23, "abs_qr", (B, H, d_r)))
+    w_uk = W.bf16_bits(W.normal(23, "abs_w", (H, d_k, d_c), std=1 / math.sqrt(512)))
+    pos = np.concatenate([[0, 1, 2 ** 20 - 1, 2 ** 20], (np.arange(B - 4, dtype=np.int64) * 65537) % (2 ** 20)])
+    pos = pos.astype(np.int32)
+    q_cat = mla.absorb_q(to_device(q_nope, "bf16"), to_device(q_r, "bf16") if d_r else None,
+                         torch.from_numpy(pos).cuda(), to_device(w_uk, "bf16"))
+    ref = O.absorb_q(W.widen(q_nope, "bf16"), W.widen(q_r, "bf16"), pos, W.widen(w_uk, "bf16"), 1e4)
+    got = q_cat.float().cpu().numpy()
+    check_bf16(got, ref, f"q_cat d_r={d_r}")
+    if d_r:
+        # the rotated part alone: one bf16 rounding of the exact rotation
+        np.testing.assert_allclose(got[..., d_c:], ref[..., d_c:], rtol=2 ** -8, atol=2e-3)
+
+
 @pytest.mark.parametrize("B", [1, 5, 40, 300])
 def test_out_up_batch_shapes(mla, B):
     H, d_c, d_v = 16, 512, 128

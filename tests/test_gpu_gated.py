@@ -32,7 +32,8 @@ def _gate_case(mla, seed, B, d_model, width, dtype):
     return o_dev.float().cpu().numpy(), ref
 
 
-@pytest.mark.parametrize("B,d_model,width", [(16, 4096, 8192), (5, 128, 256), (1, 64, 128), (40, 192, 384)])
+@pytest.mark.parametrize("B,d_model,width", [(16, 4096, 8192), (5, 128, 256), (1, 64, 128), (40, 192, 384),
+                                             (300, 256, 256)])
 def test_gate_tensor_core(mla, B, d_model, width):
     got, ref = _gate_case(mla, 1, B, d_model, width, "bf16")
     check_bf16(got, ref, f"gate B{B} d{d_model} w{width}")

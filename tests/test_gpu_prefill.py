@@ -79,14 +79,15 @@ def test_prefill_two_sequences_all_rows(mla, causal):
     np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=2e-3)
 
 
-def test_prefill_few_heads_no_rope(mla):
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_few_heads_no_rope(mla, causal):
     starts, S, H = [5, 0, 64], 130, 16
     scale = 1.0 / np.sqrt(128.0)
     q, rows = prefill_inputs(2, starts, S, H, D_C, 0)
     q_dev, cache = upload(mla, q, rows, D_C, 0, max(starts) + S + 3)
-    o, lse = run(mla, q_dev, cache, starts, scale, True)
-    o_ref, lse_ref = oracle_all(q, rows, starts, D_C, scale, True)
-    check_bf16(o, o_ref, "prefill H=16 d_r=0")
+    o, lse = run(mla, q_dev, cache, starts, scale, causal)
+    o_ref, lse_ref = oracle_all(q, rows, starts, D_C, scale, causal)
+    check_bf16(o, o_ref, f"prefill H=16 d_r=0 causal={causal}")
     np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=2e-3)
 
 
