@@ -157,7 +157,8 @@ struct Args {
                                //   problem's first block and end, the run's first block
   float* part_m;               // [2 kMaxPairs][128] running max (log2 units)
   float* part_l;               // [2 kMaxPairs][128] running sum
-  float* part_o;               // [2 kMaxPairs][512][128] unnormalised output, latent-column major
+  float* part_s;               // [2 kMaxPairs][2][128] max |O| of each half row (columns 0-255, 256-511)
+  __half* part_o;              // [2 kMaxPairs][256][128][2] O / part_s in fp16: column pairs, head, pair
   __nv_bfloat16* o_lat;        // [NP][H][512]
   float* lse;                  // [NP][H] natural-log LSE, or nullptr
 };
@@ -356,16 +357,34 @@ __device__ __forceinline__ void store_output(const Args& a, const CUtensorMap* o
       }
     }
   } else {
-    float* dst = a.part_o + piece_slot(c, b0) * (kDC * kM) + static_cast<long long>(col0) * kM + r;
-    for (int cc = 0; cc < 4; ++cc) {
-      uint32_t v[64];
-      tmem_ld64(trow + col0 + cc * 64, v);
+    // a piece: O of this half row scaled by its largest magnitude and stored in fp16
+    // (the pieces are merged into bf16 outputs; |O / max| <= 1 keeps fp16 in range and
+    // its 11-bit significand well below the output's rounding).  Stores go by column
+    // pairs, [pair][head][2], so a warp writes 128 contiguous bytes per pair.
+    const long long slot = piece_slot(c, b0);
+    float mx = 0.f;
+    for (int cc = 0; cc < 8; ++cc) {
+      uint32_t v[32];
+      tmem_ld32(trow + col0 + cc * 32, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fabsf(__uint_as_float(v[j])));
+    }
+    const float inv = mx > 0.f ? 1.f / mx : 0.f;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(a.part_o) + slot * (kDC / 2 * kM) + (col0 / 2) * kM + r;
+    for (int cc = 0; cc < 8; ++cc) {
+      uint32_t v[32];
+      tmem_ld32(trow + col0 + cc * 32, v);
       tmem_wait_ld();
       if (r < a.H) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) dst[(cc * 64 + j) * kM] = __uint_as_float(v[j]);
+        for (int j = 0; j < 32; j += 2) {
+          const __half2 hv = __floats2half2_rn(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
+          dst[(cc * 16 + j / 2) * kM] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
       }
     }
+    if (r < a.H) a.part_s[(slot * 2 + col0 / (kDC / 2)) * kM + r] = mx;
   }
 }
 
@@ -770,6 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 
   if (!score_cta && (threadIdx.x == 128 || threadIdx.x == 256)) bulk_wait0();  // output tile stores complete
   __syncthreads();
+  if (threadIdx.x == 0) MLA_TRACE_POINT(62, score_cta ? 4 : 5);
   if (threadIdx.x == 0 && *abort) record_error(MLA_ERR_DEVICE_TIMEOUT, kSiteDecodeWait);
   if (warp == 1) {
     __syncwarp();
@@ -832,9 +852,17 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
         const long long slot = q == p_first ? slot_first : 2 * static_cast<long long>(q);
         m[u] = *reinterpret_cast<const float2*>(a.part_m + slot * kM + h0);
         l[u] = *reinterpret_cast<const float2*>(a.part_l + slot * kM + h0);
-        const float* src = a.part_o + slot * (kDC * kM) + static_cast<long long>(c0) * kM + h0;
+        const float2 sc = *reinterpret_cast<const float2*>(a.part_s + (slot * 2 + c0 / (kDC / 2)) * kM + h0);
+        // [pair][head][2]: heads h0, h0 + 1 of column pair cp are 4 consecutive halves
+        const __half* src = a.part_o + (slot * (kDC / 2 * kM) + static_cast<long long>(c0 / 2) * kM + h0) * 2;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[u][j] = *reinterpret_cast<const float2*>(src + j * kM);
+        for (int jp = 0; jp < 4; ++jp) {
+          const uint2 w = *reinterpret_cast<const uint2*>(src + jp * kM * 2);
+          const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));  // head h0: columns 2jp, 2jp+1
+          const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));  // head h0+1
+          v[u][2 * jp] = make_float2(a0.x * sc.x, a1.x * sc.y);
+          v[u][2 * jp + 1] = make_float2(a0.y * sc.x, a1.y * sc.y);
+        }
       } else {
         m[u] = make_float2(-INFINITY, -INFINITY);
         l[u] = make_float2(0.f, 0.f);
@@ -954,7 +982,7 @@ static EncodeTiledFn encode_fn() {
 }
 
 struct WsLayout {
-  size_t hdr, bnd, cum, m, l, o, total;
+  size_t hdr, bnd, cum, m, l, s, o, total;
 };
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -970,8 +998,9 @@ constexpr WsLayout ws_layout(long long np) {
   w.cum = w.bnd + align256(sizeof(int32_t) * 4 * kMaxPairs);
   w.m = w.cum + align256(sizeof(int32_t) * static_cast<size_t>(np + 1));
   w.l = w.m + align256(sizeof(float) * slots * kM);
-  w.o = w.l + align256(sizeof(float) * slots * kM);
-  w.total = w.o + sizeof(float) * slots * kM * kDC;
+  w.s = w.l + align256(sizeof(float) * slots * kM);
+  w.o = w.s + align256(sizeof(float) * slots * 2 * kM);
+  w.total = w.o + 2 * slots * kM * kDC;  // fp16
   return w;
 }
 
@@ -1072,7 +1101,8 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   a.bnd = reinterpret_cast<int32_t*>(wsb + w.bnd);
   a.part_m = reinterpret_cast<float*>(wsb + w.m);
   a.part_l = reinterpret_cast<float*>(wsb + w.l);
-  a.part_o = reinterpret_cast<float*>(wsb + w.o);
+  a.part_s = reinterpret_cast<float*>(wsb + w.s);
+  a.part_o = reinterpret_cast<__half*>(wsb + w.o);
   a.o_lat = static_cast<__nv_bfloat16*>(o_lat);
   a.lse = lse;
 

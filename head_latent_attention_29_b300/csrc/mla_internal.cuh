@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/mla.h"
