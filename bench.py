@@ -62,19 +62,25 @@ def _peaks():
 class ClockSampler:
     """SM clock and clock-event reasons during the timed region: NVML when the
     Python module is present, else an nvidia-smi sampling subprocess; the GPU is
-    selected by UUID (NVML ignores CUDA_VISIBLE_DEVICES)."""
+    selected by UUID (NVML ignores CUDA_VISIBLE_DEVICES).  Every sample carries
+    its host time; the sampler is running before the region starts and keeps
+    going until a sample after its end has arrived, so a region shorter than the
+    sampling period is still bracketed by the samples on either side."""
 
     SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
                   "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
                   "clocks_event_reasons.sw_power_cap")
+    SMI_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, device_index: int, period_s: float = 0.02):
-        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self.samples = []  # (host time, SM MHz, reason names)
+        self.max_mhz = None
         self._stop = threading.Event()
         self._period = period_s
         self._mode = None
         self.error = None
         self._uuid = None
+        self._t0 = self._t1 = None
         try:
             import torch
             u = str(torch.cuda.get_device_properties(device_index).uuid)
@@ -100,58 +106,80 @@ class ClockSampler:
     def _run_nvml(self):
         while not self._stop.is_set():
             try:
-                self.samples.append(self._nv.nvmlDeviceGetClockInfo(self._h, self._nv.NVML_CLOCK_SM))
-                self.reasons |= int(self._reasons_fn(self._h))
+                mhz = self._nv.nvmlDeviceGetClockInfo(self._h, self._nv.NVML_CLOCK_SM)
+                bits = int(self._reasons_fn(self._h))
+                self.samples.append((time.perf_counter(), float(mhz),
+                                     [n for bit, n in THROTTLE_BITS.items() if bits & bit]))
             except Exception as e:
                 self.error = repr(e)[:200]
             time.sleep(self._period)
 
+    def _run_smi(self):
+        for line in self._p.stdout:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                mhz, self.max_mhz = float(f[0]), float(f[1])
+            except ValueError:
+                continue
+            names = [n for n, v in zip(self.SMI_REASONS, f[3:7]) if v.lower() in ("active", "1", "yes")]
+            self.samples.append((time.perf_counter(), mhz, names))
+
+    def _wait_for_sample_after(self, t, limit_s):
+        end = time.perf_counter() + limit_s
+        while time.perf_counter() < end:
+            if self.samples and self.samples[-1][0] > t:
+                return
+            time.sleep(0.002)
+
     def __enter__(self):
         if self._mode == "nvml":
             self._t = threading.Thread(target=self._run_nvml, daemon=True)
-            self._t.start()
         elif self._mode == "smi":
             import subprocess
             self._p = subprocess.Popen(["nvidia-smi", "-i", self._uuid, f"--query-gpu={self.SMI_FIELDS}",
                                         "--format=csv,noheader,nounits", f"-lms={int(self._period * 1000)}"],
                                        stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._run_smi, daemon=True)
+        if self._mode:
+            self._t.start()
+            self._wait_for_sample_after(0.0, 5.0)  # sampling is live before the region starts
+        self._t0 = time.perf_counter()
         return self
 
     def __exit__(self, *exc):
+        self._t1 = time.perf_counter()
+        if self._mode:
+            self._wait_for_sample_after(self._t1, 2.0)
         if self._mode == "nvml":
             self._stop.set()
             self._t.join()
         elif self._mode == "smi":
             self._p.terminate()
-            out, _ = self._p.communicate(timeout=10)
-            self._smi_lines = out.strip().splitlines()
-            self._parse_smi()
-
-    def _parse_smi(self):
-        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        self._smi_reasons = set()
-        for line in self._smi_lines:
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 7:
-                continue
             try:
-                self.samples.append(float(f[0]))
-                self.max_mhz = float(f[1])
-            except ValueError:
-                continue
-            for name, val in zip(names[1:], f[3:7]):
-                if val.lower() in ("active", "1", "yes"):
-                    self._smi_reasons.add(name)
+                self._p.wait(timeout=10)
+            except Exception:  # pragma: no cover
+                self._p.kill()
+            self._t.join(timeout=5)
+
+    def window(self):
+        """The samples taken inside the region; if it was shorter than the sampling
+        period, the last sample before it and the first after it."""
+        inside = [x for x in self.samples if self._t0 <= x[0] <= self._t1]
+        if inside:
+            return inside, "inside"
+        before = [x for x in self.samples if x[0] < self._t0][-1:]
+        after = [x for x in self.samples if x[0] > self._t1][:1]
+        return before + after, "adjacent"
 
     def summary(self):
-        if not self.samples:
+        got, where = self.window() if self._t0 is not None else ([], "none")
+        if not got:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"], "error": self.error}
-        if self._mode == "nvml":
-            names = [n for bit, n in THROTTLE_BITS.items() if self.reasons & bit]
-        else:
-            names = sorted(self._smi_reasons)
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": names,
-                "samples": len(self.samples), "source": self._mode}
+        names = sorted({n for x in got for n in x[2]})
+        return {"sm_mhz": statistics.median(x[1] for x in got), "sm_max_mhz": self.max_mhz, "reasons": names,
+                "samples": len(got), "window": where, "source": self._mode}
 
 
 # ---------------------------------------------------------------- workload
@@ -171,6 +199,17 @@ def job_throughput(units_per_rank: float, world: int, seconds_per_step: float) -
     """Whole-job rate: the units all replicas processed in one step over the
     slowest replica's step time."""
     return units_per_rank * world / seconds_per_step
+
+
+def decode_metric(workload: str, cfg) -> str:
+    """The metric's name: the headline decode shape keeps its published wording, the
+    other decode shapes spell out their own sizes."""
+    if workload == "decode_h128_b32_n4096":
+        return "MLA decode tokens/s at H=128,d_c=512,B=32,N=4K bf16; % of roofline"
+    n = f"N={cfg['N']}" if "N" in cfg else f"N={cfg['N_lo']}..{cfg['N_hi']} (ragged)"
+    extra = "" if cfg["d_r"] else ", no RoPE"
+    extra += ", output gate" if "d_model" in cfg else ""
+    return f"MLA decode tokens/s at H={cfg['H']},d_c={cfg['d_c']},B={cfg['B']},{n}{extra} bf16; % of roofline"
 
 
 def workload_bytes_flops(cfg, lens):
@@ -330,7 +369,7 @@ def run_b300(args, rank, world, device):
     traffic = _ncu_traffic(args.workload)
 
     out = {
-        "metric": "MLA decode tokens/s at H=128,d_c=512,B=32,N=4K bf16; % of roofline",
+        "metric": decode_metric(args.workload, cfg),
         "value": round(value, 1),
         "unit": "tokens/s",
         "n_gpus": world,

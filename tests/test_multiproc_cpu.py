@@ -67,3 +67,30 @@ def test_single_process_needs_no_collective():
     import bench
     assert bench.max_over_ranks(3.5, 1, None) == 3.5
     assert bench.job_throughput(32, 1, 1e-4) == pytest.approx(320000.0)
+
+
+def test_clock_window_brackets_a_short_region():
+    # samples inside the timed region are used as they are; a region shorter than
+    # the sampling period takes the samples on either side of it
+    sys.path.insert(0, ROOT)
+    import bench
+    c = bench.ClockSampler.__new__(bench.ClockSampler)
+    c.samples = [(1.0, 1900.0, []), (2.0, 1950.0, ["sw_power_cap"]), (3.0, 2000.0, [])]
+    c.max_mhz, c._mode, c.error = 2032.0, "smi", None
+    c._t0, c._t1 = 1.5, 2.5
+    s = c.summary()
+    assert (s["sm_mhz"], s["samples"], s["window"], s["reasons"]) == (1950.0, 1, "inside", ["sw_power_cap"])
+    c._t0, c._t1 = 2.1, 2.2
+    s = c.summary()
+    assert (s["sm_mhz"], s["samples"], s["window"]) == (1975.0, 2, "adjacent")
+
+
+def test_decode_metric_names_its_shape():
+    sys.path.insert(0, ROOT)
+    import bench
+    import mla_workloads as W
+    assert bench.decode_metric("decode_h128_b32_n4096", W.WORKLOADS["decode_h128_b32_n4096"]).startswith(
+        "MLA decode tokens/s at H=128,d_c=512,B=32,N=4K bf16")
+    m = bench.decode_metric("gated_h64_b16_n131072", W.WORKLOADS["gated_h64_b16_n131072"])
+    assert "H=64" in m and "N=131072" in m and "no RoPE" in m and "gate" in m
+    assert "ragged" in bench.decode_metric("ragged_h128_b64_n1k_32k", W.WORKLOADS["ragged_h128_b64_n1k_32k"])
