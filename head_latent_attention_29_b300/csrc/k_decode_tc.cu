@@ -58,6 +58,7 @@ namespace dtc {
 constexpr int kBN = 64;                     // tokens per block
 constexpr int kDC = 512;                    // latent width
 constexpr int kChDC = kDC / 64;             // 8 chunks of 64 columns cover the latent
+constexpr int kChunksPerRow = kDC / 32;     // 32-column groups of a piece row, each with its own fp16 scale
 constexpr int kChunk = kBN * 128;           // bytes of one [64 tok x 64 col] bf16 chunk
 constexpr int kM = 128;                     // head rows per MMA
 constexpr int kMaxPairs = 80;               // upper bound on clusters per launch (148 SMs -> 74)
@@ -76,8 +77,9 @@ constexpr int kPBufs = 4;                   // P tiles in flight between the CTA
 constexpr int kStageDC = kChDC * kChunk;    // 64 KB of latent chunks per stage
 constexpr int kSBufs = 3;                   // score accumulators in tensor memory
 constexpr int kPBytes = kM * 128;           // one bf16 P tile (128 heads x 64 tokens)
-constexpr int kRefBytes = kM * 4;           // per-row softmax reference sent with a tile
-constexpr uint32_t kPTxBytes = kPBytes + kRefBytes;
+constexpr int kRefBytes = kM * 4;           // one fp32 value per head row
+constexpr int kMsgBytes = kM * 8;           // per-row (reference, row sum of the bf16 tile) sent with a tile
+constexpr uint32_t kPTxBytes = kPBytes + kMsgBytes;
 
 // Shared-memory map (offsets from a 1024-aligned base).  Identical in both CTAs so
 // that a local offset names the same object in the peer.
@@ -85,8 +87,8 @@ constexpr int kOffStage = 0;                           // kStages (score) / kSta
 constexpr int kOffRope = kStages * kStageDC;           // score CTA: kStages x 8 KB RoPE chunks
 constexpr int kOffX = kOffRope + kStages * kChunk;     // score CTA: reference exchange between groups
 constexpr int kOffP = kStagesO * kStageDC;             // output CTA: kPBufs P tiles
-constexpr int kOffRef = kOffP + kPBufs * kPBytes;      // output CTA: kPBufs x 128 references
-constexpr int kOffEpi = kOffRef + kPBufs * kRefBytes;  // output CTA: per-row (m, l) for the epilogue helpers
+constexpr int kOffRef = kOffP + kPBufs * kPBytes;      // output CTA: kPBufs x 128 (reference, row sum) pairs
+constexpr int kOffEpi = kOffRef + kPBufs * kMsgBytes;  // output CTA: per-row (m, l) for the epilogue helpers
 constexpr int kStgBytes = kM * 64;                     // output CTA: one [128 rows][32 columns] bf16 output tile
 constexpr int kOffStg = kOffEpi + 2 * kRefBytes;       // output CTA: two staging tiles (one per epilogue group)
 constexpr int kOffBar = (kOffX + kRefBytes > kOffEpi + 2 * kRefBytes) ? kOffX + kRefBytes : kOffEpi + 2 * kRefBytes;
@@ -124,6 +126,7 @@ struct Misc {                     // at kOffMisc
   int abort;
   long long lo, hi, cum0;
   int b0, len0;
+  int active;  // this cluster has a run
 };
 static_assert(sizeof(Misc) <= 128, "misc");
 
@@ -157,7 +160,7 @@ struct Args {
                                //   problem's first block and end, the run's first block
   float* part_m;               // [2 kMaxPairs][128] running max (log2 units)
   float* part_l;               // [2 kMaxPairs][128] running sum
-  float* part_s;               // [2 kMaxPairs][2][128] max |O| of each half row (columns 0-255, 256-511)
+  float* part_s;               // [2 kMaxPairs][16][128] max |O| over each 32 latent columns of a row
   __half* part_o;              // [2 kMaxPairs][256][128][2] O / part_s in fp16: column pairs, head, pair
   __nv_bfloat16* o_lat;        // [NP][H][512]
   float* lse;                  // [NP][H] natural-log LSE, or nullptr
@@ -209,10 +212,10 @@ __device__ __forceinline__ uint32_t ring_chunk(uint32_t base, int st, int ch) {
 // cost C is cut into P equal runs, P = min(clusters, T, C / (sw + 1)) so that every
 // run holds at least one block.  A run starts at the first block whose cost position
 // (problem start + sw + block offset) reaches p C / P.  One warp.
-// The writer of the table (one CTA per launch) also checks every length, fills the
-// block prefix table and counts the problems with no rows; each run records its
-// first block and the problem holding it for the combine.
-__device__ void plan_run(const Args& a, Misc* misc, bool write_table, bool write_bnd) {
+// The writer of the table (one warp per launch) also checks every length, fills the
+// block prefix table and counts the problems with no rows.  Reads only the problem
+// lengths; writes the workspace only with write_table.
+__device__ void plan_run(const Args& a, Misc* misc, bool write_table) {
   const int lane = threadIdx.x & 31;
   const int sw = a.switch_cost;
   long long T = 0;
@@ -290,13 +293,7 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table, bool write
     misc->b0 = b0;
     misc->cum0 = cum0;
     misc->len0 = len0;
-    if (write_bnd && active) {
-      int32_t* e = a.bnd + 4 * cluster_id_x();
-      e[0] = b0;
-      e[1] = static_cast<int32_t>(cum0);
-      e[2] = static_cast<int32_t>(cum0 + (len0 + kBN - 1) / kBN);
-      e[3] = static_cast<int32_t>(lo);
-    }
+    misc->active = active ? 1 : 0;
     if (write_table) {
       a.cum[a.NP] = static_cast<int32_t>(T);
       a.hdr[0] = static_cast<int32_t>(T);
@@ -357,34 +354,36 @@ __device__ __forceinline__ void store_output(const Args& a, const CUtensorMap* o
       }
     }
   } else {
-    // a piece: O of this half row scaled by its largest magnitude and stored in fp16
-    // (the pieces are merged into bf16 outputs; |O / max| <= 1 keeps fp16 in range and
-    // its 11-bit significand well below the output's rounding).  Stores go by column
-    // pairs, [pair][head][2], so a warp writes 128 contiguous bytes per pair.
+    // a piece: every 32 columns of the row scaled by their largest magnitude and stored
+    // in fp16 (the pieces are merged into bf16 outputs; |O / max| <= 1 keeps fp16 in
+    // range and its 11-bit significand well below the output's rounding).  One pass
+    // over tensor memory, the next chunk's load in flight while a chunk is stored.
+    // Stores go by column pairs, [pair][head][2], so a warp writes 128 contiguous
+    // bytes per pair.
     const long long slot = piece_slot(c, b0);
-    float mx = 0.f;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(a.part_o) + slot * (kDC / 2 * kM) + (col0 / 2) * kM + r;
+    float* sdst = a.part_s + (slot * kChunksPerRow + col0 / 32) * kM + r;
+    uint32_t v[32];
+    tmem_ld32(trow + col0, v);
     for (int cc = 0; cc < 8; ++cc) {
-      uint32_t v[32];
-      tmem_ld32(trow + col0 + cc * 32, v);
       tmem_wait_ld();
+      float mx = 0.f;
 #pragma unroll
       for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fabsf(__uint_as_float(v[j])));
-    }
-    const float inv = mx > 0.f ? 1.f / mx : 0.f;
-    uint32_t* dst = reinterpret_cast<uint32_t*>(a.part_o) + slot * (kDC / 2 * kM) + (col0 / 2) * kM + r;
-    for (int cc = 0; cc < 8; ++cc) {
-      uint32_t v[32];
-      tmem_ld32(trow + col0 + cc * 32, v);
-      tmem_wait_ld();
+      const float inv = mx > 0.f ? 1.f / mx : 0.f;
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const __half2 hv = __floats2half2_rn(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
+        w[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      if (cc + 1 < 8) tmem_ld32(trow + col0 + (cc + 1) * 32, v);
       if (r < a.H) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const __half2 hv = __floats2half2_rn(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
-          dst[(cc * 16 + j / 2) * kM] = *reinterpret_cast<const uint32_t*>(&hv);
-        }
+        for (int j = 0; j < 16; ++j) dst[(cc * 16 + j) * kM] = w[j];
+        sdst[cc * kM] = mx;
       }
     }
-    if (r < a.H) a.part_s[(slot * 2 + col0 / (kDC / 2)) * kM + r] = mx;
   }
 }
 
@@ -445,10 +444,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     tmem_relinquish();
   }
   if (threadIdx.x == 0) MLA_TRACE_POINT(63, score_cta ? 0 : 2);
+  // the run plan reads only the problem lengths (seq_lens / q_start, which no kernel
+  // of this library writes), so it overlaps the previous kernel's tail
+  if (warp == 2) plan_run(a, misc, false);
   griddep_launch();
   // the workspace, o_lat and q_cat may still be in use by the previous kernels
   griddep_wait();
-  if (warp == 2) plan_run(a, misc, cluster_id_x() == 0 && score_cta, score_cta);
+  if (score_cta && warp == 3 && cluster_id_x() == 0) {
+    Misc tmp;
+    plan_run(a, &tmp, true);  // the block table and run count for the combine
+  }
+  if (score_cta && threadIdx.x == 64 && misc->active) {  // this run's record for the combine
+    int32_t* e = a.bnd + 4 * cluster_id_x();
+    e[0] = misc->b0;
+    e[1] = static_cast<int32_t>(misc->cum0);
+    e[2] = static_cast<int32_t>(misc->cum0 + (misc->len0 + kBN - 1) / kBN);
+    e[3] = static_cast<int32_t>(misc->lo);
+  }
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // peer barriers initialised before any remote arrive
@@ -465,8 +477,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     Cursor c;
     c.start(*misc, a.pb);
     int li = 0;  // ring load index: the score CTA's ring also carries each problem's query
+    // 64 cache rows of block c into ring slot st
+    auto load_block = [&](const Cursor& cb, int st) {
+      mbar_arrive_expect_tx_if(leader, bar_addr(sbase, kBarFull + st), nload * kChunk);
+      for (int ch = 0; ch < nload; ++ch)
+        tma_load_3d_if(leader, ring_chunk(sbase, st, ch), &map, bar_addr(sbase, kBarFull + st), ch * 64, cb.t0(),
+                       cb.cs);
+    };
+    bool head_loaded = false;  // the run's first block went out ahead of its query
     for (int k = 0; c.ok(); c.next(), ++k) {
       if (score_cta && c.first()) {
+        if (k == 0) {
+          // run start: every slot is free, so the first block (HBM latency) is issued
+          // before the query (likely in L2) that precedes it in ring order
+          load_block(c, 2 % kStages);
+          head_loaded = true;
+        }
         // the problem's query, rows 0..63 and 64..127, as 64 x 64 boxes into two ring
         // slots (latent area: 8 boxes, RoPE area: the ninth); the softmax threads move
         // it into tensor memory and the MMA warp releases the slots
@@ -478,19 +504,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
             tma_load_2d_if(leader, ring_chunk(sbase, st, ch), &qmap, bar_addr(sbase, kBarFull + st), ch * 64,
                            c.b * a.H + part * kBN);
         }
-        // meanwhile the next problem's query moves into L2
-        if (c.b + 1 < a.NP)
-          prefetch_l2_bulk_if(leader, a.q_cat + static_cast<long long>(c.b + 1) * a.H * a.R,
-                              static_cast<uint32_t>(a.H * a.R * 2));
+      } else if (score_cta && c.g == c.cum + 1 && c.b + 1 < a.NP) {
+        // the problem's second block: the next problem's query moves into L2 meanwhile
+        prefetch_l2_bulk_if(leader, a.q_cat + static_cast<long long>(c.b + 1) * a.H * a.R,
+                            static_cast<uint32_t>(a.H * a.R * 2));
       }
       const int st = (score_cta ? li : k) % nst;
       const int ph = (score_cta ? li : k) / nst;
       ++li;
+      if (head_loaded) {
+        head_loaded = false;
+        continue;
+      }
       if (!warp_wait(bar_addr(sbase, kBarEmpty + st), (ph & 1) ^ 1, abort)) break;
       MLA_TRACE_POINT(k, score_cta ? 8 : 7);
-      mbar_arrive_expect_tx_if(leader, bar_addr(sbase, kBarFull + st), nload * kChunk);
-      for (int ch = 0; ch < nload; ++ch)
-        tma_load_3d_if(leader, ring_chunk(sbase, st, ch), &map, bar_addr(sbase, kBarFull + st), ch * 64, c.t0(), c.cs);
+      load_block(c, st);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -514,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         }
         const int st = li % kStages, sb = k % kSBufs;
         if (!warp_wait(bar_addr(sbase, kBarFull + st), (li / kStages) & 1, abort)) break;
+        MLA_TRACE_POINT(k, 13);
         ++li;
         if (!warp_wait(bar_addr(sbase, kBarSEmpty + sb), ((k / kSBufs) & 1) ^ 1, abort)) break;
         MLA_TRACE_POINT(k, 0);
@@ -557,6 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
             mma_ss_if(leader, tmem + half * 256, adesc, sdesc_sw128(stage + half * 4 * kChunk + kk * 16 * 128, kChunk, 1024),
                       idesc, acc0 | (kk > 0 ? 1u : 0u));
         }
+        MLA_TRACE_POINT(k, 13);
         tc_commit_if(leader, bar_addr(sbase, kBarEmpty + st));
         tc_commit_if(leader, bar_addr(sbase, kBarODone + pb));
         tc_commit_mc_if(leader, bar_addr(sbase, kBarPFree + pb), static_cast<uint16_t>(1u));  // to the score CTA
@@ -656,6 +686,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         const float p1 = fast_exp2(fmaf(__uint_as_float(sr[j + 1]), a.scale_log2, neg));
         pk[j >> 1] = pack_bf16x2(p0, p1);
       }
+      // the row sum of the probabilities as rounded to bf16, i.e. of the values the
+      // PV product multiplies (the output CTA normalises by exactly what it summed)
+      float psum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        psum[j & 3] += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xFFFF0000u);
+      const float ps = (psum[0] + psum[1]) + (psum[2] + psum[3]);
+      if (r == 0) MLA_TRACE_POINT(k, 14);
       if (!warp_wait(bar_addr(sbase, kBarPFree + pb), ((k / kPBufs) & 1) ^ 1, abort)) break;
       if (r == 0) MLA_TRACE_POINT(k, 2);
       // P row r into the output CTA's P tile (K-major, 128-byte swizzle) and the row's
@@ -665,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc)
         st_async_v4(prow + ((cc ^ (r & 7)) << 4), pbar, 1u, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      st_async_b32(sbase + kOffRef + pb * kRefBytes + r * 4, pbar, 1u, __float_as_uint(m_ref));
+      st_async_v2(sbase + kOffRef + pb * kMsgBytes + r * 8, pbar, 1u, __float_as_uint(m_ref), __float_as_uint(ps));
       if (r == 0) MLA_TRACE_POINT(k, 3);
     }
     // the output CTA has consumed this group's last tile (its release, an arrival
@@ -687,7 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       const int pb = k % kPBufs, st = k % kStagesO;
       if (!warp_wait<true>(bar_addr(sbase, kBarPFull + pb), (k / kPBufs) & 1, abort)) break;
       if (r == 0) MLA_TRACE_POINT(k, 4);
-      const float ref = reinterpret_cast<const float*>(gbase + kOffRef + pb * kRefBytes)[r];
+      const float2 msg = reinterpret_cast<const float2*>(gbase + kOffRef + pb * kMsgBytes)[r];
+      const float ref = msg.x, ps = msg.y;
       float alpha = 1.f;
       if (!c.first()) alpha = fast_exp2(m - ref);
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
@@ -722,19 +761,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       fence_proxy_async_cta();  // P arrived through st.async; zeroed rows through generic stores
       tc_fence_before();
       mbar_arrive(bar_addr(sbase, kBarPvGo + pb));
-      // the row sum of the P tile as stored, i.e. of the values the MMA multiplies
-      // (the MMA only reads the tile too).  The eight 16-byte pieces of a row are read
-      // in swizzled order (piece cc ^ r % 8): the order does not matter to the sum,
-      // and the 8 rows of a quarter warp then hit 8 distinct bank groups
-      const uint8_t* prow = gbase + kOffP + pb * kPBytes + (r >> 3) * 1024 + (r & 7) * 128;
-      float ps = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        const uint4 v = *reinterpret_cast<const uint4*>(prow + ((cc ^ (r & 7)) << 4));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ps += __uint_as_float(w[i] << 16) + __uint_as_float(w[i] & 0xFFFF0000u);
-      }
       l = c.first() ? ps : l * alpha + ps;
       m = ref;
       // this buffer's next tile (block k + kPBufs) is sent only after PV of block k
@@ -852,7 +878,7 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
         const long long slot = q == p_first ? slot_first : 2 * static_cast<long long>(q);
         m[u] = *reinterpret_cast<const float2*>(a.part_m + slot * kM + h0);
         l[u] = *reinterpret_cast<const float2*>(a.part_l + slot * kM + h0);
-        const float2 sc = *reinterpret_cast<const float2*>(a.part_s + (slot * 2 + c0 / (kDC / 2)) * kM + h0);
+        const float2 sc = *reinterpret_cast<const float2*>(a.part_s + (slot * kChunksPerRow + cb32) * kM + h0);
         // [pair][head][2]: heads h0, h0 + 1 of column pair cp are 4 consecutive halves
         const __half* src = a.part_o + (slot * (kDC / 2 * kM) + static_cast<long long>(c0 / 2) * kM + h0) * 2;
 #pragma unroll
@@ -999,7 +1025,7 @@ constexpr WsLayout ws_layout(long long np) {
   w.m = w.cum + align256(sizeof(int32_t) * static_cast<size_t>(np + 1));
   w.l = w.m + align256(sizeof(float) * slots * kM);
   w.s = w.l + align256(sizeof(float) * slots * kM);
-  w.o = w.s + align256(sizeof(float) * slots * 2 * kM);
+  w.o = w.s + align256(sizeof(float) * slots * kChunksPerRow * kM);
   w.total = w.o + 2 * slots * kM * kDC;  // fp16
   return w;
 }

@@ -253,6 +253,13 @@ __device__ __forceinline__ void st_async_v4(uint32_t local, uint32_t bar, uint32
       :: "r"(local), "r"(bar), "r"(cta), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+__device__ __forceinline__ void st_async_v2(uint32_t local, uint32_t bar, uint32_t cta, uint32_t a, uint32_t b) {
+  asm volatile(
+      "{\n\t.reg .b32 ra, rb;\n\tmapa.shared::cluster.u32 ra, %0, %2;\n\tmapa.shared::cluster.u32 rb, %1, %2;\n\t"
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [ra], {%3, %4}, [rb];\n\t}"
+      :: "r"(local), "r"(bar), "r"(cta), "r"(a), "r"(b) : "memory");
+}
+
 __device__ __forceinline__ void st_async_b32(uint32_t local, uint32_t bar, uint32_t cta, uint32_t v) {
   asm volatile(
       "{\n\t.reg .b32 ra, rb;\n\tmapa.shared::cluster.u32 ra, %0, %2;\n\tmapa.shared::cluster.u32 rb, %1, %2;\n\t"
