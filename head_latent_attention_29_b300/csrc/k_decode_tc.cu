@@ -833,9 +833,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 // owns heads 2(t % 64), +1 and columns 8(t / 64)..+7: a warp reads 256 contiguous
 // bytes per column of a piece, and up to kCombinePieces pieces are in flight at once
 // (their maximum first, then one weighted sum).  The merged tile is staged in shared
-// memory ([head][column], padded rows) and written out as 64-byte runs.
+// memory ([head][column], padded rows) and written out as 64-byte runs.  Two pieces
+// per round keep a thread at 64 registers, so four blocks fit on an SM and a B = 32
+// launch's ~530 blocks run in one wave.
 constexpr int kCombineThreads = 256;
-constexpr int kCombinePieces = 4;
+constexpr int kCombinePieces = 2;
 
 __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, long long P, __nv_bfloat16* s_o,
                                              const int32_t* bnd) {
@@ -954,7 +956,7 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
 // Block (x, j) merges columns [32 x, 32 x + 32) of the j-th problem that needs a
 // merge (found from the run table: boundary p cuts a problem and is the first
 // boundary inside it); the last row of blocks writes the problems with no rows.
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Args a) {
+__global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(const Args a) {
   __shared__ __align__(16) __nv_bfloat16 s_o[kM * 40];
   __shared__ int32_t s_bnd[4 * kMaxPairs];
   __shared__ int s_p;
