@@ -24,7 +24,7 @@ import torch
 
 __all__ = [
     "MlaError", "LatentCache", "lib", "cache_append", "absorb_q", "decode_workspace",
-    "decode_attn", "decode_attn_noalloc", "out_up", "gate", "get_device_error", "LIB_PATH",
+    "decode_attn", "decode_attn_noalloc", "out_up", "gate", "get_device_error", "debug_inject_fault", "LIB_PATH",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -73,6 +73,7 @@ _SIGS = {
     "mla_gate": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]),
     "mla_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+    "mla_debug_inject_fault": (ctypes.c_int, [ctypes.c_int32]),
     "mla_decode_attn_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(_Cache), ctypes.c_void_p,
                                                ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p]),
@@ -282,3 +283,10 @@ def get_device_error() -> tuple[int, int]:
     word = ctypes.c_uint32(0)
     st = lib().mla_get_device_error(ctypes.byref(word))
     return st, word.value
+
+
+def debug_inject_fault(kind: int) -> None:
+    """Fault injection for tests of the bounded waits: kind 1 makes later bf16
+    attention launches issue no loads in their score CTAs, so their waits run out
+    (MLA_ERR_DEVICE_TIMEOUT in the device error word); kind 0 switches it off."""
+    _check(lib().mla_debug_inject_fault(int(kind)), "mla_debug_inject_fault")

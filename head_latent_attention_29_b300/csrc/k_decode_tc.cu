@@ -164,6 +164,8 @@ struct Args {
   __half* part_o;              // [2 kMaxPairs][256][128][2] O / part_s in fp16: column pairs, head, pair
   __nv_bfloat16* o_lat;        // [NP][H][512]
   float* lse;                  // [NP][H] natural-log LSE, or nullptr
+  int fault;                   // injected fault for tests of the failure detection: 1 = the score CTA
+                               //   issues no loads, so the waits on them run out (0 in normal use)
 };
 
 // Walks the 64-token blocks [lo, hi) of the flattened token stream.
@@ -485,7 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
                        cb.cs);
     };
     bool head_loaded = false;  // the run's first block went out ahead of its query
-    for (int k = 0; c.ok(); c.next(), ++k) {
+    const bool skip_loads = score_cta && a.fault == 1;
+    for (int k = 0; c.ok() && !skip_loads; c.next(), ++k) {
       if (score_cta && c.first()) {
         if (k == 0) {
           // run start: every slot is free, so the first block (HBM latency) is issued
@@ -1032,6 +1035,9 @@ constexpr WsLayout ws_layout(long long np) {
   return w;
 }
 
+// Fault injection for the tests of the bounded waits (see mla_debug_inject_fault).
+static int g_inject_fault = 0;
+
 static int pairs_for_device() {
   static int cached[64] = {0};
   int dev = 0;
@@ -1060,6 +1066,8 @@ static int pairs_for_device() {
 }  // namespace dtc
 
 size_t decode_tc_workspace_size(int32_t B) { return dtc::ws_layout(B).total; }
+
+void set_fault_injection(int32_t kind) { dtc::g_inject_fault = kind == 1 ? 1 : 0; }
 
 size_t prefill_tc_workspace_size(int32_t B, int32_t S) {
   return dtc::ws_layout(static_cast<long long>(B) * S).total;
@@ -1133,6 +1141,7 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   a.part_o = reinterpret_cast<__half*>(wsb + w.o);
   a.o_lat = static_cast<__nv_bfloat16*>(o_lat);
   a.lse = lse;
+  a.fault = g_inject_fault;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * npairs, 1, 1);

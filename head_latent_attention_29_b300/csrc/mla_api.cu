@@ -151,6 +151,12 @@ MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, 
   return mla::launch_gate(h, w_g, o, B, d_model, width, dtype, as_stream(stream));
 }
 
+MLA_API mla_status mla_debug_inject_fault(int32_t kind) {
+  if (kind != 0 && kind != 1) return MLA_ERR_INVALID_ARG;
+  mla::set_fault_injection(kind);
+  return MLA_OK;
+}
+
 MLA_API mla_status mla_get_device_error(uint32_t* detail) {
   if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
   unsigned int word = 0;

@@ -137,6 +137,7 @@ mla_status launch_prefill_f32(const float* q_cat, const mla_cache& c, const int3
                               int32_t causal, int32_t H, float scale, float* o_lat, float* lse, cudaStream_t s);
 
 // tensor-core decode and prefill (bf16): sizes and launch
+void set_fault_injection(int32_t kind);
 size_t decode_tc_workspace_size(int32_t B);
 size_t prefill_tc_workspace_size(int32_t B, int32_t S);
 mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,

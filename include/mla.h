@@ -243,6 +243,20 @@ MLA_API mla_status mla_decode_attn_noalloc(const void* q_cat, const mla_cache* c
  */
 MLA_API mla_status mla_get_device_error(uint32_t* detail);
 
+/*
+ * mla_debug_inject_fault -- fault injection for tests of the failure detection.
+ *   (No counterpart on the pages: it exercises this library's bounded waits.)
+ *   kind = 1: every later mla_decode_attn / mla_prefill_attn launch on the bf16
+ *   tensor-core path issues no cache or query loads in its score CTAs, so the
+ *   waits on those loads run out after their bound (about one second): the call
+ *   records MLA_ERR_DEVICE_TIMEOUT in the device error word, its outputs are
+ *   undefined, and the CUDA context stays usable.  kind = 0 switches it off.
+ *   Nothing faults, traps or hangs.  Process-wide setting, not synchronised
+ *   between host threads; for tests only.  Returns MLA_ERR_INVALID_ARG for any
+ *   other kind.
+ */
+MLA_API mla_status mla_debug_inject_fault(int32_t kind);
+
 #ifdef __cplusplus
 }
 #endif
