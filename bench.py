@@ -624,10 +624,17 @@ def _ncu_traffic(workload):
 
 
 def _kernel_hash():
+    """sha256[:16] of the attention kernels' source with comments and blank space
+    removed, so that the stored DRAM counters follow code changes, not comment edits."""
     import hashlib
+    import re
     p = os.path.join(ROOT, "head_latent_attention_29_b300", "csrc", "k_decode_tc.cu")
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(p) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    code = "\n".join(line.strip() for line in src.splitlines() if line.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 # ---------------------------------------------------------------- CPU oracle baseline

@@ -13,32 +13,35 @@
 //    the whole tensor memory of one SM.  Each unit of work therefore runs on a
 //    2-CTA cluster:
 //      - CTA 0 (score CTA) holds the absorbed query in tensor memory (A operand
-//        of S = Q C^T, 288 columns), computes S for 64-token blocks into a
-//        double-buffered 64-column accumulator, runs the online softmax (one
-//        thread per head row, no cross-thread reduction), and writes the bf16
-//        probabilities P straight into CTA 1's shared memory with st.async,
-//        which completes bytes on CTA 1's barrier (no cluster-scope fences on
-//        the producer side).
+//        of S = Q C^T, 288 columns), computes S for 64-token blocks into three
+//        64-column accumulators, runs the online softmax (one thread per head
+//        row, no cross-thread reduction; two warpgroups on alternate blocks), and
+//        writes the bf16 probabilities P, with each row's reference maximum and
+//        the row sum of the rounded tile, straight into CTA 1's shared memory
+//        with st.async, which completes bytes on CTA 1's barrier (no
+//        cluster-scope fences on the producer side).
 //      - CTA 1 (output CTA) accumulates O += P C[:, 0:512] with two N = 256
 //        MMAs per 16-token step into its full 512-column tensor memory, and
 //        rescales O in place on the rare blocks where the running maximum of a
 //        row grew by more than 2^8.
 //    The two contractions (576 and 512 wide) are split across the two SMs with
 //    no redundant work.
-//  * Cache rows stream in through TMA (128-byte swizzled 64x64 chunks, 3-stage
-//    ring per CTA).  The same swizzled chunk is the K-major B operand of
-//    S = Q C^T and the MN-major B operand of O = P C.  The score CTA's ring also
+//  * Cache rows stream in through TMA (128-byte swizzled 64x64 chunks; a 3-slot
+//    ring in the score CTA, whose loads go to HBM, and a 2-slot ring in the output
+//    CTA, whose loads of the same rows hit L2).  The same swizzled chunk is the
+//    K-major B operand of S = Q C^T and the MN-major B operand of O = P C.  The
+//    score CTA's ring also
 //    carries each problem's query (two slots of 64 rows) on its way to tensor
 //    memory, so a new problem costs two ring loads instead of per-thread reads.
 //  * A "problem" is one query row group (all heads of one query) against a prefix
 //    of one cached sequence: in decode, sequence b's query against its N_b rows; in
 //    causal prefill, query i of sequence b against rows [0, start_b + i] (the rows
 //    of the prompt itself, already appended).  The blocks of all problems form one
-//    token stream that is cut into equal runs of 64-token blocks, one run per
-//    cluster, so every SM pair gets the same work whatever the mix of lengths.  A
-//    problem that lies inside one run is normalised and written out directly; one
-//    cut by run boundaries leaves an unnormalised partial (m, l, O) per piece, and
-//    a combine kernel merges the pieces.
+//    token stream that is cut into runs of equal cost (blocks plus a fixed cost per
+//    problem), one run per cluster, so every SM pair gets the same work whatever
+//    the mix of lengths.  A problem that lies inside one run is normalised and
+//    written out directly; one cut by run boundaries leaves an unnormalised
+//    partial (m, l, O) per piece, and a combine kernel merges the pieces.
 #include <cmath>
 
 #include "mla_internal.cuh"
