@@ -94,3 +94,20 @@ def test_decode_metric_names_its_shape():
     m = bench.decode_metric("gated_h64_b16_n131072", W.WORKLOADS["gated_h64_b16_n131072"])
     assert "H=64" in m and "N=131072" in m and "no RoPE" in m and "gate" in m
     assert "ragged" in bench.decode_metric("ragged_h128_b64_n1k_32k", W.WORKLOADS["ragged_h128_b64_n1k_32k"])
+
+
+def test_stored_traffic_follows_kernel_code_not_comments(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    src = os.path.join(ROOT, "head_latent_attention_29_b300", "csrc", "k_decode_tc.cu")
+    with open(src) as f:
+        text = f.read()
+    d = tmp_path / "head_latent_attention_29_b300" / "csrc"
+    d.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (d / "k_decode_tc.cu").write_text(text)
+    h0 = bench._kernel_hash()
+    (d / "k_decode_tc.cu").write_text("// a new leading comment\n/* and a block\n comment */\n" + text + "\n\n")
+    assert bench._kernel_hash() == h0
+    (d / "k_decode_tc.cu").write_text(text.replace("constexpr int kBN = 64;", "constexpr int kBN = 32;"))
+    assert bench._kernel_hash() != h0
