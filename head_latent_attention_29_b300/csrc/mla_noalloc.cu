@@ -10,7 +10,7 @@
 // nothing.
 //
 // The buffer holds the workspace of a batch of up to kNoAllocMaxBatch sequences
-// (about 50 MB).  Every GPU that loads the library keeps it until the process
+// (about 22 MB).  Every GPU that loads the library keeps it until the process
 // exits.  All calls on a device share it, so calls whose kernels could overlap on
 // the GPU (different streams without ordering between them) race on it.  The
 // kernels overwrite every scratch word they later read (run table, partial

@@ -220,7 +220,7 @@ MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, 
  *   allocator that cannot be re-entered) or embedders that only own the input and
  *   output buffers.  This entry point computes exactly what mla_decode_attn does,
  *   with the same kernels, but takes the split-KV scratch from a buffer built into
- *   the library (about 21 MB per GPU that loads the library, held until the
+ *   the library (about 22 MB per GPU that loads the library, held until the
  *   process exits), so it allocates nothing.
  *   Arguments are those of mla_decode_attn minus the workspace.  Limits: bf16 cache
  *   only (MLA_ERR_UNSUPPORTED otherwise) and at most 32 sequences (cache->B > 32
