@@ -220,11 +220,28 @@ def workload_bytes_flops(cfg, lens):
     return bytes_attn, flops_attn
 
 
+def paged_block_table(lens, seed: int, page_rows: int = 64):
+    """Block table [B, max_blocks] int32 giving each sequence's 64-row blocks
+    distinct pages of one pool in a seeded random order (how pages end up after
+    sequences of a serving batch have grown and finished at different times), and
+    the pool size (exactly the pages the lengths need)."""
+    need = [-(-int(n) // page_rows) for n in lens]
+    max_blocks = max(1, max(need))
+    num_pages = max(1, sum(need))
+    perm = np.random.default_rng([seed, 0x9A6E]).permutation(num_pages).astype(np.int32)
+    table = np.zeros((len(lens), max_blocks), dtype=np.int32)
+    k = 0
+    for b, nb in enumerate(need):
+        table[b, :nb] = perm[k:k + nb]
+        k += nb
+    return table, num_pages
+
+
 class DeviceWorkload:
     """Resident inputs of one replica: ROTATE latent caches, each with a captured
     decode-step graph, shared weights and the step's pinned host inputs."""
 
-    def __init__(self, name: str, seed: int, device, rotate: int = ROTATE):
+    def __init__(self, name: str, seed: int, device, rotate: int = ROTATE, paged: bool = False):
         import torch
         import head_latent_attention_29_b300 as mla
         from head_latent_attention_29_b300.step import DecodeStep
@@ -245,17 +262,30 @@ class DeviceWorkload:
             return torch.from_numpy(np.ascontiguousarray(W.bf16_bits(x)).view(np.int16)).view(bf).pin_memory()
 
         # cache copy 0 is filled from the seeded draws through the library's own
-        # append (RoPE on the key); the other copies are device-side clones
-        c0 = mla.LatentCache(B, N_max, d_c, d_r, dtype=bf, device=device)
+        # append (RoPE on the key); the other copies are device-side clones.  The
+        # paged variant draws every sequence's pages from one pool in shuffled order.
+        self.paged = paged
+        if paged:
+            table, num_pages = paged_block_table(self.lens, seed)
+            table = torch.from_numpy(table).to(device)
+
+            def new_cache(data=None):
+                return mla.PagedLatentCache(num_pages, B, table.shape[1], d_c, d_r, dtype=bf, device=device,
+                                            block_table=table, data=data)
+            append = mla.cache_append_paged
+        else:
+            def new_cache(data=None):
+                return mla.LatentCache(B, N_max, d_c, d_r, dtype=bf, device=device, data=data)
+            append = mla.cache_append
+        c0 = new_cache()
         for b in range(B):
             n = int(self.lens[b])
             c, k = W.latent_rows(cfg, seed, b, n)
             idx = torch.full((n,), b, dtype=torch.int32, device=device)
             pos = torch.arange(n, dtype=torch.int32, device=device)
-            mla.cache_append(c0, up(c), up(k) if d_r else None, idx, pos, rb)
+            append(c0, up(c), up(k) if d_r else None, idx, pos, rb)
         self.rotate = rotate
-        caches = [c0] + [mla.LatentCache(B, N_max, d_c, d_r, dtype=bf, device=device, data=c0.data.clone())
-                         for _ in range(rotate - 1)]
+        caches = [c0] + [new_cache(c0.data.clone()) for _ in range(rotate - 1)]
         w_uk, w_uv = W.up_weights(cfg, seed)
         w_uk, w_uv = up(w_uk), up(w_uv)
         self.gated = d_r == 0 and "d_model" in cfg
@@ -290,9 +320,10 @@ class DeviceWorkload:
         self.attn_graph = torch.cuda.CUDAGraph()
         s0 = self.steps[0]
         with torch.cuda.graph(self.attn_graph):
+            attend = mla.decode_attn_paged if paged else mla.decode_attn
             for i in range(10):
                 st = self.steps[i % rotate]
-                mla.decode_attn(st.q_cat, st.cache, seq_lens, cfg["scale"], st.ws, st.o_lat, st.lse)
+                attend(st.q_cat, st.cache, seq_lens, cfg["scale"], st.ws, st.o_lat, st.lse)
         self.kernels_per_step = s0.kernels_per_step
 
     def step(self, i: int):
@@ -304,7 +335,7 @@ def run_b300(args, rank, world, device):
     import torch.distributed as dist
 
     torch.cuda.set_device(device)
-    wl = DeviceWorkload(args.workload, args.seed + rank, device, args.rotate)
+    wl = DeviceWorkload(args.workload, args.seed + rank, device, args.rotate, getattr(args, "paged", False))
     cfg = wl.cfg
     stream = torch.cuda.current_stream(device)
 
@@ -366,7 +397,7 @@ def run_b300(args, rank, world, device):
     t_mem = bytes_attn / (hbm * 1e9)
     t_tc = flops_attn / (tc_burst * 1e12)
     roof_us = max(t_mem, t_tc) * 1e6
-    traffic = _ncu_traffic(args.workload)
+    traffic = None if wl.paged else _ncu_traffic(args.workload)  # counters were taken on the contiguous cache
 
     out = {
         "metric": decode_metric(args.workload, cfg),
@@ -387,6 +418,7 @@ def run_b300(args, rank, world, device):
             "parallelism": f"replicas x{world}",
             "l2": f"{wl.rotate} rotating cache copies ({wl.rotate * bytes_attn / 1e6:.0f} MB vs 126 MB L2)",
             "step": "append+absorb_q+decode_attn(split+combine)+out_up" + ("+gate" if wl.gated else ""),
+            "cache": "paged (64-row pages, shuffled block table)" if wl.paged else "contiguous [B, N_max, 576]",
         },
         "gpu_launches": wl.kernels_per_step * args.steps,
         "e2e": {"value": round(tokens_per_step / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -723,9 +755,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rotate", type=int, default=ROTATE, help="cache copies rotated between steps (>= 1)")
+    ap.add_argument("--paged", action="store_true",
+                    help="decode workloads: 64-row pages of one pool in shuffled order behind a block table")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.paged and "S" in W.WORKLOADS[args.workload]:
+        ap.error("--paged applies to decode workloads")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -25,6 +25,7 @@ import torch
 __all__ = [
     "MlaError", "LatentCache", "lib", "cache_append", "absorb_q", "decode_workspace",
     "decode_attn", "decode_attn_noalloc", "out_up", "gate", "get_device_error", "debug_inject_fault", "LIB_PATH",
+    "PagedLatentCache", "cache_append_paged", "decode_attn_paged", "PAGE_ROWS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -48,6 +49,16 @@ class _Cache(ctypes.Structure):
         ("_pad", ctypes.c_int32), ("row_stride", ctypes.c_int64),
     ]
 
+
+class _PagedCache(ctypes.Structure):
+    _fields_ = [
+        ("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+        ("d_c", ctypes.c_int32), ("d_r", ctypes.c_int32), ("row_stride", ctypes.c_int64),
+        ("block_table", ctypes.c_void_p), ("B", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
+    ]
+
+
+PAGE_ROWS = 64
 
 _lib_handle = None
 
@@ -74,6 +85,12 @@ _SIGS = {
                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]),
     "mla_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "mla_debug_inject_fault": (ctypes.c_int, [ctypes.c_int32]),
+    "mla_cache_append_paged": (ctypes.c_int, [ctypes.POINTER(_PagedCache), ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_float,
+                                              ctypes.c_void_p]),
+    "mla_decode_attn_paged": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(_PagedCache), ctypes.c_void_p,
+                                             ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "mla_decode_attn_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(_Cache), ctypes.c_void_p,
                                                ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p]),
@@ -290,3 +307,76 @@ def debug_inject_fault(kind: int) -> None:
     attention launches issue no loads in their score CTAs, so their waits run out
     (MLA_ERR_DEVICE_TIMEOUT in the device error word); kind 0 switches it off."""
     _check(lib().mla_debug_inject_fault(int(kind)), "mla_debug_inject_fault")
+
+
+class PagedLatentCache:
+    """A paged latent cache: a pool of ``num_pages`` pages of 64 rows
+    [num_pages, 64, row_stride] and a block table [B, max_blocks] int32 naming the
+    page of each 64-row block of each sequence (row t of sequence b is row t % 64 of
+    page block_table[b, t // 64]).  Both tensors are allocated by torch and owned by
+    this object unless passed in (``data``, ``block_table``); the caller fills the
+    block table."""
+
+    def __init__(self, num_pages: int, B: int, max_blocks: int, d_c: int, d_r: int, dtype=torch.bfloat16,
+                 device="cuda", row_stride: int | None = None, block_table: torch.Tensor | None = None,
+                 data: torch.Tensor | None = None):
+        esz = 2 if dtype == torch.bfloat16 else 4
+        R = d_c + d_r
+        if row_stride is None:
+            row_stride = ((R * esz + 15) // 16) * 16 // esz
+        self.num_pages, self.B, self.max_blocks = num_pages, B, max_blocks
+        self.d_c, self.d_r, self.row_stride, self.dtype = d_c, d_r, row_stride, dtype
+        if data is None:
+            data = torch.zeros((num_pages, PAGE_ROWS, row_stride), dtype=dtype, device=device)
+        elif tuple(data.shape) != (num_pages, PAGE_ROWS, row_stride) or data.dtype != dtype:
+            raise ValueError("page pool shape/dtype mismatch")
+        self.data = data
+        if block_table is None:
+            block_table = torch.zeros((B, max_blocks), dtype=torch.int32, device=device)
+        elif tuple(block_table.shape) != (B, max_blocks) or block_table.dtype != torch.int32:
+            raise ValueError("block table must be int32 [B, max_blocks]")
+        self.block_table = block_table.contiguous()
+
+    @property
+    def N_max(self) -> int:
+        return self.max_blocks * PAGE_ROWS
+
+    def struct(self) -> _PagedCache:
+        return _PagedCache(self.data.data_ptr(), _DT[self.dtype], self.num_pages, self.d_c, self.d_r,
+                           self.row_stride, self.block_table.data_ptr(), self.B, self.max_blocks)
+
+
+def cache_append_paged(cache: PagedLatentCache, c_kv: torch.Tensor, k_r: torch.Tensor | None,
+                       seq_idx: torch.Tensor, pos: torch.Tensor, rope_base: float = 10000.0) -> None:
+    """Write T rows into the paged cache (see cache_append)."""
+    _dev_tensor(c_kv, "c_kv", cache.dtype)
+    if cache.d_r > 0:
+        _dev_tensor(k_r, "k_r", cache.dtype)
+    _dev_tensor(seq_idx, "seq_idx", torch.int32)
+    _dev_tensor(pos, "pos", torch.int32)
+    st = cache.struct()
+    _check(lib().mla_cache_append_paged(ctypes.byref(st), _ptr(c_kv), _ptr(k_r if cache.d_r > 0 else None),
+                                        _ptr(seq_idx), _ptr(pos), seq_idx.numel(), float(rope_base),
+                                        _stream(c_kv)), "mla_cache_append_paged")
+
+
+def decode_attn_paged(q_cat: torch.Tensor, cache: PagedLatentCache, seq_lens: torch.Tensor, scale: float,
+                      workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                      lse: torch.Tensor | None = None, want_lse: bool = True):
+    """o_lat [B, H, d_c] (and lse [B, H]) of absorbed decode attention over a paged cache."""
+    _dev_tensor(q_cat, "q_cat", cache.dtype)
+    B, H, R = q_cat.shape
+    if B != cache.B or R != cache.d_c + cache.d_r:
+        raise ValueError("q_cat shape does not match the cache")
+    _dev_tensor(seq_lens, "seq_lens", torch.int32)
+    if workspace is None:
+        workspace = decode_workspace(B, H, cache.d_c, cache.dtype, q_cat.device)
+    if out is None:
+        out = torch.empty((B, H, cache.d_c), dtype=cache.dtype, device=q_cat.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q_cat.device)
+    st = cache.struct()
+    _check(lib().mla_decode_attn_paged(_ptr(q_cat), ctypes.byref(st), _ptr(seq_lens), H, float(scale),
+                                       _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse), _stream(q_cat)),
+           "mla_decode_attn_paged")
+    return out, lse

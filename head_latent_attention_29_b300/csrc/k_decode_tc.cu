@@ -169,6 +169,9 @@ struct Args {
   float* lse;                  // [NP][H] natural-log LSE, or nullptr
   int fault;                   // injected fault for tests of the failure detection: 1 = the score CTA
                                //   issues no loads, so the waits on them run out (0 in normal use)
+  const int32_t* block_table;  // paged cache: [seqs][max_blocks] page of each 64-row block; nullptr when
+                               //   the cache is contiguous
+  int max_blocks, num_pages;
 };
 
 // Walks the 64-token blocks [lo, hi) of the flattened token stream.
@@ -205,6 +208,25 @@ struct Cursor {
 };
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
+
+// TMA coordinates (row, plane) of the 64-row block of c: row t0 of sequence plane cs
+// in a contiguous cache; row 0 of the block's page in a paged pool (an index
+// outside the pool is recorded and page 0 read instead, so the load stays in
+// bounds and its barrier completes).
+__device__ __forceinline__ void block_coords(const Args& a, const Cursor& c, int* row, int* plane) {
+  if (a.block_table == nullptr) {
+    *row = c.t0();
+    *plane = c.cs;
+    return;
+  }
+  int pg = a.block_table[static_cast<long long>(c.cs) * a.max_blocks + c.t0() / kBN];
+  if (pg < 0 || pg >= a.num_pages) {
+    record_error(MLA_ERR_DEVICE_INDEX, kSitePageIndex);
+    pg = 0;
+  }
+  *row = 0;
+  *plane = pg;
+}
 
 // Shared address of 64-column chunk ch (8 KB: 64 rows x 128 bytes, 128-byte swizzle)
 // of ring slot st: chunks 0-7 in the slot's latent area, chunk 8 in its RoPE area.
@@ -484,10 +506,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     int li = 0;  // ring load index: the score CTA's ring also carries each problem's query
     // 64 cache rows of block c into ring slot st
     auto load_block = [&](const Cursor& cb, int st) {
+      int row, plane;
+      block_coords(a, cb, &row, &plane);
       mbar_arrive_expect_tx_if(leader, bar_addr(sbase, kBarFull + st), nload * kChunk);
       for (int ch = 0; ch < nload; ++ch)
-        tma_load_3d_if(leader, ring_chunk(sbase, st, ch), &map, bar_addr(sbase, kBarFull + st), ch * 64, cb.t0(),
-                       cb.cs);
+        tma_load_3d_if(leader, ring_chunk(sbase, st, ch), &map, bar_addr(sbase, kBarFull + st), ch * 64, row, plane);
     };
     bool head_loaded = false;  // the run's first block went out ahead of its query
     const bool skip_loads = score_cta && a.fault == 1;
@@ -1076,9 +1099,16 @@ size_t prefill_tc_workspace_size(int32_t B, int32_t S) {
   return dtc::ws_layout(static_cast<long long>(B) * S).total;
 }
 
+// A paged pool (table != nullptr) is passed as c with c.data the pool, c.B the
+// sequences and c.N_max = 64 x max_blocks.
+struct PagedView {
+  const int32_t* table;
+  int32_t max_blocks, num_pages;
+};
+
 static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dtc::Problems& pbs, long long np,
                                  int32_t H, float scale, void* ws, size_t ws_bytes, void* o_lat, float* lse,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, const PagedView& pv = PagedView{nullptr, 0, 0}) {
   using namespace dtc;
   const WsLayout w = ws_layout(np);
   if (ws == nullptr || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MLA_ERR_WORKSPACE;
@@ -1091,10 +1121,14 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
 
   const int R = c.d_c + c.d_r;
   CUtensorMap map;
-  const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(R), static_cast<cuuint64_t>(c.N_max),
-                              static_cast<cuuint64_t>(c.B)};
+  // contiguous: (R, N_max, B), one plane per sequence; paged: (R, 64, pages), one
+  // plane per page, every 64-row block a whole page
+  const bool paged = pv.table != nullptr;
+  const cuuint64_t plane_rows = paged ? static_cast<cuuint64_t>(kBN) : static_cast<cuuint64_t>(c.N_max);
+  const cuuint64_t planes = paged ? static_cast<cuuint64_t>(pv.num_pages) : static_cast<cuuint64_t>(c.B);
+  const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(R), plane_rows, planes};
   const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(c.row_stride) * 2,
-                                 static_cast<cuuint64_t>(c.row_stride) * 2 * static_cast<cuuint64_t>(c.N_max)};
+                                 static_cast<cuuint64_t>(c.row_stride) * 2 * plane_rows};
   const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBN), 1};
   const cuuint32_t estride[3] = {1, 1, 1};
   if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c.data, gdim, gstride, box, estride,
@@ -1145,6 +1179,9 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   a.o_lat = static_cast<__nv_bfloat16*>(o_lat);
   a.lse = lse;
   a.fault = g_inject_fault;
+  a.block_table = pv.table;
+  a.max_blocks = pv.max_blocks;
+  a.num_pages = pv.num_pages;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * npairs, 1, 1);
@@ -1169,14 +1206,16 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
 }
 
 mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
-                            float scale, void* ws, size_t ws_bytes, void* o_lat, float* lse, cudaStream_t s) {
+                            float scale, void* ws, size_t ws_bytes, void* o_lat, float* lse, cudaStream_t s,
+                            const int32_t* block_table, int32_t max_blocks, int32_t num_pages) {
   dtc::Problems p = {};
   p.seq_lens = seq_lens;
   p.q_start = nullptr;
   p.S = 1;
   p.causal = 0;
   p.n_max = c.N_max;
-  return launch_attn_tc(q_cat, c, p, c.B, H, scale, ws, ws_bytes, o_lat, lse, s);
+  return launch_attn_tc(q_cat, c, p, c.B, H, scale, ws, ws_bytes, o_lat, lse, s,
+                        PagedView{block_table, max_blocks, num_pages});
 }
 
 mla_status launch_prefill_tc(const void* q_cat, const mla_cache& c, const int32_t* q_start, int32_t S,

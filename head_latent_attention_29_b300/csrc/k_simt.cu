@@ -33,15 +33,24 @@ static void ensure_smem(const void* fn, size_t bytes) {
 // ============================================================================
 // Cache append: cache[seq][pos] = [c_kv || RoPE(k_r, pos)]
 // (icman.com.cn MLA article, section 2: the 64-wide key is cached with RoPE
-// applied; 0539edu.com section 5.2: the cache is written by position.)
+// applied; 0539edu.com section 5.2: the cache is written by position.)  With a
+// block table the cache is paged: row pos of sequence seq is row pos % 64 of page
+// table[seq][pos / 64] of the pool.
 // ============================================================================
+struct PageMap {
+  const int32_t* table;  // [B][max_blocks] page of each 64-row block, or nullptr (contiguous cache)
+  int32_t max_blocks;
+  int32_t num_pages;
+};
+
 template <typename T>
 __global__ void __launch_bounds__(128) cache_append_kernel(T* __restrict__ cache, int32_t B, int32_t N_max,
                                                            int32_t d_c, int32_t d_r, int64_t row_stride,
                                                            const T* __restrict__ c_kv, const T* __restrict__ k_r,
                                                            const int32_t* __restrict__ seq_idx,
                                                            const int32_t* __restrict__ pos, int32_t n_rows,
-                                                           const __grid_constant__ RopeTable rope, int vec_ok) {
+                                                           const __grid_constant__ RopeTable rope, int vec_ok,
+                                                           PageMap pages) {
   __shared__ float s_hi[64], s_lo[64];
   griddep_launch();
   rope_table_to_smem(rope, d_r / 2, s_hi, s_lo);
@@ -53,7 +62,16 @@ __global__ void __launch_bounds__(128) cache_append_kernel(T* __restrict__ cache
       if (threadIdx.x == 0) record_error(MLA_ERR_DEVICE_INDEX, kSiteAppendIndex);
       continue;
     }
-    T* dst = cache + (static_cast<int64_t>(b) * N_max + p) * row_stride;
+    int64_t row = static_cast<int64_t>(b) * N_max + p;
+    if (pages.table != nullptr) {
+      const int32_t pg = pages.table[static_cast<int64_t>(b) * pages.max_blocks + p / kPageRows];
+      if (pg < 0 || pg >= pages.num_pages) {
+        if (threadIdx.x == 0) record_error(MLA_ERR_DEVICE_INDEX, kSitePageIndex);
+        continue;
+      }
+      row = static_cast<int64_t>(pg) * kPageRows + p % kPageRows;
+    }
+    T* dst = cache + row * row_stride;
     const T* src = c_kv + i * d_c;
     if (vec_ok) {
       const int nvec = d_c * static_cast<int>(sizeof(T)) / 16;
@@ -76,7 +94,9 @@ __global__ void __launch_bounds__(128) cache_append_kernel(T* __restrict__ cache
 }
 
 mla_status launch_cache_append(const mla_cache& c, const void* c_kv, const void* k_r, const int32_t* seq_idx,
-                               const int32_t* pos, int32_t T, float rope_base, cudaStream_t s) {
+                               const int32_t* pos, int32_t T, float rope_base, cudaStream_t s,
+                               const int32_t* block_table, int32_t max_blocks, int32_t num_pages) {
+  const PageMap pages = {block_table, max_blocks, num_pages};
   const int grid = static_cast<int>(T < 148 * 16 ? T : 148 * 16);
   const size_t esz = c.dtype == MLA_BF16 ? 2 : 4;
   const int vec_ok = ((c.d_c * esz) % 16 == 0) && ((c.row_stride * esz) % 16 == 0) && aligned16(c_kv) &&
@@ -86,13 +106,13 @@ mla_status launch_cache_append(const mla_cache& c, const void* c_kv, const void*
                                      static_cast<__nv_bfloat16*>(c.data), c.B, c.N_max, c.d_c, c.d_r,
                                      static_cast<int64_t>(c.row_stride), static_cast<const __nv_bfloat16*>(c_kv),
                                      static_cast<const __nv_bfloat16*>(k_r), seq_idx, pos, T,
-                                     rope_table(c.d_r, rope_base), vec_ok);
+                                     rope_table(c.d_r, rope_base), vec_ok, pages);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
   } else {
     cache_append_kernel<float><<<grid, 128, 0, s>>>(static_cast<float*>(c.data), c.B, c.N_max, c.d_c, c.d_r,
                                                     c.row_stride, static_cast<const float*>(c_kv),
                                                     static_cast<const float*>(k_r), seq_idx, pos, T,
-                                                    rope_table(c.d_r, rope_base), vec_ok);
+                                                    rope_table(c.d_r, rope_base), vec_ok, pages);
   }
   return cuda_status(cudaGetLastError());
 }

@@ -24,6 +24,28 @@ mla_status check_cache(const mla_cache* c) {
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+// Checks a paged cache and views it as the contiguous form the launchers take:
+// B sequences of N_max = 64 x max_blocks rows over the page pool.
+mla_status check_paged(const mla_paged_cache* p, mla_cache* view) {
+  if (p == nullptr || p->data == nullptr || p->block_table == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!valid_dtype(p->dtype)) return MLA_ERR_INVALID_ARG;
+  if (p->num_pages <= 0 || p->B <= 0 || p->max_blocks <= 0 || p->d_c <= 0 || p->d_r < 0 || (p->d_r & 1) != 0)
+    return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(p->max_blocks) * MLA_PAGE_ROWS > INT32_MAX) return MLA_ERR_INVALID_ARG;
+  if (p->row_stride < static_cast<int64_t>(p->d_c) + p->d_r) return MLA_ERR_INVALID_ARG;
+  if ((p->row_stride * static_cast<int64_t>(elem_size(p->dtype))) % 16 != 0) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(p->data) || !aligned4(p->block_table)) return MLA_ERR_INVALID_ARG;
+  view->data = p->data;
+  view->dtype = p->dtype;
+  view->B = p->B;
+  view->N_max = p->max_blocks * MLA_PAGE_ROWS;
+  view->d_c = p->d_c;
+  view->d_r = p->d_r;
+  view->_pad = 0;
+  view->row_stride = p->row_stride;
+  return MLA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -149,6 +171,37 @@ MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, 
       aligned16(o))
     return mla::launch_gate_tc(h, w_g, o, B, d_model, width, as_stream(stream));
   return mla::launch_gate(h, w_g, o, B, d_model, width, dtype, as_stream(stream));
+}
+
+MLA_API mla_status mla_cache_append_paged(const mla_paged_cache* cache, const void* c_kv, const void* k_r,
+                                          const int32_t* seq_idx, const int32_t* pos, int32_t T, float rope_base,
+                                          void* stream) {
+  mla_cache view;
+  mla_status st = check_paged(cache, &view);
+  if (st != MLA_OK) return st;
+  if (T < 0) return MLA_ERR_INVALID_ARG;
+  if (T == 0) return MLA_OK;
+  if (c_kv == nullptr || seq_idx == nullptr || pos == nullptr) return MLA_ERR_INVALID_ARG;
+  if (view.d_r > 0 && k_r == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!(rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (view.d_r > 128) return MLA_ERR_UNSUPPORTED;
+  return mla::launch_cache_append(view, c_kv, k_r, seq_idx, pos, T, rope_base, as_stream(stream),
+                                  cache->block_table, cache->max_blocks, cache->num_pages);
+}
+
+MLA_API mla_status mla_decode_attn_paged(const void* q_cat, const mla_paged_cache* cache, const int32_t* seq_lens,
+                                         int32_t H, float scale, void* workspace, size_t workspace_bytes,
+                                         void* o_lat, float* lse, void* stream) {
+  mla_cache view;
+  mla_status st = check_paged(cache, &view);
+  if (st != MLA_OK) return st;
+  if (q_cat == nullptr || seq_lens == nullptr || o_lat == nullptr || H <= 0) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_cat) || !aligned16(o_lat)) return MLA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) && !(scale < 0.f) && scale != 0.f) return MLA_ERR_INVALID_ARG;  // NaN
+  if (view.dtype != MLA_BF16 || view.d_c != 512 || (view.d_r != 0 && view.d_r != 64) || H > 128)
+    return MLA_ERR_UNSUPPORTED;
+  return mla::launch_decode_tc(q_cat, view, seq_lens, H, scale, workspace, workspace_bytes, o_lat, lse,
+                               as_stream(stream), cache->block_table, cache->max_blocks, cache->num_pages);
 }
 
 MLA_API mla_status mla_debug_inject_fault(int32_t kind) {

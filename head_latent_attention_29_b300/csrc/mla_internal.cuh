@@ -23,6 +23,7 @@ enum ErrorSite : unsigned int {
   kSiteDecodeLength = 2,
   kSiteDecodeWait = 3,
   kSiteDecodeTmem = 4,
+  kSitePageIndex = 5,
 };
 
 __device__ __forceinline__ void record_error(mla_status st, unsigned int site) {
@@ -34,6 +35,8 @@ __device__ __forceinline__ float ld_elem(const float* p) { return *p; }
 __device__ __forceinline__ float ld_elem(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void st_elem(float* p, float v) { *p = v; }
 __device__ __forceinline__ void st_elem(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+constexpr int kPageRows = MLA_PAGE_ROWS;  // rows per page of a paged cache
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -111,8 +114,12 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 // ---- host launchers (one per kernel family), defined in the .cu files -------
+// block_table != nullptr: a paged pool viewed as c (c.B sequences of c.N_max = 64 x
+// max_blocks rows; c.data the pool of num_pages pages)
 mla_status launch_cache_append(const mla_cache& c, const void* c_kv, const void* k_r, const int32_t* seq_idx,
-                               const int32_t* pos, int32_t T, float rope_base, cudaStream_t s);
+                               const int32_t* pos, int32_t T, float rope_base, cudaStream_t s,
+                               const int32_t* block_table = nullptr, int32_t max_blocks = 0,
+                               int32_t num_pages = 0);
 mla_status launch_absorb_q(const void* q_nope, const void* q_rope, const int32_t* q_pos, const void* w_uk,
                            void* q_cat, int32_t B, int32_t H, int32_t d_k, int32_t d_c, int32_t d_r,
                            int32_t dtype, float rope_base, cudaStream_t s);
@@ -141,7 +148,8 @@ void set_fault_injection(int32_t kind);
 size_t decode_tc_workspace_size(int32_t B);
 size_t prefill_tc_workspace_size(int32_t B, int32_t S);
 mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
-                            float scale, void* ws, size_t ws_bytes, void* o_lat, float* lse, cudaStream_t s);
+                            float scale, void* ws, size_t ws_bytes, void* o_lat, float* lse, cudaStream_t s,
+                            const int32_t* block_table = nullptr, int32_t max_blocks = 0, int32_t num_pages = 0);
 mla_status launch_prefill_tc(const void* q_cat, const mla_cache& c, const int32_t* q_start, int32_t S,
                              int32_t causal, int32_t H, float scale, void* ws, size_t ws_bytes, void* o_lat,
                              float* lse, cudaStream_t s);

@@ -10,19 +10,21 @@ from __future__ import annotations
 
 import torch
 
-from . import LatentCache, absorb_q, cache_append, decode_attn, decode_workspace, gate, out_up
+from . import (LatentCache, PagedLatentCache, absorb_q, cache_append, cache_append_paged, decode_attn,
+               decode_attn_paged, decode_workspace, gate, out_up)
 
 
 class DecodeStep:
-    """Static buffers + captured graph of one decode step over `cache`.
+    """Static buffers + captured graph of one decode step over `cache` (a
+    LatentCache, or a PagedLatentCache whose block table covers every sequence).
 
     Step inputs (device, static): c_kv [B, d_c], k_r [B, d_r], q_nope [B, H, d_k],
     q_rope [B, H, d_r], optional h [B, d_model]; the new token of sequence b is
     written at position seq_lens[b] - 1 and attends to seq_lens[b] tokens.
     Output: o [B, H, d_v] (gated in place when W_g is given)."""
 
-    def __init__(self, cache: LatentCache, w_uk: torch.Tensor, w_uv: torch.Tensor, seq_lens: torch.Tensor,
-                 scale: float, rope_base: float = 10000.0, w_g: torch.Tensor | None = None,
+    def __init__(self, cache: LatentCache | PagedLatentCache, w_uk: torch.Tensor, w_uv: torch.Tensor,
+                 seq_lens: torch.Tensor, scale: float, rope_base: float = 10000.0, w_g: torch.Tensor | None = None,
                  stream: torch.cuda.Stream | None = None):
         dev = cache.data.device
         self.cache, self.w_uk, self.w_uv, self.w_g = cache, w_uk, w_uv, w_g
@@ -55,9 +57,11 @@ class DecodeStep:
     def launch(self) -> None:
         """Queue the step's kernels on the current stream (no graph)."""
         d = self.inputs
-        cache_append(self.cache, d["c_kv"], d.get("k_r"), self.seq_idx, self.pos, self.rope_base)
+        paged = isinstance(self.cache, PagedLatentCache)
+        append, attend = (cache_append_paged, decode_attn_paged) if paged else (cache_append, decode_attn)
+        append(self.cache, d["c_kv"], d.get("k_r"), self.seq_idx, self.pos, self.rope_base)
         absorb_q(d["q_nope"], d.get("q_rope"), self.pos, self.w_uk, self.rope_base, out=self.q_cat)
-        decode_attn(self.q_cat, self.cache, self.seq_lens, self.scale, self.ws, self.o_lat, self.lse)
+        attend(self.q_cat, self.cache, self.seq_lens, self.scale, self.ws, self.o_lat, self.lse)
         out_up(self.o_lat, self.w_uv, out=self.o)
         if self.w_g is not None:
             gate(d["h"], self.w_g, self.o.view(self.B, -1))

@@ -81,6 +81,27 @@ typedef struct {
   int64_t row_stride; /* elements between consecutive rows                        */
 } mla_cache;
 
+/*
+ * A paged latent cache: rows live in fixed pages of MLA_PAGE_ROWS rows taken from
+ * one pool, so sequences can grow without a per-sequence preallocation (the
+ * position-indexed buffer of 0539edu.com section 5.2, split into pages).  Row t of
+ * sequence b is row t % MLA_PAGE_ROWS of page block_table[b][t / MLA_PAGE_ROWS],
+ * and holds [c_KV(t) || RoPE(k_R(t), t)] like mla_cache.  The caller owns the pool,
+ * the block table and the page assignment; a page may belong to one sequence only.
+ */
+#define MLA_PAGE_ROWS 64
+typedef struct {
+  void* data;                  /* device pointer, [num_pages][MLA_PAGE_ROWS][row_stride] */
+  int32_t dtype;               /* mla_dtype                                               */
+  int32_t num_pages;           /* pages in the pool                                       */
+  int32_t d_c;                 /* latent width                                            */
+  int32_t d_r;                 /* decoupled RoPE key width (0 = no positional key)        */
+  int64_t row_stride;          /* elements between consecutive rows (same rules as above) */
+  const int32_t* block_table;  /* device pointer, [B][max_blocks] int32 page indices      */
+  int32_t B;                   /* sequences                                               */
+  int32_t max_blocks;          /* block-table entries per sequence; lengths <= 64 x this  */
+} mla_paged_cache;
+
 /* Version of this ABI (bumped on any incompatible change). */
 MLA_API int32_t mla_abi_version(void);
 
@@ -211,6 +232,33 @@ MLA_API mla_status mla_out_up(const void* o_lat, const void* w_uv, void* o, int3
  */
 MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, int32_t d_model,
                             int32_t width, int32_t dtype, void* stream);
+
+/*
+ * mla_cache_append_paged -- mla_cache_append into a paged cache: row
+ *   (seq_idx[i], pos[i]) goes to row pos[i] % MLA_PAGE_ROWS of page
+ *   block_table[seq_idx[i]][pos[i] / MLA_PAGE_ROWS].  Arguments and RoPE as
+ *   mla_cache_append.  A row whose sequence, position (pos >= 64 x max_blocks) or
+ *   page index (outside [0, num_pages)) is out of range is skipped and recorded as
+ *   MLA_ERR_DEVICE_INDEX.
+ */
+MLA_API mla_status mla_cache_append_paged(const mla_paged_cache* cache, const void* c_kv, const void* k_r,
+                                          const int32_t* seq_idx, const int32_t* pos, int32_t T,
+                                          float rope_base, void* stream);
+
+/*
+ * mla_decode_attn_paged -- mla_decode_attn over a paged cache (same result, bit
+ *   for bit, as mla_decode_attn over a contiguous cache holding the same rows).
+ *   seq_lens [B] int32 device, 0 <= seq_lens[b] <= 64 x max_blocks (clamped and
+ *   recorded as MLA_ERR_DEVICE_INDEX otherwise); the first ceil(seq_lens[b] / 64)
+ *   block-table entries of sequence b must name pages of the pool (an index
+ *   outside [0, num_pages) is recorded as MLA_ERR_DEVICE_INDEX and page 0 is read
+ *   instead).  Rows of the last page past seq_lens[b] may hold anything.
+ *   Workspace as mla_decode_attn (mla_decode_workspace_size(B, ...)).  bf16 pool,
+ *   d_c = 512, d_r in {0, 64}, 1 <= H <= 128; other shapes: MLA_ERR_UNSUPPORTED.
+ */
+MLA_API mla_status mla_decode_attn_paged(const void* q_cat, const mla_paged_cache* cache,
+                                         const int32_t* seq_lens, int32_t H, float scale, void* workspace,
+                                         size_t workspace_bytes, void* o_lat, float* lse, void* stream);
 
 /*
  * mla_decode_attn_noalloc -- mla_decode_attn for callers that cannot allocate.

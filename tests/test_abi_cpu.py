@@ -93,3 +93,37 @@ def test_product_path_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(mla, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         mla.lib()
+
+
+def test_paged_cache_validation(libmla):
+    import head_latent_attention_29_b300 as mla
+    INVALID, UNSUPPORTED = 1, 2
+    assert ctypes.sizeof(mla._PagedCache) == 48
+    assert mla.PAGE_ROWS == 64
+    p = ctypes.c_void_p(0x2000)
+    ok = dict(data=0x1000, dtype=0, num_pages=16, d_c=512, d_r=64, row_stride=576, block_table=0x3000, B=2,
+              max_blocks=8)
+
+    def paged(**kw):
+        f = dict(ok, **kw)
+        return mla._PagedCache(f["data"], f["dtype"], f["num_pages"], f["d_c"], f["d_r"], f["row_stride"],
+                               f["block_table"], f["B"], f["max_blocks"])
+
+    def decode(c, H=128):
+        return libmla.mla_decode_attn_paged(p, ctypes.byref(c), p, H, 0.1, p, 1 << 20, p, None, None)
+
+    assert libmla.mla_decode_attn_paged(p, None, p, 128, 0.1, p, 1 << 20, p, None, None) == INVALID
+    assert decode(paged(block_table=0)) == INVALID          # a paged cache needs its block table
+    assert decode(paged(block_table=0x3002)) == INVALID     # int32 entries: 4-byte aligned
+    assert decode(paged(data=0x1008)) == INVALID            # pool base 16-byte aligned
+    assert decode(paged(num_pages=0)) == INVALID
+    assert decode(paged(max_blocks=0)) == INVALID
+    assert decode(paged(max_blocks=1 << 26)) == INVALID     # 64 x max_blocks must fit int32 positions
+    assert decode(paged(row_stride=570)) == INVALID
+    assert decode(paged(d_r=63)) == INVALID
+    assert decode(paged(d_c=256, row_stride=320)) == UNSUPPORTED
+    assert decode(paged(), H=256) == UNSUPPORTED
+    assert decode(paged(dtype=1, row_stride=576)) == UNSUPPORTED  # fp32 pools have no paged kernel
+    assert libmla.mla_cache_append_paged(ctypes.byref(paged(block_table=0)), p, p, p, p, 1, 10000.0, None) == INVALID
+    assert libmla.mla_cache_append_paged(ctypes.byref(paged()), p, p, p, p, -1, 10000.0, None) == INVALID
+    assert libmla.mla_cache_append_paged(ctypes.byref(paged()), p, p, p, p, 0, 10000.0, None) == 0
