@@ -56,6 +56,18 @@ WORKLOADS: dict[str, dict] = {
         dtype="bf16", rope_base=10000.0, w_std=1.0 / math.sqrt(512.0),
         scale=1.0 / math.sqrt(192.0),
     ),
+    # the new tokens' cache rows straight from their hidden states: c_KV =
+    # RMSNorm(h W_DKV), k_R = RoPE(h W_KR), written at position N - 1 of each of
+    # the 32 decode sequences (DeepSeek-V3 hidden size)
+    "kvdown_b32_d7168": dict(
+        T=32, B=32, N=4096, d_model=7168, d_c=512, d_r=64,
+        dtype="bf16", rope_base=10000.0, eps=1e-6,
+    ),
+    # the same for a 8192-token prompt chunk of 4 sequences (prefill shape)
+    "kvdown_t32768_d7168": dict(
+        T=32768, B=4, prompt=8192, d_model=7168, d_c=512, d_r=64,
+        dtype="bf16", rope_base=10000.0, eps=1e-6,
+    ),
     # gated MLA without RoPE: 64 heads, 131072 cached tokens, full-rank gate
     "gated_h64_b16_n131072": dict(
         B=16, H=64, d_c=512, d_r=0, d_k=128, d_v=128, N=131072, d_model=4096,
@@ -171,3 +183,17 @@ def hidden_model(cfg: dict, seed: int):
     w_uk = normal(seed, "w_uk", (H, d_k, d_c), std=s_c)
     w_uv = normal(seed, "w_uv", (H, d_v, d_c), std=s_c)
     return dict(h=h, w_dkv=w_dkv, w_kr=w_kr, w_uq=w_uq, w_uk=w_uk, w_uv=w_uv)
+
+
+def kv_down_inputs(cfg: dict, seed: int, T: int | None = None):
+    """Hidden states h [T, d_model] ~ N(0,1), W_DKV [d_model, d_c] and W_KR
+    [d_model, d_r] ~ N(0, 1/d_model), and the RMSNorm gain gamma [d_c] ~ 1 + N(0, 0.1^2)
+    (a trained gain is not all ones; a unit gain would hide a dropped gain)."""
+    T = cfg["T"] if T is None else T
+    dm, d_c, d_r = cfg["d_model"], cfg["d_c"], cfg["d_r"]
+    s_in = 1.0 / math.sqrt(dm)
+    h = normal(seed, "kvd_h", (T, dm))
+    w_dkv = normal(seed, "kvd_w_dkv", (dm, d_c), std=s_in)
+    w_kr = normal(seed, "kvd_w_kr", (dm, d_r), std=s_in)
+    gamma = 1.0 + normal(seed, "kvd_gamma", (d_c,), std=0.1)
+    return h, w_dkv, w_kr, gamma.astype(np.float32)

@@ -24,11 +24,17 @@ Everything here is plain float64 numpy, written to be read against the pages:
 * "Gated MLA" (tahou.com) -- section 2.6 / 3.2 (full-rank sigmoid output gate
   multiplied channel-wise into the concatenated v-width output) and section 3.3
   (no positional encoding in the gated variant).
+* The same 0539edu.com article, section 6.3: an RMSNorm placed after the
+  compression projection keeps c_KV's range stable over long contexts (as in
+  DeepSeek-V3), written there as an RMSNorm module of width d_c applied to
+  h W_DKV; and the interview guide's section 6.2 listing, where the RoPE key is
+  its own projection h W_KR of the hidden state.
 
 Readings where the pages are silent (each is listed in the design doc):
 RoPE rotates adjacent pairs (2i, 2i+1) with theta_i = base^(-2i/d_r); the decode
 query sits at position N-1 and attends to all N cached tokens including itself;
-the softmax scale is a runtime argument.
+the softmax scale is a runtime argument; the RMSNorm has a per-channel gain gamma
+(all ones when untrained) and a runtime epsilon inside the square root.
 
 Parity status: every function below is pinned by tests/test_oracle_pins.py
 (closed forms, invariants, brute force on tiny shapes, and the pages' printed
@@ -266,3 +272,25 @@ def project_from_hidden(h: np.ndarray, w_dkv, w_kr, w_uq, H: int, d_k: int, d_r:
     k_r = h @ np.asarray(w_kr, dtype=np.float64)
     q = (h @ np.asarray(w_uq, dtype=np.float64)).reshape(h.shape[0], H, d_k + d_r)
     return c_kv, k_r, q[..., :d_k], q[..., d_k:]
+
+
+# --------------------------------------------------------------------------
+# Cache rows straight from hidden states: normalised latent + rotated key
+# --------------------------------------------------------------------------
+def rms_norm(x: np.ndarray, gamma, eps: float) -> np.ndarray:
+    """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps), scaled channel-wise
+    by gamma (0539edu.com section 6.3: applied to c_KV right after h W_DKV)."""
+    x = np.asarray(x, dtype=np.float64)
+    mean_sq = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(mean_sq + float(eps)) * np.asarray(gamma, dtype=np.float64)
+
+
+def kv_down_rows(h: np.ndarray, w_dkv, w_kr, gamma, eps: float, positions, base: float) -> np.ndarray:
+    """The cache rows new tokens write, computed from their hidden states h [n, d_model]:
+    [RMSNorm(h W_DKV) || RoPE(h W_KR, position)] (0539edu.com sections 2.2 and 6.3
+    for the normalised latent; hotelren.com section 6.2 for the key projection
+    shared by all heads; icman.com.cn section 2 for caching the key rotated)."""
+    h = np.asarray(h, dtype=np.float64)
+    c_kv = rms_norm(h @ np.asarray(w_dkv, dtype=np.float64), gamma, eps)
+    k_r = h @ np.asarray(w_kr, dtype=np.float64)
+    return cache_rows(c_kv, k_r, positions, base)

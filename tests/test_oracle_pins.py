@@ -370,3 +370,75 @@ def test_bf16_rounding_is_nearest_even():
     y = W.bf16_to_f32(W.bf16_bits(x))
     np.testing.assert_array_equal(y[:4], np.array([1.0, 1.0, 1.0 + 2 ** -6, -2.5], dtype=np.float32))
     assert abs(y[4] - 3.0e38) / 3.0e38 < 2 ** -8
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm on the compressed latent and cache rows from hidden states
+# ---------------------------------------------------------------------------
+def test_rms_norm_matches_the_library_routine():
+    # torch's own RMSNorm (CPU, float64) with a non-unit gain: a dropped gain, a
+    # sum in place of the mean or eps outside the square root each fail here
+    import torch
+    x = _rand((7, 48), 31)
+    g = 1.0 + _rand(48, 32, 0.3)
+    for eps in (0.0, 1e-6, 0.5):
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (48,), weight=torch.from_numpy(g), eps=eps).numpy()
+        np.testing.assert_allclose(O.rms_norm(x, g, eps), ref, rtol=1e-13, atol=1e-14)
+
+
+def test_rms_norm_closed_forms():
+    # a constant vector c (any width) has mean square c^2: RMSNorm gives
+    # gamma * c / sqrt(c^2 + eps), so gamma * sign(c) at eps = 0
+    g = np.array([1.0, 2.0, -0.5, 3.0])
+    np.testing.assert_allclose(O.rms_norm(np.full(4, -3.0), g, 0.0), -g, rtol=1e-15)
+    np.testing.assert_allclose(O.rms_norm(np.full(4, 2.0), g, 5.0), g * 2.0 / 3.0, rtol=1e-15)
+    # x = (3, 4): mean square 12.5
+    np.testing.assert_allclose(O.rms_norm(np.array([3.0, 4.0]), np.ones(2), 0.0),
+                               np.array([3.0, 4.0]) / math.sqrt(12.5), rtol=1e-15)
+    # unit gain, eps = 0: the output's mean square is exactly 1 and the map is
+    # invariant to a positive rescale of its input
+    x = _rand((3, 512), 33)
+    y = O.rms_norm(x, np.ones(512), 0.0)
+    np.testing.assert_allclose(np.mean(y * y, axis=-1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(O.rms_norm(17.0 * x, np.ones(512), 0.0), y, rtol=1e-13)
+
+
+def test_kv_down_rows_brute_force():
+    # tiny shapes, every sum written out as a loop, the rotation as a 2 x 2 matrix
+    rng = np.random.default_rng(34)
+    n, dm, d_c, d_r, base, eps = 3, 6, 4, 4, 100.0, 1e-3
+    h = rng.standard_normal((n, dm))
+    w_dkv = rng.standard_normal((dm, d_c))
+    w_kr = rng.standard_normal((dm, d_r))
+    g = 1.0 + 0.2 * rng.standard_normal(d_c)
+    pos = np.array([0, 5, 1234])
+    got = O.kv_down_rows(h, w_dkv, w_kr, g, eps, pos, base)
+    assert got.shape == (n, d_c + d_r)
+    for t in range(n):
+        c = [sum(h[t, i] * w_dkv[i, j] for i in range(dm)) for j in range(d_c)]
+        ms = sum(v * v for v in c) / d_c
+        for j in range(d_c):
+            assert got[t, j] == pytest.approx(c[j] / math.sqrt(ms + eps) * g[j], rel=1e-12)
+        k = [sum(h[t, i] * w_kr[i, j] for i in range(dm)) for j in range(d_r)]
+        for p in range(d_r // 2):
+            ang = pos[t] * base ** (-2.0 * p / d_r)
+            rot = np.array([[math.cos(ang), -math.sin(ang)], [math.sin(ang), math.cos(ang)]])
+            want = rot @ np.array([k[2 * p], k[2 * p + 1]])
+            np.testing.assert_allclose(got[t, d_c + 2 * p:d_c + 2 * p + 2], want, rtol=1e-11, atol=1e-12)
+
+
+def test_kv_down_rows_invariants():
+    # at position 0 the key is the plain projection; at any position every rotated
+    # pair keeps its length; with a unit gain the latent part has unit mean square
+    cfg = W.WORKLOADS["kvdown_b32_d7168"]
+    h, w_dkv, w_kr, _ = W.kv_down_inputs(dict(cfg, d_model=256), seed=3, T=5)
+    rows0 = O.kv_down_rows(h, w_dkv, w_kr, np.ones(512), 0.0, np.zeros(5), 1e4)
+    np.testing.assert_allclose(rows0[:, 512:], h.astype(np.float64) @ w_kr.astype(np.float64), rtol=1e-12)
+    np.testing.assert_allclose(np.mean(rows0[:, :512] ** 2, axis=-1), 1.0, rtol=1e-13)
+    rows = O.kv_down_rows(h, w_dkv, w_kr, np.ones(512), 0.0, np.arange(5) * 1000 + 7, 1e4)
+    pair = lambda r: np.hypot(r[:, 512::2], r[:, 513::2])
+    np.testing.assert_allclose(pair(rows), pair(rows0), rtol=1e-12)
+    assert not np.allclose(rows[:, 512:], rows0[:, 512:])
+    # no positional key (d_r = 0): the row is the normalised latent alone
+    r = O.kv_down_rows(h, w_dkv, np.zeros((256, 0)), np.ones(512), 0.0, np.zeros(5), 1e4)
+    assert r.shape == (5, 512)
