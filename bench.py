@@ -603,6 +603,185 @@ def run_b300_prefill(args, rank, world, device):
     }
 
 
+# ---------------------------------------------------------------- cache rows from hidden states
+def kvdown_rows_slots(cfg):
+    """(sequence, position) of every token a kv_down step writes: the new token at
+    position N - 1 of each decode sequence, or a whole prompt per sequence."""
+    if "prompt" in cfg:
+        B, P = cfg["B"], cfg["prompt"]
+        return np.repeat(np.arange(B, dtype=np.int32), P), np.tile(np.arange(P, dtype=np.int32), B), B, P
+    B, N, T = cfg["B"], cfg["N"], cfg["T"]
+    return np.arange(T, dtype=np.int32) % B, np.full(T, N - 1, dtype=np.int32), B, N
+
+
+def kvdown_bytes_flops(cfg):
+    """Algorithmic bytes (W once, h once, gamma, the rows written) and FLOPs of one step."""
+    T, dm, R, d_c = cfg["T"], cfg["d_model"], cfg["d_c"] + cfg["d_r"], cfg["d_c"]
+    return 2 * (dm * R + T * dm + d_c + T * R), 2 * T * dm * R
+
+
+class KvDownWorkload:
+    """kv_down_append over static buffers, captured in CUDA graphs.  Decode-sized
+    steps rotate through enough weight copies that every step reads W from HBM."""
+
+    def __init__(self, name, seed, device):
+        import torch
+        import head_latent_attention_29_b300 as mla
+        self.mla, self.torch = mla, torch
+        cfg = dict(W.WORKLOADS[name])
+        self.cfg = cfg
+        bf = torch.bfloat16
+        T, dm, d_c, d_r = cfg["T"], cfg["d_model"], cfg["d_c"], cfg["d_r"]
+        self.T = T
+        h, w_dkv, w_kr, gamma = W.kv_down_inputs(cfg, seed)
+        up = lambda x: torch.from_numpy(np.ascontiguousarray(W.bf16_bits(x)).view(np.int16)).view(bf)
+        self.h_host = up(h).pin_memory()
+        self.h = self.h_host.to(device)
+        w = up(np.concatenate([w_dkv, w_kr], axis=1)).to(device)
+        w_bytes = w.numel() * 2
+        self.rotate = max(1, math.ceil(160e6 / w_bytes)) if T * dm * 2 < 126e6 else 1
+        self.ws_list = [w] + [w.clone() for _ in range(self.rotate - 1)]
+        self.gamma = up(gamma).to(device)
+        seq, pos, B, N = kvdown_rows_slots(cfg)
+        self.seq, self.pos = torch.from_numpy(seq).to(device), torch.from_numpy(pos).to(device)
+        seq_l, pos_l = self.seq.long(), self.pos.long()
+        self.cache = mla.LatentCache(B, N, d_c, d_r, dtype=bf, device=device)
+        self.ws = mla.kv_down_workspace(T, dm, d_c, d_r, bf, device)
+        self.eps, self.base = cfg["eps"], cfg["rope_base"]
+        self.rows_host = torch.empty((T, d_c + d_r), dtype=bf).pin_memory()
+        self.kernels_per_step = 2  # projection (tensor cores) + partial sums / norm / RoPE / store
+
+        def call(w):
+            mla.kv_down_append(self.cache, self.h, w, self.gamma, self.seq, self.pos, self.eps, self.base, self.ws)
+
+        for w in self.ws_list:
+            call(w)  # one eager run each: one-time host setup happens outside capture
+        torch.cuda.synchronize(device)
+        self.graphs, self.e2e = [], []
+        for w in self.ws_list:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                call(w)
+            self.graphs.append(g)
+        # end to end: h in from pinned memory, the written rows back to pinned memory
+        self.rows_dev = torch.empty((T, d_c + d_r), dtype=bf, device=device)
+        for w in self.ws_list[:1]:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.h.copy_(self.h_host, non_blocking=True)
+                call(w)
+                self.rows_dev.copy_(self.cache.data[seq_l, pos_l, : d_c + d_r])
+                self.rows_host.copy_(self.rows_dev, non_blocking=True)
+            self.e2e.append(g)
+
+    def step(self, i):
+        self.graphs[i % self.rotate].replay()
+
+
+def run_b300_kvdown(args, rank, world, device):
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(device)
+    wl = KvDownWorkload(args.workload, args.seed + rank, device)
+    cfg = wl.cfg
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for i in range(args.warmup):
+        wl.step(i)
+    torch.cuda.synchronize(device)
+    steps = args.steps if wl.T <= 4096 else max(3, min(args.steps, 200))
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            wl.step(i)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier()
+    ms_step = max_over_ranks(e0.elapsed_time(e1), world, device) / steps
+    value = job_throughput(wl.T, world, ms_step * 1e-3)
+
+    n_e2e = max(20, min(steps // 10, 2000)) if wl.T <= 4096 else 5
+    wl.e2e[0].replay()
+    torch.cuda.synchronize(device)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        wl.e2e[0].replay()
+        stream.synchronize()
+    barrier()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world, device)
+
+    hbm, tc_burst, tc_sust, peak_kind = _peaks()
+    bytes_alg, flops = kvdown_bytes_flops(cfg)
+    t_mem, t_tc = bytes_alg / (hbm * 1e9), flops / (tc_burst * 1e12)
+    us = ms_step * 1e3
+    tensor = t_tc > t_mem
+    achieved = flops / (us * 1e-6) / 1e12 if tensor else bytes_alg / (us * 1e-6) / 1e9
+    peak = tc_burst if tensor else hbm
+    R = cfg["d_c"] + cfg["d_r"]
+    return {
+        "metric": f"MLA cache rows from hidden states tokens/s (RMSNorm(h W_DKV) || RoPE(h W_KR), append) at "
+                  f"T={wl.T},d_model={cfg['d_model']},d_c={cfg['d_c']},d_r={cfg['d_r']} bf16; % of roofline",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) hidden states, N(0,1/d_model) projections, gain 1+N(0,0.01))",
+        "config": {"workload": args.workload, "T": wl.T, "d_model": cfg["d_model"], "d_c": cfg["d_c"],
+                   "d_r": cfg["d_r"], "parallelism": f"replicas x{world}",
+                   "l2": (f"{wl.rotate} rotating weight copies ({wl.rotate * cfg['d_model'] * R * 2 / 1e6:.0f} MB "
+                          "vs 126 MB L2)" if wl.rotate > 1 else "inputs larger than L2"),
+                   "step": "kv_down_append (projection on the tensor cores + norm/RoPE/store)"},
+        "gpu_launches": wl.kernels_per_step * steps,
+        "e2e": {"value": round(wl.T * world / e2e_s, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": wl.h_host.numel() * 2, "d2h_bytes_per_step": wl.rows_host.numel() * 2},
+        "roofline": {
+            "bound": "tensor" if tensor else "hbm", "kernel": "kv_down_append (projection + finish)",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s" if tensor else "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "peak_source": f"{peak_kind} " + ("bf16_tflops (burst)" if tensor else "hbm_gbs"),
+            "step_us": round(us, 3), "algorithmic_bytes": bytes_alg, "algorithmic_flops": flops,
+            "roofline_us": round(max(t_mem, t_tc) * 1e6, 3),
+        },
+        "clocks": clk.summary(),
+    }
+
+
+def cpu_baseline_kvdown(workload: str, seed: int, budget_s: float = 12.0):
+    """Time the float64 oracle's rows-from-hidden-states step on the host cores for
+    a bounded sample of the workload's tokens (weights widened once: resident state)."""
+    from oracle import mla_oracle as O
+    cfg = dict(W.WORKLOADS[workload])
+    d_c = cfg["d_c"]
+    n = min(cfg["T"], 32)
+    h, w_dkv, w_kr, gamma = W.kv_down_inputs(dict(cfg, T=n), seed)
+    wd = lambda x: W.widen(W.as_dtype(x, "bf16"), "bf16")
+    h, w, g = wd(h), wd(np.concatenate([w_dkv, w_kr], axis=1)), wd(gamma)
+    _, pos, _, _ = kvdown_rows_slots(cfg)
+    pos = pos[:n]
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        O.kv_down_rows(h, w[:, :d_c], w[:, d_c:], g, cfg["eps"], pos, cfg["rope_base"])
+        done += n
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    try:
+        from threadpoolctl import threadpool_info
+        threads = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+    except Exception:  # pragma: no cover
+        threads = []
+    return {"value": round(done / el, 3), "unit": "tokens/s", "cores": max(threads) if threads else 1,
+            "kind": "oracle", "host_cpus": os.cpu_count(),
+            "sample": f"{done} tokens in batches of {n} (float64 numpy), {el:.1f} s"}
+
+
 _PREFILL_ORACLE_STATE = {}
 
 
@@ -716,7 +895,8 @@ def run_reference(args, rank, world):
         return None
     cfg = W.WORKLOADS[args.workload]
     prefill = "S" in cfg
-    fn = cpu_baseline_prefill if prefill else cpu_baseline
+    kvdown = "T" in cfg
+    fn = cpu_baseline_kvdown if kvdown else (cpu_baseline_prefill if prefill else cpu_baseline)
     steps = []
     for _ in range(max(1, args.warmup)):
         fn(args.workload, args.seed, budget_s=0.5)
@@ -727,17 +907,22 @@ def run_reference(args, rank, world):
     v = statistics.median(vals)
     cb = dict(steps[-1])
     cb["value"] = round(v, 3)
-    metric = (f"MLA causal prefill prompt tokens/s at H={cfg['H']},d_c={cfg['d_c']},B={cfg['B']},S={cfg['S']} bf16; "
-              "% of roofline" if prefill
-              else "MLA decode tokens/s at H=128,d_c=512,B=32,N=4K bf16; % of roofline")
-    tokens_per_step = cfg["B"] * cfg.get("S", 1)
+    if kvdown:
+        metric = (f"MLA cache rows from hidden states tokens/s (RMSNorm(h W_DKV) || RoPE(h W_KR), append) at "
+                  f"T={cfg['T']},d_model={cfg['d_model']},d_c={cfg['d_c']},d_r={cfg['d_r']} bf16; % of roofline")
+    elif prefill:
+        metric = (f"MLA causal prefill prompt tokens/s at H={cfg['H']},d_c={cfg['d_c']},B={cfg['B']},S={cfg['S']} bf16; "
+                  "% of roofline")
+    else:
+        metric = decode_metric(args.workload, cfg)
+    tokens_per_step = cfg["T"] if kvdown else cfg["B"] * cfg.get("S", 1)
     return {
         "impl": "reference",
         "metric": metric,
         "value": round(v, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * tokens_per_step / v, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "B": cfg["B"], "H": cfg["H"], "d_c": cfg["d_c"], "d_r": cfg["d_r"],
+        "config": {"workload": args.workload, "B": cfg["B"], "H": cfg.get("H"), "d_c": cfg["d_c"], "d_r": cfg["d_r"],
                    "parallelism": "host cores (oracle)"},
         "cpu_baseline": cb,
         "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -760,7 +945,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.paged and "S" in W.WORKLOADS[args.workload]:
+    if args.paged and ("S" in W.WORKLOADS[args.workload] or "T" in W.WORKLOADS[args.workload]):
         ap.error("--paged applies to decode workloads")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -780,7 +965,11 @@ def main():
         torch.cuda.set_device(device)
         dist.init_process_group("nccl", device_id=device)
     try:
-        if "S" in W.WORKLOADS[args.workload]:
+        if "T" in W.WORKLOADS[args.workload]:
+            out = run_b300_kvdown(args, rank, world, device)
+            if rank == 0 and not args.no_cpu_baseline:
+                out["cpu_baseline"] = cpu_baseline_kvdown(args.workload, args.seed, budget_s=args.cpu_seconds)
+        elif "S" in W.WORKLOADS[args.workload]:
             out = run_b300_prefill(args, rank, world, device)
             if rank == 0 and not args.no_cpu_baseline:
                 out["cpu_baseline"] = cpu_baseline_prefill(args.workload, args.seed, budget_s=args.cpu_seconds)

@@ -26,6 +26,7 @@ __all__ = [
     "MlaError", "LatentCache", "lib", "cache_append", "absorb_q", "decode_workspace",
     "decode_attn", "decode_attn_noalloc", "out_up", "gate", "get_device_error", "debug_inject_fault", "LIB_PATH",
     "PagedLatentCache", "cache_append_paged", "decode_attn_paged", "PAGE_ROWS",
+    "kv_down_workspace", "kv_down_append",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -91,6 +92,16 @@ _SIGS = {
     "mla_decode_attn_paged": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(_PagedCache), ctypes.c_void_p,
                                              ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t,
                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "mla_kv_down_workspace_size": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                     ctypes.c_int32, ctypes.c_int32]),
+    "mla_kv_down_append": (ctypes.c_int, [ctypes.POINTER(_Cache), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                          ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t,
+                                          ctypes.c_void_p]),
+    "mla_kv_down_append_paged": (ctypes.c_int, [ctypes.POINTER(_PagedCache), ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p,
+                                                ctypes.c_size_t, ctypes.c_void_p]),
     "mla_decode_attn_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(_Cache), ctypes.c_void_p,
                                                ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p]),
@@ -380,3 +391,36 @@ def decode_attn_paged(q_cat: torch.Tensor, cache: PagedLatentCache, seq_lens: to
                                        _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse), _stream(q_cat)),
            "mla_decode_attn_paged")
     return out, lse
+
+
+def kv_down_workspace(T: int, d_model: int, d_c: int, d_r: int, dtype=torch.bfloat16,
+                      device="cuda") -> torch.Tensor:
+    """Device scratch for kv_down_append of T tokens."""
+    n = lib().mla_kv_down_workspace_size(T, d_model, d_c, d_r, _DT[dtype])
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def kv_down_append(cache, h: torch.Tensor, w_dkvr: torch.Tensor, gamma: torch.Tensor, seq_idx: torch.Tensor,
+                   pos: torch.Tensor, eps: float = 1e-6, rope_base: float = 10000.0,
+                   workspace: torch.Tensor | None = None) -> None:
+    """Write the rows of T new tokens from their hidden states h [T, d_model]:
+    cache[seq_idx[i], pos[i]] = [RMSNorm(h[i] W_DKV) * gamma || RoPE(h[i] W_KR, pos[i])],
+    with w_dkvr = [W_DKV | W_KR] of shape [d_model, d_c + d_r] (LatentCache or
+    PagedLatentCache)."""
+    _dev_tensor(h, "h", cache.dtype)
+    _dev_tensor(w_dkvr, "w_dkvr", cache.dtype)
+    _dev_tensor(gamma, "gamma", cache.dtype)
+    _dev_tensor(seq_idx, "seq_idx", torch.int32)
+    _dev_tensor(pos, "pos", torch.int32)
+    T, d_model = h.shape
+    if tuple(w_dkvr.shape) != (d_model, cache.d_c + cache.d_r) or tuple(gamma.shape) != (cache.d_c,):
+        raise ValueError("w_dkvr must be [d_model, d_c + d_r] and gamma [d_c]")
+    if seq_idx.numel() != T or pos.numel() != T:
+        raise ValueError("seq_idx and pos need one entry per token")
+    if workspace is None:
+        workspace = kv_down_workspace(T, d_model, cache.d_c, cache.d_r, cache.dtype, h.device)
+    st = cache.struct()
+    fn, name = ((lib().mla_kv_down_append_paged, "mla_kv_down_append_paged") if isinstance(cache, PagedLatentCache)
+                else (lib().mla_kv_down_append, "mla_kv_down_append"))
+    _check(fn(ctypes.byref(st), _ptr(h), _ptr(w_dkvr), _ptr(gamma), float(eps), _ptr(seq_idx), _ptr(pos), T,
+              d_model, float(rope_base), _ptr(workspace), workspace.numel(), _stream(h)), name)

@@ -3,5 +3,6 @@
 #include "k_simt.cu"
 #include "k_decode_tc.cu"
 #include "k_headgemm.cu"
+#include "k_kvdown.cu"
 #include "mla_api.cu"
 #include "mla_noalloc.cu"

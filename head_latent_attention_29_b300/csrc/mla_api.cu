@@ -46,6 +46,23 @@ mla_status check_paged(const mla_paged_cache* p, mla_cache* view) {
   return MLA_OK;
 }
 
+// Shared checks and dispatch of the two kv_down entry points (view = the cache as
+// the launchers take it; block_table etc. set for a paged pool).
+mla_status kv_down(const mla_cache& view, const void* h, const void* w, const void* gamma, float eps,
+                   const int32_t* seq_idx, const int32_t* pos, int32_t T, int32_t d_model, float rope_base,
+                   void* ws, size_t ws_bytes, void* stream, const int32_t* block_table = nullptr,
+                   int32_t max_blocks = 0, int32_t num_pages = 0) {
+  if (T < 0 || d_model <= 0) return MLA_ERR_INVALID_ARG;
+  if (T == 0) return MLA_OK;
+  if (h == nullptr || w == nullptr || gamma == nullptr || seq_idx == nullptr || pos == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || !(eps < INFINITY)) return MLA_ERR_INVALID_ARG;  // also rejects NaN
+  if (!(rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (view.d_r > 128 || (view.d_c & 1) != 0 || view.d_c + view.d_r > 1024) return MLA_ERR_UNSUPPORTED;
+  return mla::launch_kv_down(view, h, w, gamma, eps, seq_idx, pos, T, d_model, rope_base, ws, ws_bytes,
+                             as_stream(stream), block_table, max_blocks, num_pages);
+}
+
 }  // namespace
 
 extern "C" {
@@ -202,6 +219,32 @@ MLA_API mla_status mla_decode_attn_paged(const void* q_cat, const mla_paged_cach
     return MLA_ERR_UNSUPPORTED;
   return mla::launch_decode_tc(q_cat, view, seq_lens, H, scale, workspace, workspace_bytes, o_lat, lse,
                                as_stream(stream), cache->block_table, cache->max_blocks, cache->num_pages);
+}
+
+MLA_API size_t mla_kv_down_workspace_size(int32_t T, int32_t d_model, int32_t d_c, int32_t d_r, int32_t dtype) {
+  if (!valid_dtype(dtype)) return 0;
+  return mla::kv_down_workspace_size(T, d_model, d_c, d_r, dtype);
+}
+
+MLA_API mla_status mla_kv_down_append(const mla_cache* cache, const void* h, const void* w_dkvr, const void* gamma,
+                                      float eps, const int32_t* seq_idx, const int32_t* pos, int32_t T,
+                                      int32_t d_model, float rope_base, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  const mla_status st = check_cache(cache);
+  if (st != MLA_OK) return st;
+  return kv_down(*cache, h, w_dkvr, gamma, eps, seq_idx, pos, T, d_model, rope_base, workspace, workspace_bytes,
+                 stream);
+}
+
+MLA_API mla_status mla_kv_down_append_paged(const mla_paged_cache* cache, const void* h, const void* w_dkvr,
+                                            const void* gamma, float eps, const int32_t* seq_idx,
+                                            const int32_t* pos, int32_t T, int32_t d_model, float rope_base,
+                                            void* workspace, size_t workspace_bytes, void* stream) {
+  mla_cache view;
+  const mla_status st = check_paged(cache, &view);
+  if (st != MLA_OK) return st;
+  return kv_down(view, h, w_dkvr, gamma, eps, seq_idx, pos, T, d_model, rope_base, workspace, workspace_bytes,
+                 stream, cache->block_table, cache->max_blocks, cache->num_pages);
 }
 
 MLA_API mla_status mla_debug_inject_fault(int32_t kind) {

@@ -143,6 +143,14 @@ mla_status launch_decode_f32(const float* q_cat, const mla_cache& c, const int32
 mla_status launch_prefill_f32(const float* q_cat, const mla_cache& c, const int32_t* q_start, int32_t S,
                               int32_t causal, int32_t H, float scale, float* o_lat, float* lse, cudaStream_t s);
 
+// cache rows from hidden states (projection, RMSNorm, RoPE, append); block_table as
+// launch_cache_append
+size_t kv_down_workspace_size(int32_t T, int32_t d_model, int32_t d_c, int32_t d_r, int32_t dtype);
+mla_status launch_kv_down(const mla_cache& c, const void* h, const void* w, const void* gamma, float eps,
+                          const int32_t* seq_idx, const int32_t* pos, int32_t T, int32_t d_model, float rope_base,
+                          void* ws, size_t ws_bytes, cudaStream_t s, const int32_t* block_table = nullptr,
+                          int32_t max_blocks = 0, int32_t num_pages = 0);
+
 // tensor-core decode and prefill (bf16): sizes and launch
 void set_fault_injection(int32_t kind);
 size_t decode_tc_workspace_size(int32_t B);

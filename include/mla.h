@@ -111,8 +111,8 @@ MLA_API const char* mla_status_string(mla_status status);
 /*
  * mla_cache_append -- write T new tokens into the latent cache.
  *   For each i < T: cache[seq_idx[i]][pos[i]] = [c_kv[i] || RoPE(k_r[i], pos[i])].
- *   RoPE rotates pairs (2j, 2j+1) of k_r by angle pos * base^(-2j/d_r); the angle
- *   is formed in double precision.  (Decoupled RoPE key: icman.com.cn section 2;
+ *   RoPE rotates pairs (2j, 2j+1) of k_r by angle pos * base^(-2j/d_r) (the
+ *   frequencies are formed in double precision, the angle to about 1e-6 rad).  (Decoupled RoPE key: icman.com.cn section 2;
  *   hotelren.com section 6.2; append-by-position: 0539edu.com section 5.2.)
  *   c_kv     [T, d_c]   dtype = cache->dtype
  *   k_r      [T, d_r]   dtype = cache->dtype; may be NULL iff d_r == 0
@@ -259,6 +259,52 @@ MLA_API mla_status mla_cache_append_paged(const mla_paged_cache* cache, const vo
 MLA_API mla_status mla_decode_attn_paged(const void* q_cat, const mla_paged_cache* cache,
                                          const int32_t* seq_lens, int32_t H, float scale, void* workspace,
                                          size_t workspace_bytes, void* o_lat, float* lse, void* stream);
+
+/*
+ * mla_kv_down_workspace_size -- bytes of device workspace mla_kv_down_append needs
+ * for T tokens (fp32 partial sums of the projection).  0 if T <= 0 or the sizes
+ * are not positive.
+ */
+MLA_API size_t mla_kv_down_workspace_size(int32_t T, int32_t d_model, int32_t d_c, int32_t d_r,
+                                          int32_t dtype);
+
+/*
+ * mla_kv_down_append -- the new tokens' cache rows straight from their hidden
+ *   states, in place of computing c_kv / k_r separately and calling
+ *   mla_cache_append:
+ *     x        = h[i] W_DKV                          (0539edu.com section 2.2)
+ *     c_KV     = x / sqrt(mean_j x_j^2 + eps) * gamma (RMSNorm after the
+ *                                                     compression: section 6.3)
+ *     k_R      = RoPE(h[i] W_KR, pos[i])             (hotelren.com section 6.2)
+ *     cache[seq_idx[i]][pos[i]] = [c_KV || k_R]      (as mla_cache_append)
+ *   The projection accumulates in fp32 (bf16 operands on the tensor cores for bf16
+ *   caches), the norm and the rotation are fp32, the row is stored in the cache
+ *   dtype.  Deterministic: the same inputs give the same bits.
+ *   h        [T, d_model]         cache dtype, device
+ *   w_dkvr   [d_model, d_c + d_r] cache dtype, device: W_DKV in columns [0, d_c),
+ *                                 W_KR in columns [d_c, d_c + d_r)
+ *   gamma    [d_c]                cache dtype, device: the RMSNorm gain
+ *   eps      >= 0, added to the mean square
+ *   seq_idx, pos [T] int32 device: as mla_cache_append (bad rows skipped and
+ *            recorded as MLA_ERR_DEVICE_INDEX)
+ *   workspace device scratch of mla_kv_down_workspace_size(T, d_model, d_c, d_r,
+ *            dtype) bytes, 16-byte aligned (MLA_ERR_WORKSPACE otherwise).
+ *   Limits: d_c even, d_c + d_r <= 1024 (MLA_ERR_UNSUPPORTED otherwise).  bf16
+ *   caches with d_model % 64 == 0, (d_c + d_r) % 8 == 0 and 16-byte aligned h and
+ *   w_dkvr take the tensor-core projection; other shapes and fp32 take a CUDA-core
+ *   one.  gamma is always applied: pass ones for an RMSNorm without gain.
+ */
+MLA_API mla_status mla_kv_down_append(const mla_cache* cache, const void* h, const void* w_dkvr,
+                                      const void* gamma, float eps, const int32_t* seq_idx,
+                                      const int32_t* pos, int32_t T, int32_t d_model, float rope_base,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* mla_kv_down_append into a paged cache (rows placed as mla_cache_append_paged). */
+MLA_API mla_status mla_kv_down_append_paged(const mla_paged_cache* cache, const void* h,
+                                            const void* w_dkvr, const void* gamma, float eps,
+                                            const int32_t* seq_idx, const int32_t* pos, int32_t T,
+                                            int32_t d_model, float rope_base, void* workspace,
+                                            size_t workspace_bytes, void* stream);
 
 /*
  * mla_decode_attn_noalloc -- mla_decode_attn for callers that cannot allocate.

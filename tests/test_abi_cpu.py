@@ -127,3 +127,36 @@ def test_paged_cache_validation(libmla):
     assert libmla.mla_cache_append_paged(ctypes.byref(paged(block_table=0)), p, p, p, p, 1, 10000.0, None) == INVALID
     assert libmla.mla_cache_append_paged(ctypes.byref(paged()), p, p, p, p, -1, 10000.0, None) == INVALID
     assert libmla.mla_cache_append_paged(ctypes.byref(paged()), p, p, p, p, 0, 10000.0, None) == 0
+
+
+def test_kv_down_validation_and_workspace(libmla):
+    import head_latent_attention_29_b300 as mla
+    INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 5
+    ws = libmla.mla_kv_down_workspace_size
+    # decode batch: 5 column tiles x 30 K ranges of fp32 partials
+    assert ws(32, 7168, 512, 64, 0) == 30 * 32 * 576 * 4
+    assert ws(32768, 7168, 512, 64, 0) == 32768 * 576 * 4   # 640 tiles: no K split
+    assert ws(40, 64, 32, 8, 1) == 40 * 40 * 4               # fp32: CUDA-core path, one range
+    assert ws(0, 7168, 512, 64, 0) == 0
+    p = ctypes.c_void_p(0x2000)
+    c = mla._Cache(0x1000, 0, 4, 300, 512, 64, 0, 576)
+
+    def call(cache=c, T=4, eps=1e-6, d_model=1024, wsb=1 << 20, ws_ptr=p, base=1e4):
+        return libmla.mla_kv_down_append(ctypes.byref(cache) if cache is not None else None, p, p, p, eps, p, p, T,
+                                         d_model, base, ws_ptr, wsb, None)
+
+    assert call(cache=None) == INVALID
+    assert call(T=-1) == INVALID
+    assert call(T=0) == 0
+    assert call(eps=float("nan")) == INVALID
+    assert call(eps=-1.0) == INVALID
+    assert call(d_model=0) == INVALID
+    assert call(base=0.0) == INVALID
+    assert call(wsb=16) == WORKSPACE                        # far below the partials' size
+    assert call(ws_ptr=ctypes.c_void_p(0x2008)) == WORKSPACE  # 16-byte aligned scratch
+    assert call(cache=mla._Cache(0x1000, 0, 4, 300, 511, 65, 0, 576)) == INVALID  # odd d_r
+    assert call(cache=mla._Cache(0x1000, 0, 4, 300, 511, 64, 0, 576)) == UNSUPPORTED  # odd d_c
+    assert call(cache=mla._Cache(0x1000, 1, 4, 300, 1024, 64, 0, 1088)) == UNSUPPORTED  # row over 1024
+    pc = mla._PagedCache(0x1000, 0, 16, 512, 64, 576, 0, 2, 8)  # paged without a block table
+    assert libmla.mla_kv_down_append_paged(ctypes.byref(pc), p, p, p, 1e-6, p, p, 4, 1024, 1e4, p, 1 << 20,
+                                           None) == INVALID
