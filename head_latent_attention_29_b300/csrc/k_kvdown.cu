@@ -237,26 +237,39 @@ __global__ void __launch_bounds__(kThreads) kvd_simt_kernel(const T* __restrict_
 
 // ---------------------------------------------------------------------------
 // (2) one block per token: partial sums -> RMSNorm on the latent, RoPE on the key,
-// the row into the (contiguous or paged) cache.  Thread t holds column pairs
-// (2q, 2q+1) for q = t, t + 128, ...: the latent pairs feed the mean square, the
-// key pairs are exactly RoPE's rotation pairs.
+// the row into the (contiguous or paged) cache.  Column pairs (2q, 2q+1) are held
+// by thread t = q % 128 of each of four groups; group g sums the K ranges g, g + 4,
+// g + 8, ... in that order, eight independent loads at a time (the partials sit in
+// L2, so a chain of dependent loads would cost an L2 round trip per range), and
+// group 0 adds the four group sums in group order.  The summation order is fixed,
+// so the result is deterministic.  The latent pairs feed the mean square; the key
+// pairs are exactly RoPE's rotation pairs.
 // ---------------------------------------------------------------------------
+constexpr int kFinishGroups = 4;
+constexpr int kFinishThreads = kThreads * kFinishGroups;
+constexpr int kSplitBatch = 8;
+
 template <typename T>
-__global__ void __launch_bounds__(kThreads) kvd_finish_kernel(const float* __restrict__ ws, int32_t splits,
-                                                              int32_t n_tok, int32_t d_c, int32_t d_r,
-                                                              const T* __restrict__ gamma, float eps,
-                                                              T* __restrict__ cache, int32_t B, int32_t N_max,
-                                                              int64_t row_stride, const int32_t* __restrict__ seq_idx,
-                                                              const int32_t* __restrict__ pos,
-                                                              const __grid_constant__ RopeTable rope, PageMap pages) {
+__global__ void __launch_bounds__(kFinishThreads) kvd_finish_kernel(const float* __restrict__ ws, int32_t splits,
+                                                                    int32_t n_tok, int32_t d_c, int32_t d_r,
+                                                                    const T* __restrict__ gamma, float eps,
+                                                                    T* __restrict__ cache, int32_t B, int32_t N_max,
+                                                                    int64_t row_stride,
+                                                                    const int32_t* __restrict__ seq_idx,
+                                                                    const int32_t* __restrict__ pos,
+                                                                    const __grid_constant__ RopeTable rope,
+                                                                    PageMap pages) {
   __shared__ float s_hi[64], s_lo[64];
+  __shared__ float2 s_part[kFinishGroups - 1][kMaxR / 2];
   __shared__ float s_red[kThreads / 32];
   griddep_launch();
   rope_table_to_smem(rope, d_r / 2, s_hi, s_lo);
   griddep_wait();  // the partials come from the previous kernel
   const int R = d_c + d_r;
   const int pairs = R / 2;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = threadIdx.x / kThreads, t = threadIdx.x % kThreads;
+  const int lane = t & 31, warp = t >> 5;
+  const size_t split_stride = static_cast<size_t>(n_tok) * R;
   for (int i = blockIdx.x; i < n_tok; i += gridDim.x) {
     const int32_t b = seq_idx[i];
     const int32_t p = pos[i];
@@ -273,47 +286,83 @@ __global__ void __launch_bounds__(kThreads) kvd_finish_kernel(const float* __res
       }
       row = static_cast<int64_t>(pg) * kPageRows + p % kPageRows;
     }
+    const float* src = ws + static_cast<size_t>(i) * R;
     float2 v[kPairsPerThread];
-    float ss = 0.f;
 #pragma unroll
-    for (int u = 0; u < kPairsPerThread; ++u) {
-      const int q = threadIdx.x + u * kThreads;
-      v[u] = make_float2(0.f, 0.f);
-      if (q < pairs) {
-        const float* src = ws + static_cast<size_t>(i) * R + 2 * q;
-        for (int s = 0; s < splits; ++s) {
-          const float2 x = *reinterpret_cast<const float2*>(src + static_cast<size_t>(s) * n_tok * R);
-          v[u].x += x.x;
-          v[u].y += x.y;
+    for (int u = 0; u < kPairsPerThread; ++u) v[u] = make_float2(0.f, 0.f);
+    for (int s0 = g; s0 < splits; s0 += kFinishGroups * kSplitBatch) {
+      float2 x[kPairsPerThread][kSplitBatch];
+#pragma unroll
+      for (int u = 0; u < kPairsPerThread; ++u) {
+        const int q = t + u * kThreads;
+#pragma unroll
+        for (int k = 0; k < kSplitBatch; ++k) {
+          const int sp = s0 + k * kFinishGroups;
+          x[u][k] = (q < pairs && sp < splits)
+                        ? *reinterpret_cast<const float2*>(src + sp * split_stride + 2 * q)
+                        : make_float2(0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kPairsPerThread; ++u) {
+#pragma unroll
+        for (int k = 0; k < kSplitBatch; ++k) {
+          if (s0 + k * kFinishGroups < splits) {
+            v[u].x += x[u][k].x;
+            v[u].y += x[u][k].y;
+          }
+        }
+      }
+    }
+    if (g > 0) {
+#pragma unroll
+      for (int u = 0; u < kPairsPerThread; ++u) {
+        const int q = t + u * kThreads;
+        if (q < pairs) s_part[g - 1][q] = v[u];
+      }
+    }
+    __syncthreads();
+    if (g == 0) {
+      float ss = 0.f;
+#pragma unroll
+      for (int u = 0; u < kPairsPerThread; ++u) {
+        const int q = t + u * kThreads;
+        if (q >= pairs) continue;
+#pragma unroll
+        for (int gg = 0; gg < kFinishGroups - 1; ++gg) {
+          v[u].x += s_part[gg][q].x;
+          v[u].y += s_part[gg][q].y;
         }
         if (2 * q < d_c) ss = fmaf(v[u].x, v[u].x, fmaf(v[u].y, v[u].y, ss));
       }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) s_red[warp] = ss;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) s_red[warp] = ss;
     __syncthreads();
-    float tot = 0.f;
+    if (g == 0) {
+      float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) tot += s_red[w];
-    __syncthreads();  // s_red is rewritten by the next token
-    const float r = rsqrtf(tot / static_cast<float>(d_c) + eps);
-    T* dst = cache + row * row_stride;
+      for (int w = 0; w < kThreads / 32; ++w) tot += s_red[w];
+      const float r = rsqrtf(tot / static_cast<float>(d_c) + eps);
+      T* dst = cache + row * row_stride;
 #pragma unroll
-    for (int u = 0; u < kPairsPerThread; ++u) {
-      const int q = threadIdx.x + u * kThreads;
-      if (q >= pairs) continue;
-      if (2 * q < d_c) {
-        st_elem(dst + 2 * q, v[u].x * r * ld_elem(gamma + 2 * q));
-        st_elem(dst + 2 * q + 1, v[u].y * r * ld_elem(gamma + 2 * q + 1));
-      } else {
-        const int j = q - d_c / 2;
-        float sn, cs;
-        rope_sincos(p, s_hi[j], s_lo[j], &sn, &cs);
-        st_elem(dst + 2 * q, fmaf(v[u].x, cs, -v[u].y * sn));
-        st_elem(dst + 2 * q + 1, fmaf(v[u].x, sn, v[u].y * cs));
+      for (int u = 0; u < kPairsPerThread; ++u) {
+        const int q = t + u * kThreads;
+        if (q >= pairs) continue;
+        if (2 * q < d_c) {
+          st_elem(dst + 2 * q, v[u].x * r * ld_elem(gamma + 2 * q));
+          st_elem(dst + 2 * q + 1, v[u].y * r * ld_elem(gamma + 2 * q + 1));
+        } else {
+          const int j = q - d_c / 2;
+          float sn, cs;
+          rope_sincos(p, s_hi[j], s_lo[j], &sn, &cs);
+          st_elem(dst + 2 * q, fmaf(v[u].x, cs, -v[u].y * sn));
+          st_elem(dst + 2 * q + 1, fmaf(v[u].x, sn, v[u].y * cs));
+        }
       }
     }
+    __syncthreads();  // s_part and s_red are rewritten for the next token
   }
 }
 
@@ -375,11 +424,11 @@ mla_status launch_kv_down(const mla_cache& c, const void* h, const void* w, cons
   const int grid = T < 148 * 16 ? T : 148 * 16;
   cudaError_t e;
   if (c.dtype == MLA_BF16)
-    e = launch_pdl(kvd_finish_kernel<__nv_bfloat16>, dim3(grid), dim3(kThreads), 0, s, wsf, p.splits, T, c.d_c,
+    e = launch_pdl(kvd_finish_kernel<__nv_bfloat16>, dim3(grid), dim3(kFinishThreads), 0, s, wsf, p.splits, T, c.d_c,
                    c.d_r, static_cast<const __nv_bfloat16*>(gamma), eps, static_cast<__nv_bfloat16*>(c.data), c.B,
                    c.N_max, static_cast<int64_t>(c.row_stride), seq_idx, pos, rope_table(c.d_r, rope_base), pages);
   else
-    e = launch_pdl(kvd_finish_kernel<float>, dim3(grid), dim3(kThreads), 0, s, wsf, p.splits, T, c.d_c, c.d_r,
+    e = launch_pdl(kvd_finish_kernel<float>, dim3(grid), dim3(kFinishThreads), 0, s, wsf, p.splits, T, c.d_c, c.d_r,
                    static_cast<const float*>(gamma), eps, static_cast<float*>(c.data), c.B, c.N_max,
                    static_cast<int64_t>(c.row_stride), seq_idx, pos, rope_table(c.d_r, rope_base), pages);
   return cuda_status(e);
