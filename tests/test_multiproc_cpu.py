@@ -111,3 +111,35 @@ def test_stored_traffic_follows_kernel_code_not_comments(tmp_path, monkeypatch):
     assert bench._kernel_hash() == h0
     (d / "k_decode_tc.cu").write_text(text.replace("constexpr int kBN = 64;", "constexpr int kBN = 32;"))
     assert bench._kernel_hash() != h0
+
+
+def test_paged_block_table_is_a_permutation_of_the_needed_pages():
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    lens = np.array([4096, 1, 64, 65, 0, 130])
+    table, num_pages = bench.paged_block_table(lens, seed=3)
+    need = [-(-int(n) // 64) for n in lens]
+    assert num_pages == sum(need) and table.shape == (len(lens), max(need))
+    used = np.concatenate([table[b, :k] for b, k in enumerate(need)])
+    assert sorted(used.tolist()) == list(range(num_pages))   # every page once, no sharing
+    assert not np.array_equal(used, np.arange(num_pages))    # shuffled, not the contiguous order
+    t2, _ = bench.paged_block_table(lens, seed=3)
+    assert np.array_equal(table, t2)                          # seeded
+
+
+def test_kv_down_bench_accounting():
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    import mla_workloads as W
+    cfg = W.WORKLOADS["kvdown_b32_d7168"]
+    seq, pos, B, N = bench.kvdown_rows_slots(cfg)
+    assert (B, N) == (32, 4096) and np.array_equal(seq, np.arange(32)) and np.all(pos == 4095)
+    nbytes, flops = bench.kvdown_bytes_flops(cfg)
+    # W once (7168 x 576 bf16) + h (32 x 7168) + gamma (512) + 32 rows of 576
+    assert nbytes == 2 * (7168 * 576 + 32 * 7168 + 512 + 32 * 576)
+    assert flops == 2 * 32 * 7168 * 576
+    cfg = W.WORKLOADS["kvdown_t32768_d7168"]
+    seq, pos, B, N = bench.kvdown_rows_slots(cfg)
+    assert len(seq) == cfg["T"] == B * N and len(set(zip(seq.tolist(), pos.tolist()))) == cfg["T"]
