@@ -260,6 +260,37 @@ def prefill_absorbed_rows(q_cat: np.ndarray, rows: np.ndarray, d_c: int, scale: 
     return np.stack(outs), np.stack(lses)
 
 
+def prefill_explicit_rows(q_nope: np.ndarray, q_rope: np.ndarray, c_kv: np.ndarray, k_r_raw: np.ndarray,
+                          w_uk: np.ndarray, w_uv: np.ndarray, scale: float, base: float,
+                          query_positions, causal: bool = True, start: int = 0):
+    """Prefill without absorption: every head's keys and values are rebuilt from the
+    latent once, k_h,t = [c_KV,t W_UK,h^T || RoPE(k_R,t, t)] and v_h,t = c_KV,t W_UV,h^T,
+    and the prompt queries q_h,i = [q_nope,h,i || RoPE(q_R,h,i, start + i)] run standard
+    softmax attention (0539edu.com section 2.2 and the training-form listing of
+    section 3.2; the same page notes the absorbed form costs more compute in prefill
+    and that the explicit form is the precision fallback; hotelren.com section 6.2
+    for the rotated key shared by all heads).
+
+    q_nope [S, H, d_k], q_rope [S, H, d_r] for the prompt queries at positions
+    start..start+S-1; c_kv [n, d_c] and k_r_raw [n, d_r] for the sequence's rows
+    0..n-1 (n >= start + S).  Query i reads rows 0..start+i when causal, else rows
+    0..start+S-1.  Returns (o [k, H, d_v], lse [k, H]) for the k selected i."""
+    c_kv = np.asarray(c_kv, dtype=np.float64)
+    k_nope = np.einsum("tc,hdc->htd", c_kv, np.asarray(w_uk, dtype=np.float64))   # [H, n, d_k]
+    v = np.einsum("tc,hdc->htd", c_kv, np.asarray(w_uv, dtype=np.float64))        # [H, n, d_v]
+    k_rot = rope(k_r_raw, np.arange(c_kv.shape[0]), base)                           # [n, d_r]
+    q_nope = np.asarray(q_nope, dtype=np.float64)
+    S = q_nope.shape[0]
+    outs, lses = [], []
+    for i in query_positions:
+        n = start + i + 1 if causal else start + S
+        q_rot = rope(q_rope[i], start + i, base)                                   # [H, d_r]
+        s = scale * (np.einsum("hd,htd->ht", q_nope[i], k_nope[:, :n]) + q_rot @ k_rot[:n].T)
+        outs.append(np.einsum("ht,htd->hd", softmax_rows(s), v[:, :n]))
+        lses.append(logsumexp_rows(s))
+    return np.stack(outs), np.stack(lses)
+
+
 # --------------------------------------------------------------------------
 # Tiny hidden-state-driven decode (projections as input preparation)
 # --------------------------------------------------------------------------

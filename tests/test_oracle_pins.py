@@ -442,3 +442,54 @@ def test_kv_down_rows_invariants():
     # no positional key (d_r = 0): the row is the normalised latent alone
     r = O.kv_down_rows(h, w_dkv, np.zeros((256, 0)), np.ones(512), 0.0, np.zeros(5), 1e4)
     assert r.shape == (5, 512)
+
+
+# ---------------------------------------------------------------------------
+# Explicit (non-absorbed) prefill
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("causal,start", [(True, 0), (True, 5), (False, 3)])
+def test_explicit_prefill_equals_absorbed(causal, start):
+    # the absorption identities (0539edu.com section 3.1) make the two forms equal:
+    # a transposed W_UK / W_UV, a RoPE at the wrong position or a wrong causal
+    # limit in either would break it
+    rng = np.random.default_rng(41 + start)
+    S, H, d_c, d_r, d_k, d_v, base, scale = 6, 3, 16, 4, 8, 5, 100.0, 0.3
+    n = start + S
+    c_kv, k_r = rng.standard_normal((n, d_c)), rng.standard_normal((n, d_r))
+    q_nope, q_r = rng.standard_normal((S, H, d_k)), rng.standard_normal((S, H, d_r))
+    w_uk, w_uv = rng.standard_normal((H, d_k, d_c)) * 0.3, rng.standard_normal((H, d_v, d_c)) * 0.3
+    o_ex, lse_ex = O.prefill_explicit_rows(q_nope, q_r, c_kv, k_r, w_uk, w_uv, scale, base, range(S), causal, start)
+    rows = O.cache_rows(c_kv, k_r, np.arange(n), base)
+    q_cat = np.stack([O.absorb_q(q_nope[i], q_r[i], start + i, w_uk, base) for i in range(S)])
+    o_lat, lse_ab = O.prefill_absorbed_rows(q_cat, rows, d_c, scale, range(S), causal, start)
+    np.testing.assert_allclose(o_ex, O.out_up(o_lat, w_uv), rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(lse_ex, lse_ab, rtol=1e-12)
+
+
+def test_explicit_prefill_brute_force():
+    # one head, every score and weight written out as loops
+    rng = np.random.default_rng(47)
+    S, d_c, d_r, d_k, d_v, base, scale = 4, 3, 2, 2, 2, 10.0, 0.7
+    c_kv, k_r = rng.standard_normal((S, d_c)), rng.standard_normal((S, d_r))
+    q_nope, q_r = rng.standard_normal((S, 1, d_k)), rng.standard_normal((S, 1, d_r))
+    w_uk, w_uv = rng.standard_normal((1, d_k, d_c)), rng.standard_normal((1, d_v, d_c))
+    o, lse = O.prefill_explicit_rows(q_nope, q_r, c_kv, k_r, w_uk, w_uv, scale, base, range(S))
+
+    def rot(x, p):  # d_r = 2: one pair, angle p * base^0 = p
+        return [x[0] * math.cos(p) - x[1] * math.sin(p), x[0] * math.sin(p) + x[1] * math.cos(p)]
+
+    for i in range(S):
+        qr = rot(q_r[i, 0], i)
+        scores = []
+        for t in range(i + 1):
+            k = [sum(c_kv[t, c] * w_uk[0, d, c] for c in range(d_c)) for d in range(d_k)]
+            kr = rot(k_r[t], t)
+            scores.append(scale * (sum(q_nope[i, 0, d] * k[d] for d in range(d_k)) + qr[0] * kr[0] + qr[1] * kr[1]))
+        z = sum(math.exp(x) for x in scores)
+        for d in range(d_v):
+            want = sum(math.exp(scores[t]) / z * sum(c_kv[t, c] * w_uv[0, d, c] for c in range(d_c))
+                       for t in range(i + 1))
+            assert o[i, 0, d] == pytest.approx(want, rel=1e-11, abs=1e-13)
+        assert lse[i, 0] == pytest.approx(math.log(z), rel=1e-12)
+    # the first query attends only to token 0: its value row exactly
+    np.testing.assert_allclose(o[0, 0], w_uv[0] @ c_kv[0], rtol=1e-13)
