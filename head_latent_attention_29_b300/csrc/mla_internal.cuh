@@ -41,10 +41,10 @@ constexpr int kPageRows = MLA_PAGE_ROWS;  // rows per page of a paged cache
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-// RoPE frequencies theta_i = base^(-2i/d_r), i < d_r/2, computed once on the host in
-// double and passed by value to the kernels (d_r <= 128).
-// RoPE frequencies as turns per position: u_i = theta_i / (2 pi), theta_i =
-// base^(-2i/d_r), held as an unevaluated fp32 sum u_hi + u_lo (about 48 bits).
+// RoPE frequencies as turns per position, u_i = theta_i / (2 pi) with theta_i =
+// base^(-2i/d_r) for i < d_r/2 (d_r <= 128): computed once on the host in double,
+// held as an unevaluated fp32 sum u_hi + u_lo (about 48 bits) and passed by value
+// to the kernels.
 struct RopeTable {
   float u_hi[64];
   float u_lo[64];

@@ -112,8 +112,9 @@ MLA_API const char* mla_status_string(mla_status status);
  * mla_cache_append -- write T new tokens into the latent cache.
  *   For each i < T: cache[seq_idx[i]][pos[i]] = [c_kv[i] || RoPE(k_r[i], pos[i])].
  *   RoPE rotates pairs (2j, 2j+1) of k_r by angle pos * base^(-2j/d_r) (the
- *   frequencies are formed in double precision, the angle to about 1e-6 rad).  (Decoupled RoPE key: icman.com.cn section 2;
- *   hotelren.com section 6.2; append-by-position: 0539edu.com section 5.2.)
+ *   frequencies are formed in double precision, the angle to about 1e-6 rad).
+ *   (Decoupled RoPE key: icman.com.cn section 2; hotelren.com section 6.2;
+ *   append-by-position: 0539edu.com section 5.2.)
  *   c_kv     [T, d_c]   dtype = cache->dtype
  *   k_r      [T, d_r]   dtype = cache->dtype; may be NULL iff d_r == 0
  *   seq_idx  [T] int32  sequence of each row, in [0, B)
