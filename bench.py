@@ -220,6 +220,20 @@ def workload_bytes_flops(cfg, lens):
     return bytes_attn, flops_attn
 
 
+def step_bytes_flops(cfg, lens):
+    """Algorithmic bytes and FLOPs of the whole decode step: the attention's cache
+    read plus the weights the step streams once (W_UK and W_UV, and W_g for the
+    gated workload), and the absorb, up-projection and gate contractions."""
+    B, H, d_c, d_k, d_v = cfg["B"], cfg["H"], cfg["d_c"], cfg["d_k"], cfg["d_v"]
+    nbytes, flops = workload_bytes_flops(cfg, lens)
+    nbytes += H * (d_k + d_v) * d_c * 2
+    flops += 2 * B * H * (d_k + d_v) * d_c
+    if cfg["d_r"] == 0 and "d_model" in cfg:
+        nbytes += cfg["d_model"] * H * d_v * 2
+        flops += 2 * B * cfg["d_model"] * H * d_v
+    return nbytes, flops
+
+
 def paged_block_table(lens, seed: int, page_rows: int = 64):
     """Block table [B, max_blocks] int32 giving each sequence's 64-row blocks
     distinct pages of one pool in a seeded random order (how pages end up after
@@ -398,6 +412,8 @@ def run_b300(args, rank, world, device):
     t_tc = flops_attn / (tc_burst * 1e12)
     roof_us = max(t_mem, t_tc) * 1e6
     traffic = None if wl.paged else _ncu_traffic(args.workload)  # counters were taken on the contiguous cache
+    step_bytes, step_flops = step_bytes_flops(cfg, wl.lens)
+    step_roof_us = max(step_bytes / (hbm * 1e9), step_flops / (tc_burst * 1e12)) * 1e6
 
     out = {
         "metric": decode_metric(args.workload, cfg),
@@ -433,6 +449,12 @@ def run_b300(args, rank, world, device):
             "roofline_us": round(roof_us, 3), "frac_of_roofline": round(roof_us / attn_us, 4),
             "frac_of_roofline_sustained_tc": (round(max(t_mem, flops_attn / (tc_sust * 1e12)) * 1e6 / attn_us, 4)
                                               if tc_sust else None),
+        },
+        "step_roofline": {
+            "bound": "hbm" if step_bytes / (hbm * 1e9) >= step_flops / (tc_burst * 1e12) else "tensor",
+            "algorithmic_bytes": step_bytes, "algorithmic_flops": step_flops,
+            "roofline_us": round(step_roof_us, 3), "step_us": round(ms_step * 1e3, 3),
+            "frac": round(step_roof_us / (ms_step * 1e3), 4),
         },
         "clocks": clk.summary(),
     }

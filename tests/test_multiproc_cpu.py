@@ -143,3 +143,26 @@ def test_kv_down_bench_accounting():
     cfg = W.WORKLOADS["kvdown_t32768_d7168"]
     seq, pos, B, N = bench.kvdown_rows_slots(cfg)
     assert len(seq) == cfg["T"] == B * N and len(set(zip(seq.tolist(), pos.tolist()))) == cfg["T"]
+
+
+def test_decode_step_roofline_accounting():
+    # the whole step adds W_UK and W_UV (2 x 128 x 128 x 512 bf16 = 33.6 MB) to the
+    # cache read, and the absorb and up-projection contractions (2 B H (d_k + d_v) d_c
+    # = 1.07 GFLOP) to the attention's FLOPs; the gated step adds W_g and its GEMM
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    import mla_workloads as W
+    cfg = W.WORKLOADS["decode_h128_b32_n4096"]
+    lens = W.seq_lens(cfg, 0)
+    b_att, f_att = bench.workload_bytes_flops(cfg, lens)
+    b_step, f_step = bench.step_bytes_flops(cfg, lens)
+    assert b_att == 150_994_944 and b_step - b_att == 33_554_432
+    assert f_step - f_att == 1_073_741_824
+    g = W.WORKLOADS["gated_h64_b16_n131072"]
+    lens = W.seq_lens(g, 0)
+    b_att, f_att = bench.workload_bytes_flops(g, lens)
+    b_step, f_step = bench.step_bytes_flops(g, lens)
+    assert b_step - b_att == 64 * 256 * 512 * 2 + 4096 * 8192 * 2
+    assert f_step - f_att == 2 * 16 * 64 * 256 * 512 + 2 * 16 * 4096 * 8192
+    assert np.isclose(b_att, 16 * 131072 * 512 * 2)
