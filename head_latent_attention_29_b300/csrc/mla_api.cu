@@ -1,9 +1,37 @@
 // extern "C" entry points of libmla: host-side validation and dispatch to the
 // kernels.  Nothing here allocates device memory or synchronises the host
 // (except mla_get_device_error, which reads the device error word).
+#include <cstdlib>
+
+#include <nvtx3/nvToolsExt.h>
+
 #include "mla_internal.cuh"
 
 namespace {
+
+// Optional NVTX ranges around the compute entry points, so that a profiler can
+// select one operation's kernels (ncu --nvtx --nvtx-include "mla_decode_attn/").
+// On when MLA_NVTX=1 is in the environment at the first call; otherwise each call
+// costs one predictable branch.
+bool nvtx_on() {
+  static const bool on = [] {
+    const char* v = std::getenv("MLA_NVTX");
+    return v != nullptr && v[0] == '1';
+  }();
+  return on;
+}
+
+struct OpRange {
+  bool on;
+  explicit OpRange(const char* name) : on(nvtx_on()) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~OpRange() {
+    if (on) nvtxRangePop();
+  }
+  OpRange(const OpRange&) = delete;
+  OpRange& operator=(const OpRange&) = delete;
+};
 
 using mla::aligned16;
 using mla::aligned4;
@@ -85,6 +113,7 @@ MLA_API const char* mla_status_string(mla_status st) {
 MLA_API mla_status mla_cache_append(const mla_cache* cache, const void* c_kv, const void* k_r,
                                     const int32_t* seq_idx, const int32_t* pos, int32_t T, float rope_base,
                                     void* stream) {
+  const OpRange range("mla_cache_append");
   mla_status st = check_cache(cache);
   if (st != MLA_OK) return st;
   if (T < 0) return MLA_ERR_INVALID_ARG;
@@ -99,6 +128,7 @@ MLA_API mla_status mla_cache_append(const mla_cache* cache, const void* c_kv, co
 MLA_API mla_status mla_absorb_q(const void* q_nope, const void* q_rope, const int32_t* q_pos, const void* w_uk,
                                 void* q_cat, int32_t B, int32_t H, int32_t d_k, int32_t d_c, int32_t d_r,
                                 int32_t dtype, float rope_base, void* stream) {
+  const OpRange range("mla_absorb_q");
   if (!valid_dtype(dtype)) return MLA_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || d_k <= 0 || d_c <= 0 || d_r < 0 || (d_r & 1) != 0) return MLA_ERR_INVALID_ARG;
   if (q_nope == nullptr || w_uk == nullptr || q_cat == nullptr || q_pos == nullptr) return MLA_ERR_INVALID_ARG;
@@ -124,6 +154,7 @@ MLA_API size_t mla_decode_workspace_size(int32_t B, int32_t H, int32_t d_c, int3
 MLA_API mla_status mla_decode_attn(const void* q_cat, const mla_cache* cache, const int32_t* seq_lens, int32_t H,
                                    float scale, void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
                                    void* stream) {
+  const OpRange range("mla_decode_attn");
   mla_status st = check_cache(cache);
   if (st != MLA_OK) return st;
   if (q_cat == nullptr || seq_lens == nullptr || o_lat == nullptr || H <= 0) return MLA_ERR_INVALID_ARG;
@@ -149,6 +180,7 @@ MLA_API size_t mla_prefill_workspace_size(int32_t B, int32_t S, int32_t H, int32
 MLA_API mla_status mla_prefill_attn(const void* q_cat, const mla_cache* cache, const int32_t* q_start, int32_t S,
                                     int32_t H, float scale, int32_t causal, void* workspace,
                                     size_t workspace_bytes, void* o_lat, float* lse, void* stream) {
+  const OpRange range("mla_prefill_attn");
   mla_status st = check_cache(cache);
   if (st != MLA_OK) return st;
   if (q_cat == nullptr || q_start == nullptr || o_lat == nullptr || H <= 0 || S <= 0) return MLA_ERR_INVALID_ARG;
@@ -169,6 +201,7 @@ MLA_API mla_status mla_prefill_attn(const void* q_cat, const mla_cache* cache, c
 
 MLA_API mla_status mla_out_up(const void* o_lat, const void* w_uv, void* o, int32_t B, int32_t H, int32_t d_c,
                               int32_t d_v, int32_t dtype, void* stream) {
+  const OpRange range("mla_out_up");
   if (!valid_dtype(dtype)) return MLA_ERR_INVALID_ARG;
   if (o_lat == nullptr || w_uv == nullptr || o == nullptr) return MLA_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || d_c <= 0 || d_v <= 0) return MLA_ERR_INVALID_ARG;
@@ -181,6 +214,7 @@ MLA_API mla_status mla_out_up(const void* o_lat, const void* w_uv, void* o, int3
 
 MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, int32_t d_model, int32_t width,
                             int32_t dtype, void* stream) {
+  const OpRange range("mla_gate");
   if (!valid_dtype(dtype)) return MLA_ERR_INVALID_ARG;
   if (h == nullptr || w_g == nullptr || o == nullptr) return MLA_ERR_INVALID_ARG;
   if (B <= 0 || d_model <= 0 || width <= 0) return MLA_ERR_INVALID_ARG;
@@ -193,6 +227,7 @@ MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, 
 MLA_API mla_status mla_cache_append_paged(const mla_paged_cache* cache, const void* c_kv, const void* k_r,
                                           const int32_t* seq_idx, const int32_t* pos, int32_t T, float rope_base,
                                           void* stream) {
+  const OpRange range("mla_cache_append_paged");
   mla_cache view;
   mla_status st = check_paged(cache, &view);
   if (st != MLA_OK) return st;
@@ -209,6 +244,7 @@ MLA_API mla_status mla_cache_append_paged(const mla_paged_cache* cache, const vo
 MLA_API mla_status mla_decode_attn_paged(const void* q_cat, const mla_paged_cache* cache, const int32_t* seq_lens,
                                          int32_t H, float scale, void* workspace, size_t workspace_bytes,
                                          void* o_lat, float* lse, void* stream) {
+  const OpRange range("mla_decode_attn_paged");
   mla_cache view;
   mla_status st = check_paged(cache, &view);
   if (st != MLA_OK) return st;
@@ -230,6 +266,7 @@ MLA_API mla_status mla_kv_down_append(const mla_cache* cache, const void* h, con
                                       float eps, const int32_t* seq_idx, const int32_t* pos, int32_t T,
                                       int32_t d_model, float rope_base, void* workspace, size_t workspace_bytes,
                                       void* stream) {
+  const OpRange range("mla_kv_down_append");
   const mla_status st = check_cache(cache);
   if (st != MLA_OK) return st;
   return kv_down(*cache, h, w_dkvr, gamma, eps, seq_idx, pos, T, d_model, rope_base, workspace, workspace_bytes,
@@ -240,6 +277,7 @@ MLA_API mla_status mla_kv_down_append_paged(const mla_paged_cache* cache, const 
                                             const void* gamma, float eps, const int32_t* seq_idx,
                                             const int32_t* pos, int32_t T, int32_t d_model, float rope_base,
                                             void* workspace, size_t workspace_bytes, void* stream) {
+  const OpRange range("mla_kv_down_append_paged");
   mla_cache view;
   const mla_status st = check_paged(cache, &view);
   if (st != MLA_OK) return st;

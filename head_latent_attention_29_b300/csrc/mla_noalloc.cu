@@ -49,6 +49,7 @@ extern "C" {
 
 MLA_API mla_status mla_decode_attn_noalloc(const void* q_cat, const mla_cache* cache, const int32_t* seq_lens,
                                            int32_t H, float scale, void* o_lat, float* lse, void* stream) {
+  const OpRange range("mla_decode_attn_noalloc");
   if (cache == nullptr || q_cat == nullptr || seq_lens == nullptr || o_lat == nullptr) return MLA_ERR_INVALID_ARG;
   if (cache->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
   if (cache->B > mla::kNoAllocMaxBatch) return MLA_ERR_WORKSPACE;  // beyond the built-in scratch

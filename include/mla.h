@@ -32,6 +32,9 @@
  *     sequence length out of range) are skipped/clamped by the kernels and
  *     recorded in a device error word, which mla_get_device_error() returns.
  *   - No exception crosses this ABI; every entry point returns mla_status.
+ *   - With MLA_NVTX=1 in the environment (read at the first call), every compute
+ *     entry point runs inside an NVTX range named after it, so that a profiler can
+ *     select one operation's kernels; off, each call costs one branch.
  */
 #ifndef MLA_H_
 #define MLA_H_
