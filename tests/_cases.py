@@ -5,7 +5,6 @@ only from the float64 oracle.  The CUDA path receives the same materialised
 (bf16 or fp32) bytes the oracle widens."""
 from __future__ import annotations
 
-import math
 
 import numpy as np
 import torch

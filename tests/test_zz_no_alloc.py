@@ -5,7 +5,6 @@ mla_decode_attn_noalloc serves callers that cannot allocate device memory when
 they run attention (graph capture/replay, non-reentrant allocators, embedders
 that only own their input and output buffers); it takes its scratch from a buffer
 built into the library.  This file is collected last on purpose."""
-import ctypes
 import math
 
 import numpy as np
