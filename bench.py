@@ -1,7 +1,7 @@
 """MLA decode benchmark (one JSON line on stdout).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
-                    [--workload decode_h128_b32_n4096]
+                    [--workload decode_h128_b32_n4096] [--paged]
 
 A step is one decode step of the whole hot path for every sequence of the batch:
 append the new token's latent row (RoPE on its key), absorb W_UK into the query,
@@ -21,6 +21,15 @@ path).
 
 `--impl reference` times the float64 CPU oracle on a bounded sample of the same
 workload on the host cores (rank 0 only).
+
+Other workloads (see mla_workloads): ragged and gated decode steps; prefill
+steps (`prefill_*`: append the prompt rows, absorb every query, causal prefill
+attention, W_UV); and the new tokens' cache rows straight from hidden states
+(`kvdown_*`: projection, RMSNorm, RoPE, append).  `--paged` runs a decode
+workload over a paged cache (64-row pages of one pool in shuffled order).  The
+decode line carries the attention op's roofline (`roofline`, with the ncu DRAM
+traffic when the stored counters match the kernel source) and the whole step's
+(`step_roofline`).
 """
 from __future__ import annotations
 
