@@ -178,3 +178,44 @@ def test_nvtx_ranges_switch_on_without_a_tool(tmp_path):
     env = dict(os.environ, MLA_NVTX="1", PYTHONPATH=ROOT)
     out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120)
     assert out.returncode == 0 and out.stdout.strip() == "ok", out.stderr
+
+
+def test_header_compiles_as_c_and_layouts_match_the_binding(tmp_path, libmla):
+    # a plain C consumer of include/mla.h: the header must be valid C99, every
+    # declared entry point must link against the built library, and the structs
+    # the caller fills must have the layout the Python binding assumes
+    import shutil
+    import subprocess
+    import head_latent_attention_29_b300 as mla
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    syms = _declared_symbols()
+    src = tmp_path / "consumer.c"
+    src.write_text(
+        "#include <stddef.h>\n#include <stdint.h>\n#include <stdio.h>\n#include \"mla.h\"\n"
+        "int main(void) {\n"
+        "  volatile uintptr_t a;\n"
+        + "".join(f"  a = (uintptr_t)&{s};\n  printf(\"%d\\n\", (int)(a != 0));\n" for s in syms)
+        + "  printf(\"%zu %zu %zu %zu %zu\\n\", sizeof(mla_cache), offsetof(mla_cache, dtype), "
+          "offsetof(mla_cache, d_r), offsetof(mla_cache, row_stride), offsetof(mla_cache, N_max));\n"
+          "  printf(\"%zu %zu %zu %zu %zu\\n\", sizeof(mla_paged_cache), offsetof(mla_paged_cache, num_pages), "
+          "offsetof(mla_paged_cache, row_stride), offsetof(mla_paged_cache, block_table), "
+          "offsetof(mla_paged_cache, max_blocks));\n"
+          "  return 0;\n}\n")
+    exe = tmp_path / "consumer"
+    lib_dir = os.path.dirname(mla.LIB_PATH)
+    cc = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                         "-L", lib_dir, "-l:libmla.so", f"-Wl,-rpath,{lib_dir}", "-o", str(exe)],
+                        capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    lines = out.stdout.split()
+    assert lines[:len(syms)] == ["1"] * len(syms)
+    c = [int(x) for x in lines[len(syms):len(syms) + 5]]
+    p = [int(x) for x in lines[len(syms) + 5:len(syms) + 10]]
+    C, P = mla._Cache, mla._PagedCache
+    assert c == [ctypes.sizeof(C), C.dtype.offset, C.d_r.offset, C.row_stride.offset, C.N_max.offset]
+    assert p == [ctypes.sizeof(P), P.num_pages.offset, P.row_stride.offset, P.block_table.offset,
+                 P.max_blocks.offset]
