@@ -42,6 +42,7 @@
 //    the mix of lengths.  A problem that lies inside one run is normalised and
 //    written out directly; one cut by run boundaries leaves an unnormalised
 //    partial (m, l, O) per piece, and a combine kernel merges the pieces.
+#include <atomic>
 #include <cmath>
 
 #include "mla_internal.cuh"
@@ -1026,14 +1027,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
+  static std::atomic<EncodeTiledFn> cached{nullptr};  // looked up until it succeeds once
+  EncodeTiledFn fn = cached.load(std::memory_order_acquire);
   if (fn == nullptr) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
+        q == cudaDriverEntryPointSuccess) {
       fn = reinterpret_cast<EncodeTiledFn>(p);
+      cached.store(fn, std::memory_order_release);
+    }
   }
   return fn;
 }
@@ -1065,13 +1069,12 @@ constexpr WsLayout ws_layout(long long np) {
 static int g_inject_fault = 0;
 
 static int pairs_for_device() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];  // zero-initialised: not yet computed
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
-  if (cached[dev] > 0) return cached[dev];
-  if (cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
-      cudaSuccess)
-    return -1;
+  const int known = cached[dev].load(std::memory_order_acquire);
+  if (known > 0) return known;
+  if (ensure_smem_limit(reinterpret_cast<const void*>(decode_split_kernel), kSmemAlloc) != cudaSuccess) return -1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * kMaxPairs, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1085,8 +1088,9 @@ static int pairs_for_device() {
   cfg.numAttrs = 1;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, decode_split_kernel, &cfg) != cudaSuccess || n <= 0) return -1;
-  cached[dev] = n < kMaxPairs ? n : kMaxPairs;
-  return cached[dev];
+  const int pairs = n < kMaxPairs ? n : kMaxPairs;
+  cached[dev].store(pairs, std::memory_order_release);  // concurrent first calls compute the same value
+  return pairs;
 }
 
 }  // namespace dtc

@@ -11,6 +11,8 @@
 // M = 128 tcgen05 instruction.  W_UK[h] ([d_k][d_c]) is an MN-major A operand,
 // W_UV[h] ([d_v][d_c]) a K-major one; the per-head activations are K-major B
 // operands read straight from [B][H][K] through a 3-D tensor map.
+#include <atomic>
+
 #include "mla_internal.cuh"
 #include "mla_ptx.cuh"
 
@@ -244,13 +246,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
+  static std::atomic<EncodeTiledFn> cached{nullptr};  // looked up until it succeeds once
+  EncodeTiledFn fn = cached.load(std::memory_order_acquire);
   if (fn == nullptr) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
+        q == cudaDriverEntryPointSuccess) {
       fn = reinterpret_cast<EncodeTiledFn>(p);
+      cached.store(fn, std::memory_order_release);
+    }
   }
   return fn;
 }
@@ -315,12 +320,7 @@ static mla_status launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   const size_t ring = static_cast<size_t>(g.stages) * (kBM * kBK * 2 + g.n_tile * kBK * 2);
   const size_t tile = static_cast<size_t>(g.n_tile) * kBM * 2;
   const size_t smem = (ring > tile ? ring : tile) + 8 * (2 * kStagesHG + 1) + 1024;
-  static size_t done[2] = {0, 0};
-  if (smem > done[kAMN ? 1 : 0]) {
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
-      return MLA_ERR_CUDA;
-    done[kAMN ? 1 : 0] = smem;
-  }
+  if (ensure_smem_limit(reinterpret_cast<const void*>(k), smem) != cudaSuccess) return MLA_ERR_CUDA;
   return cuda_status(launch_pdl(k, dim3(m_tiles, g.H, n_tiles), dim3(kThreadsHG), smem, s, ma, mb, mo, g));
 }
 

@@ -399,13 +399,7 @@ mla_status launch_kv_down(const mla_cache& c, const void* h, const void* w, cons
     if (!hg::map_2d(&mh, h, d_model, T, 64, p.n_tile)) return MLA_ERR_CUDA;
     const size_t smem = static_cast<size_t>(p.stages) * (kBM * kBK * 2 + p.n_tile * kBK * 2) +
                         8 * (2 * kMaxStages + 1) + 1024;
-    static size_t done = 0;
-    if (smem > done) {
-      if (cudaFuncSetAttribute(kvd_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem)) != cudaSuccess)
-        return MLA_ERR_CUDA;
-      done = smem;
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void*>(kvd_gemm_kernel), smem) != cudaSuccess) return MLA_ERR_CUDA;
     if (launch_pdl(kvd_gemm_kernel, dim3(p.m_tiles, p.n_tiles, p.splits), dim3(kThreads), smem, s, mw, mh, g) !=
         cudaSuccess)
       return MLA_ERR_CUDA;

@@ -11,25 +11,6 @@
 
 namespace mla {
 
-// Raise a kernel's dynamic shared-memory limit once per (kernel, size): repeated
-// calls stay free of runtime configuration work, so steps can be graph-captured.
-static void ensure_smem(const void* fn, size_t bytes) {
-  if (bytes <= 48 * 1024) return;
-  static const void* done_fn[16] = {nullptr};
-  static size_t done_bytes[16] = {0};
-  for (int i = 0; i < 16; ++i) {
-    if (done_fn[i] == fn && done_bytes[i] >= bytes) return;
-  }
-  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-  for (int i = 0; i < 16; ++i) {
-    if (done_fn[i] == fn || done_fn[i] == nullptr) {
-      done_fn[i] = fn;
-      done_bytes[i] = bytes;
-      return;
-    }
-  }
-}
-
 // ============================================================================
 // Cache append: cache[seq][pos] = [c_kv || RoPE(k_r, pos)]
 // (icman.com.cn MLA article, section 2: the 64-wide key is cached with RoPE
@@ -182,13 +163,13 @@ mla_status launch_absorb_q(const void* q_nope, const void* q_rope, const int32_t
   const size_t smem = sizeof(float) * kAbsorbBatch * d_k;
   if (dtype == MLA_BF16) {
     auto k = absorb_q_kernel<__nv_bfloat16>;
-    ensure_smem(reinterpret_cast<const void*>(k), smem);
+    ensure_smem_limit(reinterpret_cast<const void*>(k), smem);
     k<<<grid, 128, smem, s>>>(static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(q_rope),
                               q_pos, static_cast<const __nv_bfloat16*>(w_uk), static_cast<__nv_bfloat16*>(q_cat),
                               B, H, d_k, d_c, d_r, rope_table(d_r, rope_base));
   } else {
     auto k = absorb_q_kernel<float>;
-    ensure_smem(reinterpret_cast<const void*>(k), smem);
+    ensure_smem_limit(reinterpret_cast<const void*>(k), smem);
     k<<<grid, 128, smem, s>>>(static_cast<const float*>(q_nope), static_cast<const float*>(q_rope), q_pos,
                               static_cast<const float*>(w_uk), static_cast<float*>(q_cat), B, H, d_k, d_c, d_r,
                               rope_table(d_r, rope_base));
@@ -245,12 +226,12 @@ mla_status launch_out_up(const void* o_lat, const void* w_uv, void* o, int32_t B
   const size_t smem = sizeof(float) * kOutBatch * d_c;
   if (dtype == MLA_BF16) {
     auto k = out_up_kernel<__nv_bfloat16>;
-    ensure_smem(reinterpret_cast<const void*>(k), smem);
+    ensure_smem_limit(reinterpret_cast<const void*>(k), smem);
     k<<<grid, 256, smem, s>>>(static_cast<const __nv_bfloat16*>(o_lat), static_cast<const __nv_bfloat16*>(w_uv),
                               static_cast<__nv_bfloat16*>(o), B, H, d_c, d_v);
   } else {
     auto k = out_up_kernel<float>;
-    ensure_smem(reinterpret_cast<const void*>(k), smem);
+    ensure_smem_limit(reinterpret_cast<const void*>(k), smem);
     k<<<grid, 256, smem, s>>>(static_cast<const float*>(o_lat), static_cast<const float*>(w_uv),
                               static_cast<float*>(o), B, H, d_c, d_v);
   }

@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -94,6 +95,42 @@ __device__ __forceinline__ void rope_sincos(int pos, float u_hi, float u_lo, flo
 }
 
 inline mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+// Raise a kernel's dynamic shared-memory limit on the current device, once per
+// (device, kernel) unless a larger size is asked for later.  A kernel attribute
+// belongs to one device's context, so every GPU the process uses gets its own
+// call; the table is guarded, so host threads may launch concurrently.  After the
+// first launch on a device no runtime configuration work remains, so a step can
+// be captured in a CUDA graph once it has run eagerly there.
+inline cudaError_t ensure_smem_limit(const void* fn, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  struct Done {
+    const void* fn;
+    int dev;
+    size_t bytes;
+  };
+  constexpr int kSlots = 256;
+  static std::mutex mu;
+  static Done done[kSlots];
+  static int n_done = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int slot = -1;
+  for (int i = 0; i < n_done; ++i) {
+    if (done[i].fn == fn && done[i].dev == dev) {
+      if (done[i].bytes >= bytes) return cudaSuccess;
+      slot = i;
+      break;
+    }
+  }
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  if (slot < 0 && n_done < kSlots) slot = n_done++;
+  if (slot >= 0) done[slot] = Done{fn, dev, bytes};  // a full table only means repeated calls
+  return cudaSuccess;
+}
 
 // Launch with programmatic stream serialisation (the kernel may start while the
 // previous kernel in the stream drains; it synchronises with griddep_wait()).
