@@ -809,7 +809,7 @@ def cpu_baseline_kvdown(workload: str, seed: int, budget_s: float = 12.0):
     except Exception:  # pragma: no cover
         threads = []
     return {"value": round(done / el, 3), "unit": "tokens/s", "cores": max(threads) if threads else 1,
-            "kind": "oracle", "host_cpus": os.cpu_count(),
+            "kind": "oracle", "host_cpus": os.cpu_count(), "cpu_model": _cpu_model(),
             "sample": f"{done} tokens in batches of {n} (float64 numpy), {el:.1f} s"}
 
 
@@ -848,7 +848,7 @@ def cpu_baseline_prefill(workload: str, seed: int, budget_s: float = 12.0):
     except Exception:  # pragma: no cover
         threads = []
     return {"value": round(done / el, 3), "unit": "tokens/s", "cores": max(threads) if threads else 1,
-            "kind": "oracle", "host_cpus": os.cpu_count(),
+            "kind": "oracle", "host_cpus": os.cpu_count(), "cpu_model": _cpu_model(),
             "sample": f"{done} prompt query rows of sequence 0 at random positions of 0..{S - 1} "
                       f"(causal prefix each), float64 numpy, {el:.1f} s"}
 
@@ -880,6 +880,19 @@ def _kernel_hash():
 
 
 # ---------------------------------------------------------------- CPU oracle baseline
+def _cpu_model() -> str:
+    """The host CPU's model name (from /proc/cpuinfo), for the baseline's record."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
 def cpu_baseline(workload: str, seed: int, budget_s: float = 12.0):
     """Time the float64 oracle's decode step (absorb_q, attention over the prebuilt
     cache rows, out_up) on the host cores for a bounded sample of sequences."""
@@ -916,7 +929,7 @@ def cpu_baseline(workload: str, seed: int, budget_s: float = 12.0):
     threads = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
     env = {k: os.environ[k] for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS") if k in os.environ}
     return {"value": round(done / el, 3), "unit": "tokens/s", "cores": max(threads) if threads else 1,
-            "kind": "oracle", "host_cpus": os.cpu_count(), "thread_env": env,
+            "kind": "oracle", "host_cpus": os.cpu_count(), "cpu_model": _cpu_model(), "thread_env": env,
             "sample": f"{done} decode steps of sequences {sample} (N={[int(lens[b]) for b in sample]}), "
                       f"float64 numpy, {el:.1f} s"}
 
