@@ -493,3 +493,20 @@ def test_explicit_prefill_brute_force():
         assert lse[i, 0] == pytest.approx(math.log(z), rel=1e-12)
     # the first query attends only to token 0: its value row exactly
     np.testing.assert_allclose(o[0, 0], w_uv[0] @ c_kv[0], rtol=1e-13)
+
+
+def test_hidden_state_workload_recipe():
+    # the kv_down inputs follow the recipe the design states: h ~ N(0,1), W_DKV and
+    # W_KR ~ N(0, 1/d_model), a gain 1 + N(0, 0.1^2); seeded and reproducible
+    cfg = W.WORKLOADS["kvdown_b32_d7168"]
+    h, w_dkv, w_kr, g = W.kv_down_inputs(cfg, 0)
+    assert h.shape == (32, 7168) and w_dkv.shape == (7168, 512) and w_kr.shape == (7168, 64) and g.shape == (512,)
+    assert abs(h.std() - 1.0) < 0.01 and abs(h.mean()) < 0.01
+    assert abs(w_dkv.std() * math.sqrt(7168) - 1.0) < 0.01 and abs(w_kr.std() * math.sqrt(7168) - 1.0) < 0.01
+    assert abs(g.mean() - 1.0) < 0.02 and abs(g.std() - 0.1) < 0.01
+    for a, b in zip((h, w_dkv, w_kr, g), W.kv_down_inputs(cfg, 0)):
+        np.testing.assert_array_equal(a, b)
+    assert not np.array_equal(h, W.kv_down_inputs(cfg, 1)[0])
+    # the projection keeps unit scale: x = h W_DKV has unit variance per channel
+    x = h.astype(np.float64) @ w_dkv.astype(np.float64)
+    assert abs(x.std() - 1.0) < 0.05
