@@ -30,7 +30,7 @@ Everything here is plain float64 numpy, written to be read against the pages:
   h W_DKV; and the interview guide's section 6.2 listing, where the RoPE key is
   its own projection h W_KR of the hidden state.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 RoPE rotates adjacent pairs (2i, 2i+1) with theta_i = base^(-2i/d_r); the decode
 query sits at position N-1 and attends to all N cached tokens including itself;
 the softmax scale is a runtime argument; the RMSNorm has a per-channel gain gamma

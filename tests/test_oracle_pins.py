@@ -105,6 +105,66 @@ def test_tiny_workload_from_hidden_states_absorbed_equals_explicit():
 
 
 # ---------------------------------------------------------------------------
+# The projections from hidden states, pinned without their own formula
+# (0539edu.com section 2.2: c_KV = h W_DKV; hotelren.com section 6.2: one RoPE
+# key k_R = h W_KR for all heads; per head d_k no-position query columns, then d_r)
+# ---------------------------------------------------------------------------
+def test_project_from_hidden_one_hot_rows_select_weight_rows():
+    rng = np.random.default_rng(7)
+    d_model, d_c, H, d_k, d_r = 6, 5, 3, 4, 2
+    w_dkv = rng.standard_normal((d_model, d_c))
+    w_kr = rng.standard_normal((d_model, d_r))
+    w_uq = rng.standard_normal((d_model, H * (d_k + d_r)))
+    # row i of h is the unit vector e_i: every projection returns row i of its weight
+    c_kv, k_r, q_nope, q_r = O.project_from_hidden(np.eye(d_model), w_dkv, w_kr, w_uq, H, d_k, d_r)
+    assert np.array_equal(c_kv, w_dkv) and np.array_equal(k_r, w_kr)
+    for i in range(d_model):
+        for hh in range(H):
+            base_col = hh * (d_k + d_r)
+            assert np.array_equal(q_nope[i, hh], w_uq[i, base_col:base_col + d_k])
+            assert np.array_equal(q_r[i, hh], w_uq[i, base_col + d_k:base_col + d_k + d_r])
+
+
+def test_project_from_hidden_head_major_split_order():
+    # W_UQ built so that head hh's block holds (hh + 1) in its d_k no-position
+    # columns and -(hh + 1) in its d_r position columns: a component-major layout
+    # or swapped q_nope / q_R columns gives different constants.
+    d_model, H, d_k, d_r = 3, 4, 5, 2
+    w_uq = np.zeros((d_model, H * (d_k + d_r)))
+    for hh in range(H):
+        w_uq[0, hh * (d_k + d_r):hh * (d_k + d_r) + d_k] = hh + 1
+        w_uq[0, hh * (d_k + d_r) + d_k:(hh + 1) * (d_k + d_r)] = -(hh + 1)
+    h = np.array([[1.0, 0.0, 0.0], [2.0, 5.0, -1.0]])  # only column 0 of h reaches W_UQ's row 0
+    _, _, q_nope, q_r = O.project_from_hidden(h, np.zeros((d_model, 1)), np.zeros((d_model, d_r)), w_uq,
+                                              H, d_k, d_r)
+    for n, scale in ((0, 1.0), (1, 2.0)):
+        for hh in range(H):
+            assert np.all(q_nope[n, hh] == scale * (hh + 1))
+            assert np.all(q_r[n, hh] == -scale * (hh + 1))
+
+
+def test_project_from_hidden_matches_scalar_loops_two_heads():
+    rng = np.random.default_rng(11)
+    n, d_model, d_c, H, d_k, d_r = 3, 4, 3, 2, 3, 2
+    h = rng.standard_normal((n, d_model))
+    w_dkv = rng.standard_normal((d_model, d_c))
+    w_kr = rng.standard_normal((d_model, d_r))
+    w_uq = rng.standard_normal((d_model, H * (d_k + d_r)))
+    c_kv, k_r, q_nope, q_r = O.project_from_hidden(h, w_dkv, w_kr, w_uq, H, d_k, d_r)
+    for t in range(n):
+        for j in range(d_c):
+            assert abs(c_kv[t, j] - sum(h[t, m] * w_dkv[m, j] for m in range(d_model))) < 1e-12
+        for j in range(d_r):
+            assert abs(k_r[t, j] - sum(h[t, m] * w_kr[m, j] for m in range(d_model))) < 1e-12
+        for hh in range(H):
+            for j in range(d_k + d_r):
+                col = hh * (d_k + d_r) + j
+                want = sum(h[t, m] * w_uq[m, col] for m in range(d_model))
+                got = q_nope[t, hh, j] if j < d_k else q_r[t, hh, j - d_k]
+                assert abs(got - want) < 1e-12
+
+
+# ---------------------------------------------------------------------------
 # Brute force with scalar loops on tiny shapes
 # ---------------------------------------------------------------------------
 def _brute_force(q_nope, q_r, q_pos, c_kv, k_r, w_uk, w_uv, scale, base):
