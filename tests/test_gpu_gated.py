@@ -39,14 +39,22 @@ def test_gate_tensor_core(mla, B, d_model, width):
     check_bf16(got, ref, f"gate B{B} d{d_model} w{width}")
 
 
-@pytest.mark.parametrize("B,d_model,width,dtype", [(3, 100, 200, "bf16"), (4, 64, 96, "f32"), (17, 33, 40, "f32")])
-def test_gate_cuda_cores(mla, B, d_model, width, dtype):
-    # shapes the tensor-core path does not take (width % 128, d_model % 64) and fp32
-    got, ref = _gate_case(mla, 2, B, d_model, width, dtype)
-    if dtype == "f32":
-        check_f32(got, ref, "gate fp32")
-    else:
-        check_bf16(got, ref, "gate bf16 (CUDA cores)")
+@pytest.mark.parametrize("B,d_model,width", [(4, 64, 96), (17, 33, 40), (3, 4096, 256)])
+def test_gate_fp32_cuda_cores(mla, B, d_model, width):
+    # fp32 runs on the CUDA cores, any shape
+    got, ref = _gate_case(mla, 2, B, d_model, width, "f32")
+    check_f32(got, ref, "gate fp32")
+
+
+def test_gate_bf16_shape_outside_the_tensor_cores_is_refused(mla):
+    # bf16 has no CUDA-core gate to fall back to: a width that is not a multiple of
+    # 128 is refused and the output is left as it was
+    o = torch.ones(3, 200, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(mla.MlaError) as e:
+        mla.gate(torch.ones(3, 100, dtype=torch.bfloat16, device="cuda"),
+                 torch.ones(100, 200, dtype=torch.bfloat16, device="cuda"), o)
+    assert e.value.status == 2  # MLA_ERR_UNSUPPORTED
+    assert bool(torch.all(o == 1))
 
 
 def test_gate_zero_weights_halves(mla):
@@ -60,9 +68,9 @@ def test_gate_zero_weights_halves(mla):
     np.testing.assert_array_equal(o_dev.float().cpu().numpy(), W.widen(o, "bf16") * 0.5)
 
 
-def test_gated_step_full_size_sampled(mla):
+def test_gated_step_full_size(mla):
     # the whole gated step at B16 x H64 x N131072 (no RoPE, scale 1/sqrt(128)):
-    # append, absorb, split attention + combine, W_UV, gate; two sequences checked
+    # append, absorb, split attention + combine, W_UV, gate; every sequence checked
     # against the oracle one by one
     case = DecodeCase("gated_h64_b16_n131072", seed=5)
     cfg = case.cfg
@@ -84,7 +92,7 @@ def test_gated_step_full_size_sampled(mla):
     assert st == 0, (st, detail)
     got = o_flat.float().cpu().numpy()
     wg64 = W.widen(w_g, "bf16")
-    for b in (0, B - 1):
+    for b in range(B):
         ref_o, ref_lat, ref_lse = case.oracle_seq(b)
         check_bf16(o_lat[b].float().cpu().numpy(), ref_lat, f"gated o_lat b={b}")
         np.testing.assert_allclose(lse[b].cpu().numpy(), ref_lse, rtol=1e-3, atol=2e-2)

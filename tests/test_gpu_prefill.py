@@ -159,7 +159,9 @@ def test_prefill_start_out_of_range_is_recorded(mla):
 
 def test_prefill_full_size_step_sampled(mla):
     # B4 x S8192 x H128: append the prompt rows (RoPE at 0..8191), absorb every
-    # query at its own position, prefill attention, W_UV; sampled rows vs the oracle
+    # query at its own position, prefill attention, W_UV.  Checked against the
+    # oracle: every 61st query row plus the first and the last 64, all heads, of
+    # every sequence (260 rows each)
     cfg = W.WORKLOADS["prefill_h128_b4_s8192"]
     B, S, H, d_k, d_v = cfg["B"], cfg["S"], cfg["H"], cfg["d_k"], cfg["d_v"]
     seed, base, scale = 11, cfg["rope_base"], cfg["scale"]
@@ -186,14 +188,20 @@ def test_prefill_full_size_step_sampled(mla):
     assert st == 0, (st, detail)
     o = o.view(B, S, H, d_v)
     wd = lambda x: W.widen(x, "bf16")
+    rows_checked = sorted(set(range(0, S, 61)) | set(range(64)) | set(range(S - 64, S)))
+    idx = torch.tensor(rows_checked, device="cuda")
     for b in range(B):
         c, k, q_nope, q_r = host[b]
-        for i in (0, 1, 63, 64, 1000, 4095, 8191 - b):
-            ref_o, ref_lat, ref_lse = O.decode_absorbed_from_parts(
-                wd(q_nope[i]), wd(q_r[i]), i, wd(c[: i + 1]), wd(k[: i + 1]), np.arange(i + 1), wd(w_uk), wd(w_uv),
-                scale, base)
-            check_bf16(o_lat[b, i].float().cpu().numpy(), ref_lat, f"prefill o_lat b={b} i={i}")
-            check_bf16(o[b, i].float().cpu().numpy(), ref_o, f"prefill o b={b} i={i}")
+        got_lat = o_lat[b].index_select(0, idx).float().cpu().numpy()
+        got_o = o[b].index_select(0, idx).float().cpu().numpy()
+        got_lse = lse[b].index_select(0, idx).cpu().numpy()
+        rows = O.cache_rows(wd(c), wd(k), np.arange(S), base)
+        q_ref = O.absorb_q(wd(q_nope[rows_checked]), wd(q_r[rows_checked]), np.asarray(rows_checked), wd(w_uk), base)
+        for j, i in enumerate(rows_checked):
+            ref_lat, ref_lse = O.decode_absorbed(q_ref[j], rows[: i + 1], D_C, scale)
+            ref_o = O.out_up(ref_lat, wd(w_uv))
+            check_bf16(got_lat[j], ref_lat, f"prefill o_lat b={b} i={i}")
+            check_bf16(got_o[j], ref_o, f"prefill o b={b} i={i}")
             # q_lat is rounded to bf16 before the scores (as in the decode step): about
             # 2^-9 relative per term, a few 1e-3 on a unit-variance score
-            np.testing.assert_allclose(lse[b, i].cpu().numpy(), ref_lse, rtol=1e-3, atol=2e-2)
+            np.testing.assert_allclose(got_lse[j], ref_lse, rtol=1e-3, atol=2e-2)
