@@ -65,6 +65,7 @@ _lib_handle = None
 
 _SIGS = {
     "mla_abi_version": (ctypes.c_int32, []),
+    "mla_build_source_hash": (ctypes.c_char_p, []),
     "mla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "mla_cache_append": (ctypes.c_int, [ctypes.POINTER(_Cache), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p]),
@@ -115,6 +116,13 @@ def lib() -> ctypes.CDLL:
         if not os.path.exists(LIB_PATH):
             raise ImportError(f"libmla.so not built at {LIB_PATH}; run `python -m head_latent_attention_29_b300._build`")
         h = ctypes.CDLL(LIB_PATH)
+        if os.path.isdir(os.path.join(_PKG, "csrc")):
+            from . import _build
+            h.mla_build_source_hash.restype = ctypes.c_char_p
+            have, want = h.mla_build_source_hash().decode(), _build.source_hash()
+            if have != want:
+                raise ImportError(f"{LIB_PATH} was built from other sources (hash {have}, sources {want}); "
+                                  "rebuild it: `python -m head_latent_attention_29_b300._build`")
         for name, (res, args) in _SIGS.items():
             fn = getattr(h, name)
             fn.restype = res
@@ -143,6 +151,15 @@ def _dev_tensor(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _out_tensor(t: torch.Tensor, name: str, shape: tuple, dtype) -> torch.Tensor:
+    """A caller-supplied output: a contiguous CUDA tensor of exactly this shape and
+    dtype (the kernels write every element through maps built from the shape)."""
+    _dev_tensor(t, name, dtype)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     return t
 
 
@@ -225,12 +242,17 @@ def decode_attn(q_cat: torch.Tensor, cache: LatentCache, seq_lens: torch.Tensor,
     if B != cache.B or R != cache.d_c + cache.d_r:
         raise ValueError("q_cat shape does not match the cache")
     _dev_tensor(seq_lens, "seq_lens", torch.int32)
+    if seq_lens.numel() != B:
+        raise ValueError("seq_lens needs one entry per sequence")
     if workspace is None:
         workspace = decode_workspace(B, H, cache.d_c, cache.dtype, q_cat.device)
     if out is None:
         out = torch.empty((B, H, cache.d_c), dtype=cache.dtype, device=q_cat.device)
+    _out_tensor(out, "out", (B, H, cache.d_c), cache.dtype)
     if lse is None and want_lse:
         lse = torch.empty((B, H), dtype=torch.float32, device=q_cat.device)
+    if lse is not None:
+        _out_tensor(lse, "lse", (B, H), torch.float32)
     st = cache.struct()
     _check(lib().mla_decode_attn(_ptr(q_cat), ctypes.byref(st), _ptr(seq_lens), H, float(scale), _ptr(workspace),
                                  workspace.numel(), _ptr(out), _ptr(lse), _stream(q_cat)), "mla_decode_attn")
@@ -254,12 +276,17 @@ def prefill_attn(q_cat: torch.Tensor, cache: LatentCache, q_start: torch.Tensor,
     if B != cache.B or R != cache.d_c + cache.d_r:
         raise ValueError("q_cat shape does not match the cache")
     _dev_tensor(q_start, "q_start", torch.int32)
+    if q_start.numel() != B:
+        raise ValueError("q_start needs one entry per sequence")
     if workspace is None:
         workspace = prefill_workspace(B, S, H, cache.d_c, cache.dtype, q_cat.device)
     if out is None:
         out = torch.empty((B, S, H, cache.d_c), dtype=cache.dtype, device=q_cat.device)
+    _out_tensor(out, "out", (B, S, H, cache.d_c), cache.dtype)
     if lse is None and want_lse:
         lse = torch.empty((B, S, H), dtype=torch.float32, device=q_cat.device)
+    if lse is not None:
+        _out_tensor(lse, "lse", (B, S, H), torch.float32)
     st = cache.struct()
     _check(lib().mla_prefill_attn(_ptr(q_cat), ctypes.byref(st), _ptr(q_start), S, H, float(scale), int(causal),
                                   _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse), _stream(q_cat)),
@@ -273,9 +300,17 @@ def decode_attn_noalloc(q_cat: torch.Tensor, cache: LatentCache, seq_lens: torch
     the split-KV scratch is a buffer built into the library (at most 32 sequences).
     `out` (and `lse` if wanted) must be preallocated by the caller."""
     _dev_tensor(q_cat, "q_cat", cache.dtype)
+    if q_cat.dim() != 3:
+        raise ValueError("q_cat must be [B, H, d_c + d_r]")
+    B, H, R = q_cat.shape
+    if B != cache.B or R != cache.d_c + cache.d_r:
+        raise ValueError("q_cat shape does not match the cache")
     _dev_tensor(seq_lens, "seq_lens", torch.int32)
-    _dev_tensor(out, "out", cache.dtype)
-    H = q_cat.shape[1]
+    if seq_lens.numel() != B:
+        raise ValueError("seq_lens needs one entry per sequence")
+    _out_tensor(out, "out", (B, H, cache.d_c), cache.dtype)
+    if lse is not None:
+        _out_tensor(lse, "lse", (B, H), torch.float32)
     st = cache.struct()
     _check(lib().mla_decode_attn_noalloc(_ptr(q_cat), ctypes.byref(st), _ptr(seq_lens), H, float(scale), _ptr(out),
                                          _ptr(lse), _stream(q_cat)), "mla_decode_attn_noalloc")
@@ -380,12 +415,17 @@ def decode_attn_paged(q_cat: torch.Tensor, cache: PagedLatentCache, seq_lens: to
     if B != cache.B or R != cache.d_c + cache.d_r:
         raise ValueError("q_cat shape does not match the cache")
     _dev_tensor(seq_lens, "seq_lens", torch.int32)
+    if seq_lens.numel() != B:
+        raise ValueError("seq_lens needs one entry per sequence")
     if workspace is None:
         workspace = decode_workspace(B, H, cache.d_c, cache.dtype, q_cat.device)
     if out is None:
         out = torch.empty((B, H, cache.d_c), dtype=cache.dtype, device=q_cat.device)
+    _out_tensor(out, "out", (B, H, cache.d_c), cache.dtype)
     if lse is None and want_lse:
         lse = torch.empty((B, H), dtype=torch.float32, device=q_cat.device)
+    if lse is not None:
+        _out_tensor(lse, "lse", (B, H), torch.float32)
     st = cache.struct()
     _check(lib().mla_decode_attn_paged(_ptr(q_cat), ctypes.byref(st), _ptr(seq_lens), H, float(scale),
                                        _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse), _stream(q_cat)),

@@ -1065,8 +1065,9 @@ constexpr WsLayout ws_layout(long long np) {
   return w;
 }
 
-// Fault injection for the tests of the bounded waits (see mla_debug_inject_fault).
-static int g_inject_fault = 0;
+// Fault injection for the tests of the bounded waits (see mla_debug_inject_fault):
+// one process-wide switch, read by every later launch on any host thread.
+static std::atomic<int> g_inject_fault{0};
 
 static int pairs_for_device() {
   static std::atomic<int> cached[64];  // zero-initialised: not yet computed
@@ -1097,7 +1098,7 @@ static int pairs_for_device() {
 
 size_t decode_tc_workspace_size(int32_t B) { return dtc::ws_layout(B).total; }
 
-void set_fault_injection(int32_t kind) { dtc::g_inject_fault = kind == 1 ? 1 : 0; }
+void set_fault_injection(int32_t kind) { dtc::g_inject_fault.store(kind == 1 ? 1 : 0, std::memory_order_relaxed); }
 
 size_t prefill_tc_workspace_size(int32_t B, int32_t S) {
   return dtc::ws_layout(static_cast<long long>(B) * S).total;
@@ -1182,7 +1183,7 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   a.part_o = reinterpret_cast<__half*>(wsb + w.o);
   a.o_lat = static_cast<__nv_bfloat16*>(o_lat);
   a.lse = lse;
-  a.fault = g_inject_fault;
+  a.fault = g_inject_fault.load(std::memory_order_relaxed);
   a.block_table = pv.table;
   a.max_blocks = pv.max_blocks;
   a.num_pages = pv.num_pages;

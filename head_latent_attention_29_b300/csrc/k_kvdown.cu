@@ -381,7 +381,10 @@ mla_status launch_kv_down(const mla_cache& c, const void* h, const void* w, cons
   const int R = c.d_c + c.d_r;
   if (R > kMaxR || (c.d_c & 1) != 0) return MLA_ERR_UNSUPPORTED;
   Plan p = plan(T, d_model, R, c.dtype);
-  if (p.tc && !(aligned16(h) && aligned16(w))) p = Plan{0, 0, 0, 1, 0, false};  // the TMA maps need 16-byte bases
+  // bf16 projects on the tensor cores only: a shape or an alignment outside that
+  // kernel is an error, never a silent switch to the CUDA-core projection
+  if (c.dtype == MLA_BF16 && !p.tc) return MLA_ERR_UNSUPPORTED;
+  if (p.tc && !(aligned16(h) && aligned16(w))) return MLA_ERR_INVALID_ARG;  // the TMA maps need 16-byte bases
   const size_t need = static_cast<size_t>(p.splits) * T * R * sizeof(float);
   if (ws == nullptr || ws_bytes < need || !aligned16(ws)) return MLA_ERR_WORKSPACE;
   float* wsf = static_cast<float*>(ws);
@@ -405,13 +408,8 @@ mla_status launch_kv_down(const mla_cache& c, const void* h, const void* w, cons
       return MLA_ERR_CUDA;
   } else {
     const dim3 grid((R + kThreads - 1) / kThreads, (T + kSimtTokens - 1) / kSimtTokens);
-    cudaError_t e;
-    if (c.dtype == MLA_BF16)
-      e = launch_pdl(kvd_simt_kernel<__nv_bfloat16>, grid, dim3(kThreads), 0, s,
-                     static_cast<const __nv_bfloat16*>(h), static_cast<const __nv_bfloat16*>(w), T, d_model, R, wsf);
-    else
-      e = launch_pdl(kvd_simt_kernel<float>, grid, dim3(kThreads), 0, s, static_cast<const float*>(h),
-                     static_cast<const float*>(w), T, d_model, R, wsf);
+    const cudaError_t e = launch_pdl(kvd_simt_kernel<float>, grid, dim3(kThreads), 0, s, static_cast<const float*>(h),
+                                     static_cast<const float*>(w), T, d_model, R, wsf);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
   }
   const PageMap pages = {block_table, max_blocks, num_pages};

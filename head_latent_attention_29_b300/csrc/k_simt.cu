@@ -159,21 +159,14 @@ __global__ void __launch_bounds__(128) absorb_q_kernel(const T* __restrict__ q_n
 mla_status launch_absorb_q(const void* q_nope, const void* q_rope, const int32_t* q_pos, const void* w_uk,
                            void* q_cat, int32_t B, int32_t H, int32_t d_k, int32_t d_c, int32_t d_r,
                            int32_t dtype, float rope_base, cudaStream_t s) {
+  if (dtype != MLA_F32) return MLA_ERR_UNSUPPORTED;  // bf16 runs on the tensor cores only
   dim3 grid((d_c + 127) / 128, H);
   const size_t smem = sizeof(float) * kAbsorbBatch * d_k;
-  if (dtype == MLA_BF16) {
-    auto k = absorb_q_kernel<__nv_bfloat16>;
-    ensure_smem_limit(reinterpret_cast<const void*>(k), smem);
-    k<<<grid, 128, smem, s>>>(static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(q_rope),
-                              q_pos, static_cast<const __nv_bfloat16*>(w_uk), static_cast<__nv_bfloat16*>(q_cat),
-                              B, H, d_k, d_c, d_r, rope_table(d_r, rope_base));
-  } else {
-    auto k = absorb_q_kernel<float>;
-    ensure_smem_limit(reinterpret_cast<const void*>(k), smem);
-    k<<<grid, 128, smem, s>>>(static_cast<const float*>(q_nope), static_cast<const float*>(q_rope), q_pos,
-                              static_cast<const float*>(w_uk), static_cast<float*>(q_cat), B, H, d_k, d_c, d_r,
-                              rope_table(d_r, rope_base));
-  }
+  auto k = absorb_q_kernel<float>;
+  ensure_smem_limit(reinterpret_cast<const void*>(k), smem);
+  k<<<grid, 128, smem, s>>>(static_cast<const float*>(q_nope), static_cast<const float*>(q_rope), q_pos,
+                            static_cast<const float*>(w_uk), static_cast<float*>(q_cat), B, H, d_k, d_c, d_r,
+                            rope_table(d_r, rope_base));
   return cuda_status(cudaGetLastError());
 }
 
@@ -222,19 +215,13 @@ __global__ void __launch_bounds__(256) out_up_kernel(const T* __restrict__ o_lat
 
 mla_status launch_out_up(const void* o_lat, const void* w_uv, void* o, int32_t B, int32_t H, int32_t d_c,
                          int32_t d_v, int32_t dtype, cudaStream_t s) {
+  if (dtype != MLA_F32) return MLA_ERR_UNSUPPORTED;  // bf16 runs on the tensor cores only
   dim3 grid((d_v + 7) / 8, H);
   const size_t smem = sizeof(float) * kOutBatch * d_c;
-  if (dtype == MLA_BF16) {
-    auto k = out_up_kernel<__nv_bfloat16>;
-    ensure_smem_limit(reinterpret_cast<const void*>(k), smem);
-    k<<<grid, 256, smem, s>>>(static_cast<const __nv_bfloat16*>(o_lat), static_cast<const __nv_bfloat16*>(w_uv),
-                              static_cast<__nv_bfloat16*>(o), B, H, d_c, d_v);
-  } else {
-    auto k = out_up_kernel<float>;
-    ensure_smem_limit(reinterpret_cast<const void*>(k), smem);
-    k<<<grid, 256, smem, s>>>(static_cast<const float*>(o_lat), static_cast<const float*>(w_uv),
-                              static_cast<float*>(o), B, H, d_c, d_v);
-  }
+  auto k = out_up_kernel<float>;
+  ensure_smem_limit(reinterpret_cast<const void*>(k), smem);
+  k<<<grid, 256, smem, s>>>(static_cast<const float*>(o_lat), static_cast<const float*>(w_uv),
+                            static_cast<float*>(o), B, H, d_c, d_v);
   return cuda_status(cudaGetLastError());
 }
 
@@ -294,15 +281,10 @@ __global__ void __launch_bounds__(256) gate_kernel(const T* __restrict__ hin, co
 
 mla_status launch_gate(const void* h, const void* w_g, void* o, int32_t B, int32_t d_model, int32_t width,
                        int32_t dtype, cudaStream_t s) {
+  if (dtype != MLA_F32) return MLA_ERR_UNSUPPORTED;  // bf16 runs on the tensor cores only
   const int grid = (width + 31) / 32;
-  if (dtype == MLA_BF16) {
-    gate_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(h),
-                                                    static_cast<const __nv_bfloat16*>(w_g),
-                                                    static_cast<__nv_bfloat16*>(o), B, d_model, width);
-  } else {
-    gate_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(h), static_cast<const float*>(w_g),
-                                            static_cast<float*>(o), B, d_model, width);
-  }
+  gate_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(h), static_cast<const float*>(w_g),
+                                          static_cast<float*>(o), B, d_model, width);
   return cuda_status(cudaGetLastError());
 }
 

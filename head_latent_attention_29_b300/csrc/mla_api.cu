@@ -97,6 +97,13 @@ extern "C" {
 
 MLA_API int32_t mla_abi_version(void) { return 1; }
 
+#ifndef MLA_SOURCE_HASH
+#define MLA_SOURCE_HASH "unknown"
+#endif
+// Tagged so that the build can read it from the library file without loading it.
+static const char kSourceHashTag[] = "MLA-SOURCE-HASH:" MLA_SOURCE_HASH;
+MLA_API const char* mla_build_source_hash(void) { return kSourceHashTag + 16; }
+
 MLA_API const char* mla_status_string(mla_status st) {
   switch (st) {
     case MLA_OK: return "MLA_OK";
@@ -135,10 +142,15 @@ MLA_API mla_status mla_absorb_q(const void* q_nope, const void* q_rope, const in
   if (d_r > 0 && q_rope == nullptr) return MLA_ERR_INVALID_ARG;
   if (!(rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
   if (d_r > 128) return MLA_ERR_UNSUPPORTED;
-  if (dtype == MLA_BF16 && mla::headgemm_absorb_supported(d_k, d_c, d_r) && aligned16(q_nope) && aligned16(w_uk) &&
-      aligned16(q_cat) && (d_r == 0 || aligned4(q_rope)))
+  if (dtype == MLA_BF16) {
+    // bf16 runs on the tensor cores only: a shape or an alignment outside that
+    // kernel is an error, never a silent switch to the CUDA-core kernel
+    if (!mla::headgemm_absorb_supported(d_k, d_c, d_r)) return MLA_ERR_UNSUPPORTED;
+    if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q_cat) || (d_r > 0 && !aligned4(q_rope)))
+      return MLA_ERR_INVALID_ARG;
     return mla::launch_absorb_q_tc(q_nope, q_rope, q_pos, w_uk, q_cat, B, H, d_k, d_c, d_r, rope_base,
                                    as_stream(stream));
+  }
   if (static_cast<size_t>(32) * d_k * sizeof(float) > 200 * 1024) return MLA_ERR_UNSUPPORTED;
   return mla::launch_absorb_q(q_nope, q_rope, q_pos, w_uk, q_cat, B, H, d_k, d_c, d_r, dtype, rope_base,
                               as_stream(stream));
@@ -205,9 +217,11 @@ MLA_API mla_status mla_out_up(const void* o_lat, const void* w_uv, void* o, int3
   if (!valid_dtype(dtype)) return MLA_ERR_INVALID_ARG;
   if (o_lat == nullptr || w_uv == nullptr || o == nullptr) return MLA_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || d_c <= 0 || d_v <= 0) return MLA_ERR_INVALID_ARG;
-  if (dtype == MLA_BF16 && mla::headgemm_out_up_supported(d_c, d_v) && aligned16(o_lat) && aligned16(w_uv) &&
-      aligned16(o))
+  if (dtype == MLA_BF16) {  // tensor cores only (no silent CUDA-core fallback)
+    if (!mla::headgemm_out_up_supported(d_c, d_v)) return MLA_ERR_UNSUPPORTED;
+    if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(o)) return MLA_ERR_INVALID_ARG;
     return mla::launch_out_up_tc(o_lat, w_uv, o, B, H, d_c, d_v, as_stream(stream));
+  }
   if (d_c > 1024) return MLA_ERR_UNSUPPORTED;
   return mla::launch_out_up(o_lat, w_uv, o, B, H, d_c, d_v, dtype, as_stream(stream));
 }
@@ -218,9 +232,11 @@ MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, 
   if (!valid_dtype(dtype)) return MLA_ERR_INVALID_ARG;
   if (h == nullptr || w_g == nullptr || o == nullptr) return MLA_ERR_INVALID_ARG;
   if (B <= 0 || d_model <= 0 || width <= 0) return MLA_ERR_INVALID_ARG;
-  if (dtype == MLA_BF16 && mla::headgemm_gate_supported(d_model, width) && aligned16(h) && aligned16(w_g) &&
-      aligned16(o))
+  if (dtype == MLA_BF16) {  // tensor cores only (no silent CUDA-core fallback)
+    if (!mla::headgemm_gate_supported(d_model, width)) return MLA_ERR_UNSUPPORTED;
+    if (!aligned16(h) || !aligned16(w_g) || !aligned16(o)) return MLA_ERR_INVALID_ARG;
     return mla::launch_gate_tc(h, w_g, o, B, d_model, width, as_stream(stream));
+  }
   return mla::launch_gate(h, w_g, o, B, d_model, width, dtype, as_stream(stream));
 }
 

@@ -1,9 +1,9 @@
 // Allocation-free decode attention.
 //
 // Some callers cannot allocate device memory at the moment they need attention:
-// code running inside a CUDA-graph replay or a capture that forbids new
-// allocations, custom allocators that are not reentrant, or embedders that only
-// own input/output buffers handed to them by a host framework.  For them
+// code running under a custom allocator that must not be re-entered from there,
+// runtimes whose device memory is fixed when they start, or embedders that only
+// own the input/output buffers handed to them by a host framework.  For them
 // mla_decode_attn_noalloc runs the same tensor-core decode kernels as
 // mla_decode_attn, but takes its split-KV scratch from a buffer that is part of
 // the library image itself (a file-scope device array), so the call allocates

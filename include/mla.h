@@ -108,6 +108,14 @@ typedef struct {
 /* Version of this ABI (bumped on any incompatible change). */
 MLA_API int32_t mla_abi_version(void);
 
+/*
+ * mla_build_source_hash -- a short hash of the sources this library was built
+ * from (set by the build; "unknown" when built without it).  The Python binding
+ * compares it with the sources beside it and refuses a library built from others.
+ * (No counterpart on the pages: a build check.)
+ */
+MLA_API const char* mla_build_source_hash(void);
+
 /* Human-readable name of a status code (static string, never NULL). */
 MLA_API const char* mla_status_string(mla_status status);
 
@@ -138,6 +146,10 @@ MLA_API mla_status mla_cache_append(const mla_cache* cache, const void* c_kv, co
  *   q_nope [B, H, d_k]; q_rope [B, H, d_r] (NULL iff d_r == 0);
  *   q_pos [B] int32 (query position, normally length-1); W_UK [H, d_k, d_c];
  *   q_cat [B, H, d_c + d_r] (output).
+ *   bf16: tensor-core kernel only; needs d_k % 64 == 0, d_c % 128 == 0,
+ *   d_r <= 128 and (d_c + d_r) % 8 == 0 (MLA_ERR_UNSUPPORTED otherwise), and
+ *   16-byte aligned q_nope, W_UK, q_cat and 4-byte aligned q_rope
+ *   (MLA_ERR_INVALID_ARG otherwise).  f32: CUDA-core kernel, d_k <= 1600.
  */
 MLA_API mla_status mla_absorb_q(const void* q_nope, const void* q_rope, const int32_t* q_pos,
                                 const void* w_uk, void* q_cat, int32_t B, int32_t H, int32_t d_k,
@@ -223,6 +235,9 @@ MLA_API mla_status mla_prefill_attn(const void* q_cat, const mla_cache* cache, c
  *   (0539edu.com section 3.1, attn v = (attn c_KV) W_UV; weight view [h, d_v, d_c]
  *   of section 3.2).  o_lat [B, H, d_c]; W_UV [H, d_v, d_c]; o [B, H, d_v].
  *   fp32 arithmetic, dtype storage.
+ *   bf16: tensor-core kernel only; needs d_c % 64 == 0 and d_v % 128 == 0
+ *   (MLA_ERR_UNSUPPORTED otherwise) and 16-byte aligned o_lat, W_UV and o
+ *   (MLA_ERR_INVALID_ARG otherwise).  f32: CUDA-core kernel, d_c <= 1024.
  */
 MLA_API mla_status mla_out_up(const void* o_lat, const void* w_uv, void* o, int32_t B, int32_t H,
                               int32_t d_c, int32_t d_v, int32_t dtype, void* stream);
@@ -233,6 +248,9 @@ MLA_API mla_status mla_out_up(const void* o_lat, const void* w_uv, void* o, int3
  *   (tahou.com sections 2.6 and 3.2: one gate value per channel of the
  *   concatenated v-width output, computed from the token's own input).
  *   h [B, d_model]; W_g [d_model, width]; o [B, width] (read and written).
+ *   bf16: tensor-core kernel only; needs d_model % 64 == 0 and width % 128 == 0
+ *   (MLA_ERR_UNSUPPORTED otherwise) and 16-byte aligned h, W_g and o
+ *   (MLA_ERR_INVALID_ARG otherwise).  f32: CUDA-core kernel, any shape.
  */
 MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, int32_t d_model,
                             int32_t width, int32_t dtype, void* stream);
@@ -294,9 +312,10 @@ MLA_API size_t mla_kv_down_workspace_size(int32_t T, int32_t d_model, int32_t d_
  *   workspace device scratch of mla_kv_down_workspace_size(T, d_model, d_c, d_r,
  *            dtype) bytes, 16-byte aligned (MLA_ERR_WORKSPACE otherwise).
  *   Limits: d_c even, d_c + d_r <= 1024 (MLA_ERR_UNSUPPORTED otherwise).  bf16
- *   caches with d_model % 64 == 0, (d_c + d_r) % 8 == 0 and 16-byte aligned h and
- *   w_dkvr take the tensor-core projection; other shapes and fp32 take a CUDA-core
- *   one.  gamma is always applied: pass ones for an RMSNorm without gain.
+ *   caches project on the tensor cores only: d_model % 64 == 0 and
+ *   (d_c + d_r) % 8 == 0 (MLA_ERR_UNSUPPORTED otherwise), 16-byte aligned h and
+ *   w_dkvr (MLA_ERR_INVALID_ARG otherwise).  fp32 caches take a CUDA-core
+ *   projection.  gamma is always applied: pass ones for an RMSNorm without gain.
  */
 MLA_API mla_status mla_kv_down_append(const mla_cache* cache, const void* h, const void* w_dkvr,
                                       const void* gamma, float eps, const int32_t* seq_idx,
@@ -313,10 +332,10 @@ MLA_API mla_status mla_kv_down_append_paged(const mla_paged_cache* cache, const 
 /*
  * mla_decode_attn_noalloc -- mla_decode_attn for callers that cannot allocate.
  *   (No counterpart on the pages this library restates: it is a deployment aid.)
- *   Some callers cannot hand the library a workspace: code that runs while new
- *   device allocations are not allowed (inside graph capture or replay, or under an
- *   allocator that cannot be re-entered) or embedders that only own the input and
- *   output buffers.  This entry point computes exactly what mla_decode_attn does,
+ *   Some callers cannot hand the library a workspace: code running under an
+ *   allocator that must not be re-entered from where attention is called, runtimes
+ *   whose device memory is fixed when they start, or embedders that only own the
+ *   input and output buffers a host framework gives them.  This entry point computes exactly what mla_decode_attn does,
  *   with the same kernels, but takes the split-KV scratch from a buffer built into
  *   the library (about 22 MB per GPU that loads the library, held until the
  *   process exits), so it allocates nothing.
@@ -349,8 +368,8 @@ MLA_API mla_status mla_get_device_error(uint32_t* detail);
  *   waits on those loads run out after their bound (about one second): the call
  *   records MLA_ERR_DEVICE_TIMEOUT in the device error word, its outputs are
  *   undefined, and the CUDA context stays usable.  kind = 0 switches it off.
- *   Nothing faults, traps or hangs.  Process-wide setting, not synchronised
- *   between host threads; for tests only.  Returns MLA_ERR_INVALID_ARG for any
+ *   Nothing faults, traps or hangs.  Process-wide setting (an atomic switch that
+ *   every later launch on any host thread or device reads); for tests only.  Returns MLA_ERR_INVALID_ARG for any
  *   other kind.
  */
 MLA_API mla_status mla_debug_inject_fault(int32_t kind);

@@ -87,11 +87,54 @@ def test_unsupported_bf16_shapes_are_refused(libmla):
     assert libmla.mla_decode_attn(p, ctypes.byref(c), p, 256, 0.1, p, 1 << 20, p, None, None) == UNSUPPORTED
 
 
+def test_bf16_head_gemms_refuse_what_the_tensor_cores_do_not_take(libmla):
+    # bf16 absorb / out-up / gate / kv_down run on the tensor-core kernels only: a
+    # shape those kernels do not take is MLA_ERR_UNSUPPORTED and a misaligned
+    # pointer MLA_ERR_INVALID_ARG, decided on the host before anything launches
+    # (no silent switch to a CUDA-core kernel)
+    import head_latent_attention_29_b300 as mla
+    INVALID, UNSUPPORTED = 1, 2
+    a, odd = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10008)
+    out_up = libmla.mla_out_up
+    assert out_up(a, a, a, 32, 128, 512, 96, 0, None) == UNSUPPORTED     # d_v % 128
+    assert out_up(a, a, a, 32, 128, 500, 128, 0, None) == UNSUPPORTED    # d_c % 64
+    assert out_up(odd, a, a, 32, 128, 512, 128, 0, None) == INVALID      # o_lat not 16-byte aligned
+    assert out_up(a, odd, a, 32, 128, 512, 128, 0, None) == INVALID
+    assert out_up(a, a, odd, 32, 128, 512, 128, 0, None) == INVALID
+    absorb = libmla.mla_absorb_q
+    assert absorb(a, a, a, a, a, 32, 128, 100, 512, 64, 0, 1e4, None) == UNSUPPORTED   # d_k % 64
+    assert absorb(a, a, a, a, a, 32, 128, 128, 500, 64, 0, 1e4, None) == UNSUPPORTED   # d_c % 128
+    assert absorb(odd, a, a, a, a, 32, 128, 128, 512, 64, 0, 1e4, None) == INVALID
+    assert absorb(a, a, a, a, odd, 32, 128, 128, 512, 64, 0, 1e4, None) == INVALID
+    assert absorb(a, ctypes.c_void_p(0x10002), a, a, a, 32, 128, 128, 512, 64, 0, 1e4, None) == INVALID
+    gate = libmla.mla_gate
+    assert gate(a, a, a, 3, 100, 256, 0, None) == UNSUPPORTED            # d_model % 64
+    assert gate(a, a, a, 3, 128, 200, 0, None) == UNSUPPORTED            # width % 128
+    assert gate(odd, a, a, 3, 128, 256, 0, None) == INVALID
+    c = mla._Cache(0x1000, 0, 4, 300, 512, 64, 0, 576)
+    kvd = libmla.mla_kv_down_append
+    assert kvd(ctypes.byref(c), a, a, a, 1e-6, a, a, 4, 200, 1e4, a, 1 << 20, None) == UNSUPPORTED  # d_model % 64
+    assert kvd(ctypes.byref(c), odd, a, a, 1e-6, a, a, 4, 256, 1e4, a, 1 << 20, None) == INVALID
+
+
 def test_product_path_fails_loudly_without_the_library(tmp_path, monkeypatch):
     import head_latent_attention_29_b300 as mla
     monkeypatch.setattr(mla, "_lib_handle", None)
     monkeypatch.setattr(mla, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
+        mla.lib()
+
+
+def test_library_built_from_other_sources_is_refused(libmla, monkeypatch):
+    # the build compiles a hash of its sources into the library; the binding
+    # compares it with the sources beside it, whatever the files' times
+    import head_latent_attention_29_b300 as mla
+    from head_latent_attention_29_b300 import _build
+    assert libmla.mla_build_source_hash().decode() == _build.source_hash() == _build.built_hash()
+    assert not _build.needs_build()
+    monkeypatch.setattr(mla, "_lib_handle", None)
+    monkeypatch.setattr(_build, "source_hash", lambda: "0123456789abcdef")
+    with pytest.raises(ImportError, match="built from other sources"):
         mla.lib()
 
 

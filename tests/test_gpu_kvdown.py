@@ -89,12 +89,14 @@ def test_kv_down_fp32_tiny_shapes(mla):
     assert _untouched_nan(cache, seq, pos, d_c + d_r)
 
 
-def test_kv_down_bf16_cuda_core_path(mla):
-    # d_model = 200 is not a multiple of 64: the bf16 CUDA-core projection
+def test_kv_down_bf16_shape_outside_the_tensor_cores_is_refused(mla):
+    # d_model = 200 is not a multiple of 64: bf16 has no CUDA-core projection to
+    # fall back to, so the call is refused and the cache stays untouched
     d_c, d_r, eps = 512, 64, 0.0
     mat, seq, pos = _inputs(9, 200, d_c, d_r, "bf16", seed=8)
-    cache = _run(mla, mat, seq, pos, "bf16", d_c, d_r, 4, 300, eps)
-    check_bf16(_written(cache, seq, pos, d_c + d_r), _oracle(mat, "bf16", d_c, pos, eps), "kv_down bf16 simt")
+    with pytest.raises(mla.MlaError) as e:
+        _run(mla, mat, seq, pos, "bf16", d_c, d_r, 4, 300, eps)
+    assert e.value.status == 2  # MLA_ERR_UNSUPPORTED
 
 
 def test_kv_down_deterministic_and_paged_equal(mla):

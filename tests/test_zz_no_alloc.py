@@ -1,17 +1,21 @@
 """The allocation-free decode entry point gives the same attention as the
 workspace entry point.
 
-mla_decode_attn_noalloc serves callers that cannot allocate device memory when
-they run attention (graph capture/replay, non-reentrant allocators, embedders
-that only own their input and output buffers); it takes its scratch from a buffer
-built into the library.  This file is collected last on purpose."""
+mla_decode_attn_noalloc is for callers that cannot hand the library device
+memory when they run attention: code under an allocator that must not be
+re-entered from that point, runtimes whose device memory is fixed at start-up,
+or embedders that only own the input and output buffers.  It runs the same
+kernels as mla_decode_attn with their scratch taken from a buffer built into the
+library, so on the same inputs its outputs must be bit-identical.  This file is
+collected last on purpose: a run that stops at the first failure has then run
+every other test."""
 import math
 
 import numpy as np
 import pytest
 import torch
 
-from tests._cases import TOL_BF16_MAX_ABS, TOL_BF16_REL_L2, direct_decode_inputs, rel_l2, upload_direct
+from tests._cases import check_bf16, direct_decode_inputs, oracle_direct, upload_direct
 
 pytestmark = pytest.mark.gpu
 
@@ -25,24 +29,31 @@ def mla():
 
 def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(mla):
     scale = 1.0 / math.sqrt(192)
-    # two calls in a row on different batches: the second must not see the first's scratch
-    for seed, lens in [(31, [4096, 100, 65, 2000, 1]), (32, [777, 3000, 64])]:
+    # two calls in a row on different batches: the second must not see the first's
+    # scratch (the lengths differ, so the run plans and the cut problems differ)
+    for k, (seed, lens) in enumerate([(31, [4096, 100, 65, 2000, 1]), (32, [777, 3000, 64, 5000] * 8)]):
         lens = np.asarray(lens, dtype=np.int32)
         q_bits, rows = direct_decode_inputs(seed, lens, 128, 512, 64)
         q, cache = upload_direct(mla, q_bits, rows, 512, 64, int(lens.max()))
         seq_lens = torch.from_numpy(lens).cuda()
-        ref_o, ref_lse = mla.decode_attn(q, cache, seq_lens, scale)
-        out = torch.empty_like(ref_o)
-        lse = torch.empty_like(ref_lse)
+        out = torch.empty((len(lens), 128, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((len(lens), 128), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        before = torch.cuda.memory_allocated()
         mla.decode_attn_noalloc(q, cache, seq_lens, scale, out, lse)
         torch.cuda.synchronize()
+        assert torch.cuda.memory_allocated() == before  # the binding allocates nothing either
         st, word = mla.get_device_error()
         assert st == 0, f"device error word {word:#x}"
-        a = out.float().cpu().numpy()
-        b = ref_o.float().cpu().numpy()
-        assert np.all(np.isfinite(a))
-        assert float(np.max(np.abs(a - b))) <= TOL_BF16_MAX_ABS and rel_l2(a, b) <= TOL_BF16_REL_L2
-        np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), atol=2e-2, rtol=1e-3)
+        ref_o, ref_lse = mla.decode_attn(q, cache, seq_lens, scale)
+        torch.cuda.synchronize()
+        # same kernels, same inputs: the same bits
+        assert torch.equal(out.view(torch.int16), ref_o.view(torch.int16)), f"call {k}: o_lat bits differ"
+        assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32)), f"call {k}: lse bits differ"
+        if k == 0:
+            o_ref, lse_ref = oracle_direct(q_bits, rows, 512, scale)
+            check_bf16(out.float().cpu().numpy(), o_ref, "no-alloc o_lat vs oracle")
+            np.testing.assert_allclose(lse.cpu().numpy(), lse_ref, atol=2e-2, rtol=1e-3)
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch(mla):
@@ -53,3 +64,17 @@ def test_noalloc_rejects_batches_beyond_its_scratch(mla):
     with pytest.raises(mla.MlaError) as e:
         mla.decode_attn_noalloc(q, cache, seq_lens, 0.07, out)
     assert e.value.status == 5  # MLA_ERR_WORKSPACE
+
+
+def test_noalloc_checks_caller_buffers_before_launch(mla):
+    cache = mla.LatentCache(4, 64, 512, 64)
+    q = torch.zeros((4, 128, 576), dtype=torch.bfloat16, device="cuda")
+    seq_lens = torch.ones(4, dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):   # output one sequence short
+        mla.decode_attn_noalloc(q, cache, seq_lens, 0.07, torch.empty((3, 128, 512), dtype=torch.bfloat16,
+                                                                      device="cuda"))
+    out = torch.empty((4, 128, 512), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):   # lse of the wrong shape
+        mla.decode_attn_noalloc(q, cache, seq_lens, 0.07, out, torch.empty((4, 64), device="cuda"))
+    with pytest.raises(ValueError):   # q_cat of another batch
+        mla.decode_attn_noalloc(q[:2], cache, seq_lens, 0.07, out)
