@@ -192,6 +192,41 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- workload
+ATTN_WARMUP = 20
+ATTN_REPS = 200
+
+
+def time_attention(replay, stream, device, launches_per_replay: int = 10):
+    """Median per-launch time (us) of the attention op over ATTN_REPS graph replays
+    after ATTN_WARMUP, each replay bracketed by CUDA events on the launching stream;
+    also the spread and the SM clock seen during the replays, with the median time
+    scaled to the maximum SM clock (time x median MHz / max MHz)."""
+    import torch
+    for _ in range(ATTN_WARMUP):
+        replay()
+    torch.cuda.synchronize(device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(ATTN_REPS + 1)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize(device)
+        ev[0].record(stream)
+        for i in range(ATTN_REPS):
+            replay()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(device)
+    per = sorted(ev[i].elapsed_time(ev[i + 1]) * 1e3 / launches_per_replay for i in range(ATTN_REPS))
+    med = statistics.median(per)
+    ck = clk.summary()
+    at_max = None
+    if ck.get("sm_mhz") and ck.get("sm_max_mhz"):
+        at_max = round(med * ck["sm_mhz"] / ck["sm_max_mhz"], 3)
+    q = lambda f: round(per[min(len(per) - 1, int(f * len(per)))], 3)
+    return {"us": med, "timing": {
+        "replays": ATTN_REPS, "launches_per_replay": launches_per_replay, "warmup_replays": ATTN_WARMUP,
+        "median_us": round(med, 3), "mean_us": round(statistics.fmean(per), 3), "min_us": round(per[0], 3),
+        "p10_us": q(0.1), "p90_us": q(0.9), "max_us": round(per[-1], 3),
+        "median_us_at_max_clock": at_max, "clocks": ck}}
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     """The largest value of x over all ranks (the slowest replica sets the job's
     time); no collective for a single process."""
@@ -386,18 +421,11 @@ def run_b300(args, rank, world, device):
     tokens_per_step = wl.B * world
     value = job_throughput(wl.B, world, ms_step * 1e-3)
 
-    # ---- dominant op (attention: split-KV kernel + combine), timed alone on its stream
-    n_rep = max(5, min(args.steps // 10, 200))
-    for _ in range(3):
-        wl.attn_graph.replay()
-    torch.cuda.synchronize(device)
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    for _ in range(n_rep):
-        wl.attn_graph.replay()
-    a1.record(stream)
-    torch.cuda.synchronize(device)
-    attn_us = a0.elapsed_time(a1) * 1e3 / (10 * n_rep)
+    # ---- dominant op (attention: split-KV kernel + combine), timed alone on its stream:
+    # 20 warm-up replays, then ATTN_REPS replays of a ten-launch graph (whatever
+    # --steps is), each bracketed by events; the median replay gives the time
+    attn = time_attention(wl.attn_graph.replay, stream, device)
+    attn_us = attn["us"]
 
     # ---- end to end: pinned inputs in, result out, host waits for every step
     n_e2e = max(20, min(args.steps // 10, 2000))
@@ -458,6 +486,7 @@ def run_b300(args, rank, world, device):
             "roofline_us": round(roof_us, 3), "frac_of_roofline": round(roof_us / attn_us, 4),
             "frac_of_roofline_sustained_tc": (round(max(t_mem, flops_attn / (tc_sust * 1e12)) * 1e6 / attn_us, 4)
                                               if tc_sust else None),
+            "timing": attn["timing"],
         },
         "step_roofline": {
             "bound": "hbm" if step_bytes / (hbm * 1e9) >= step_flops / (tc_burst * 1e12) else "tensor",
@@ -783,76 +812,6 @@ def run_b300_kvdown(args, rank, world, device):
     }
 
 
-def cpu_baseline_kvdown(workload: str, seed: int, budget_s: float = 12.0):
-    """Time the float64 oracle's rows-from-hidden-states step on the host cores for
-    a bounded sample of the workload's tokens (weights widened once: resident state)."""
-    from oracle import mla_oracle as O
-    cfg = dict(W.WORKLOADS[workload])
-    d_c = cfg["d_c"]
-    n = min(cfg["T"], 32)
-    h, w_dkv, w_kr, gamma = W.kv_down_inputs(dict(cfg, T=n), seed)
-    wd = lambda x: W.widen(W.as_dtype(x, "bf16"), "bf16")
-    h, w, g = wd(h), wd(np.concatenate([w_dkv, w_kr], axis=1)), wd(gamma)
-    _, pos, _, _ = kvdown_rows_slots(cfg)
-    pos = pos[:n]
-    done = 0
-    t0 = time.perf_counter()
-    while True:
-        O.kv_down_rows(h, w[:, :d_c], w[:, d_c:], g, cfg["eps"], pos, cfg["rope_base"])
-        done += n
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    try:
-        from threadpoolctl import threadpool_info
-        threads = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-    except Exception:  # pragma: no cover
-        threads = []
-    return {"value": round(done / el, 3), "unit": "tokens/s", "cores": max(threads) if threads else 1,
-            "kind": "oracle", "host_cpus": os.cpu_count(), "cpu_model": _cpu_model(),
-            "sample": f"{done} tokens in batches of {n} (float64 numpy), {el:.1f} s"}
-
-
-_PREFILL_ORACLE_STATE = {}
-
-
-def cpu_baseline_prefill(workload: str, seed: int, budget_s: float = 12.0):
-    """Time the float64 oracle's prompt step per query row (absorb at the row's
-    position, attention over rows 0..i, out_up) for query rows spread evenly over
-    the prompt of sequence 0; the per-token cost of an even spread is the mean
-    cost of the whole causal prompt."""
-    from oracle import mla_oracle as O
-    cfg = dict(W.WORKLOADS[workload])
-    S, base = cfg["S"], cfg["rope_base"]
-    key = (workload, seed)
-    if key not in _PREFILL_ORACLE_STATE:  # inputs and the cache rows are resident state, not step work
-        c, k, q_nope, q_r = (W.widen(x, "bf16") for x in prefill_draws(cfg, seed, 0))
-        w_uk, w_uv = (W.widen(W.as_dtype(w, "bf16"), "bf16") for w in W.up_weights(cfg, seed))
-        _PREFILL_ORACLE_STATE[key] = (O.cache_rows(c, k, np.arange(S), base), q_nope, q_r, w_uk, w_uv)
-    rows, q_nope, q_r, w_uk, w_uv = _PREFILL_ORACLE_STATE[key]
-    order = np.random.default_rng(seed).permutation(S)
-    done = 0
-    t0 = time.perf_counter()
-    while done < S:
-        i = int(order[done])
-        q_cat = O.absorb_q(q_nope[i], q_r[i], i, w_uk, base)
-        o_lat, _ = O.decode_absorbed(q_cat, rows[: i + 1], cfg["d_c"], cfg["scale"])
-        O.out_up(o_lat, w_uv)
-        done += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    try:
-        from threadpoolctl import threadpool_info
-        threads = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-    except Exception:  # pragma: no cover
-        threads = []
-    return {"value": round(done / el, 3), "unit": "tokens/s", "cores": max(threads) if threads else 1,
-            "kind": "oracle", "host_cpus": os.cpu_count(), "cpu_model": _cpu_model(),
-            "sample": f"{done} prompt query rows of sequence 0 at random positions of 0..{S - 1} "
-                      f"(causal prefix each), float64 numpy, {el:.1f} s"}
-
-
 def _ncu_traffic(workload):
     """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, if any."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -893,45 +852,200 @@ def _cpu_model() -> str:
     return platform.processor() or "unknown"
 
 
-def cpu_baseline(workload: str, seed: int, budget_s: float = 12.0):
-    """Time the float64 oracle's decode step (absorb_q, attention over the prebuilt
-    cache rows, out_up) on the host cores for a bounded sample of sequences."""
-    from oracle import mla_oracle as O
+# The oracle's step runs on every host core this process may use: one spawned
+# worker process per core (spawn, not fork: the parent holds a CUDA context), BLAS
+# held to one thread in each, the sample's inputs built once inside the workers as
+# resident state.  All workers start together and run for the same wall-clock
+# window; the rate is the tokens of all of them over that window.
+ORACLE_ROW_CAP = 1 << 20  # cached rows a decode sample may hold in all (float64 rows: ~4.8 GB)
+
+
+def _host_cores() -> int:
     try:
-        from threadpoolctl import threadpool_info
-    except Exception:  # pragma: no cover
-        threadpool_info = lambda: []  # noqa: E731
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _oracle_sample(kind: str, workload: str, seed: int):
+    """(units of work, description) of the bounded sample the oracle is timed on."""
     cfg = dict(W.WORKLOADS[workload])
-    lens = W.seq_lens(cfg, seed)
-    q_nope, q_r = W.query(cfg, seed)
-    w_uk, w_uv = W.up_weights(cfg, seed)
-    wd = lambda x: W.widen(W.as_dtype(x, cfg["dtype"]), cfg["dtype"])
-    w_uk, w_uv = wd(w_uk), wd(w_uv)
-    q_nope, q_r = wd(q_nope[:, 0]), wd(q_r[:, 0])
-    base = cfg.get("rope_base", 1e4)
-    # prebuilt rows for a few sequences (the cache is resident state, not step work)
-    sample = list(range(min(4, cfg["B"])))
-    rows = {}
-    for b in sample:
-        c, k = W.latent_rows(cfg, seed, b, int(lens[b]))
-        rows[b] = O.cache_rows(wd(c), wd(k), np.arange(int(lens[b])), base)
-    done = 0
-    t0 = time.perf_counter()
+    if kind == "decode":
+        lens = W.seq_lens(cfg, seed)
+        k, rows = 0, 0
+        while k < cfg["B"] and (k == 0 or rows + int(lens[k]) <= ORACLE_ROW_CAP):
+            rows += int(lens[k])
+            k += 1
+        return list(range(k)), (f"decode steps of sequences 0..{k - 1} of {cfg['B']} "
+                                f"({rows} cached rows, N={int(lens[:k].min())}..{int(lens[:k].max())})")
+    if kind == "prefill":
+        S = cfg["S"]
+        order = [int(i) for i in np.random.default_rng(seed).permutation(S)]
+        return order, (f"prompt query rows of sequence 0 at random positions of 0..{S - 1} "
+                       "(absorb at the row's position, causal prefix, W_UV)")
+    n = min(cfg["T"], 32)
+    return [n], f"batches of {n} tokens (projection, RMSNorm, RoPE)"
+
+
+def _oracle_units(kind: str, workload: str, seed: int, mine):
+    """Closures, one per unit of this worker's share; each runs the oracle's step on
+    its unit and returns the tokens it produced."""
+    from oracle import mla_oracle as O
+    cfg = dict(W.WORKLOADS[workload])
+    if kind == "decode":
+        lens = W.seq_lens(cfg, seed)
+        q_nope, q_r = W.query(cfg, seed)
+        w_uk, w_uv = W.up_weights(cfg, seed)
+        wd = lambda x: W.widen(W.as_dtype(x, cfg["dtype"]), cfg["dtype"])
+        w_uk, w_uv = wd(w_uk), wd(w_uv)
+        q_nope, q_r = wd(q_nope[:, 0]), wd(q_r[:, 0])
+        base = cfg.get("rope_base", 1e4)
+        units = []
+        for b in mine:
+            n = int(lens[b])
+            c, k = W.latent_rows(cfg, seed, b, n)
+            rows = O.cache_rows(wd(c), wd(k), np.arange(n), base)
+
+            def step(b=b, n=n, rows=rows):
+                q_cat = O.absorb_q(q_nope[b], q_r[b], n - 1, w_uk, base)
+                o_lat, _ = O.decode_absorbed(q_cat, rows, cfg["d_c"], cfg["scale"])
+                O.out_up(o_lat, w_uv)
+                return 1
+            units.append(step)
+        return units
+    if kind == "prefill":
+        S, base = cfg["S"], cfg["rope_base"]
+        c, k, q_nope, q_r = prefill_draws(cfg, seed, 0)
+        rows = O.cache_rows(W.widen(c, "bf16"), W.widen(k, "bf16"), np.arange(S), base)
+        sel = np.asarray(mine, dtype=np.int64)
+        qn, qr = W.widen(q_nope[sel], "bf16"), W.widen(q_r[sel], "bf16")
+        del q_nope, q_r
+        w_uk, w_uv = (W.widen(W.as_dtype(w, "bf16"), "bf16") for w in W.up_weights(cfg, seed))
+        units = []
+        for j, i in enumerate(mine):
+            def step(j=j, i=i):
+                q_cat = O.absorb_q(qn[j], qr[j], i, w_uk, base)
+                o_lat, _ = O.decode_absorbed(q_cat, rows[: i + 1], cfg["d_c"], cfg["scale"])
+                O.out_up(o_lat, w_uv)
+                return 1
+            units.append(step)
+        return units
+    n = mine[0]
+    d_c = cfg["d_c"]
+    h, w_dkv, w_kr, gamma = W.kv_down_inputs(dict(cfg, T=n), seed)
+    wd = lambda x: W.widen(W.as_dtype(x, "bf16"), "bf16")
+    h, w, g = wd(h), wd(np.concatenate([w_dkv, w_kr], axis=1)), wd(gamma)
+    pos = kvdown_rows_slots(cfg)[1][:n]
+
+    def step():
+        O.kv_down_rows(h, w[:, :d_c], w[:, d_c:], g, cfg["eps"], pos, cfg["rope_base"])
+        return n
+    return [step]
+
+
+def _oracle_worker(kind, workload, seed, share, n_workers, cmd, res):
+    """One host core of the oracle timing: build this share's units, report ready,
+    then on each ("run", start, seconds) run units round-robin from the common wall
+    clock start until the window has passed."""
+    try:
+        from threadpoolctl import threadpool_info, threadpool_limits
+        threadpool_limits(1)
+        blas = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+    except Exception:  # pragma: no cover
+        blas = [int(os.environ.get("OPENBLAS_NUM_THREADS", "0") or 0)]
+    units_all, _ = _oracle_sample(kind, workload, seed)
+    mine = units_all if kind == "kvdown" else units_all[share::n_workers]
+    units = _oracle_units(kind, workload, seed, mine)
+    res.put(("ready", share, max(blas) if blas else 1))
     while True:
-        for b in sample:
-            q_cat = O.absorb_q(q_nope[b], q_r[b], int(lens[b]) - 1, w_uk, base)
-            o_lat, _ = O.decode_absorbed(q_cat, rows[b], cfg["d_c"], cfg["scale"])
-            O.out_up(o_lat, w_uv)
-            done += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    threads = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-    env = {k: os.environ[k] for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS") if k in os.environ}
-    return {"value": round(done / el, 3), "unit": "tokens/s", "cores": max(threads) if threads else 1,
-            "kind": "oracle", "host_cpus": os.cpu_count(), "cpu_model": _cpu_model(), "thread_env": env,
-            "sample": f"{done} decode steps of sequences {sample} (N={[int(lens[b]) for b in sample]}), "
-                      f"float64 numpy, {el:.1f} s"}
+        m = cmd.get()
+        if m[0] != "run":
+            return
+        _, t_start, seconds = m
+        while time.time() < t_start:
+            time.sleep(0.0005)
+        tokens, i = 0, 0
+        while True:
+            tokens += units[i % len(units)]()
+            i += 1
+            now = time.time()
+            if now >= t_start + seconds:
+                break
+        res.put(("done", share, tokens, now))
+
+
+class OracleHost:
+    """The float64 oracle timed on the host cores (test infrastructure: only the CPU
+    baseline and the reference arm use it)."""
+
+    def __init__(self, kind: str, workload: str, seed: int):
+        import multiprocessing as mp
+        units, self.sample = _oracle_sample(kind, workload, seed)
+        cores = _host_cores()
+        self.n = cores if kind != "decode" else max(1, min(cores, len(units)))
+        self.cores_available = cores
+        ctx = mp.get_context("spawn")
+        self.res = ctx.Queue()
+        self.cmd = [ctx.Queue() for _ in range(self.n)]
+        # BLAS in the workers held to one thread from their first import on
+        saved = {k: os.environ.get(k) for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")}
+        try:
+            for k in saved:
+                os.environ[k] = "1"
+            self.procs = [ctx.Process(target=_oracle_worker, args=(kind, workload, seed, i, self.n, self.cmd[i],
+                                                                    self.res), daemon=True)
+                          for i in range(self.n)]
+            for p in self.procs:
+                p.start()
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        ready = [self.res.get(timeout=900) for _ in range(self.n)]
+        self.blas_threads = max(r[2] for r in ready)
+
+    def measure(self, seconds: float) -> float:
+        t_start = time.time() + 0.05
+        for q in self.cmd:
+            q.put(("run", t_start, float(seconds)))
+        done = [self.res.get(timeout=seconds + 900) for _ in range(self.n)]
+        self.tokens = sum(d[2] for d in done)
+        self.wall = max(d[3] for d in done) - t_start
+        return self.tokens / self.wall
+
+    def record(self, value: float) -> dict:
+        return {"value": round(value, 3), "unit": "tokens/s", "cores": self.n * self.blas_threads,
+                "kind": "oracle", "workers": self.n, "blas_threads_per_worker": self.blas_threads,
+                "host_cpus": os.cpu_count(), "cpus_usable": self.cores_available, "cpu_model": _cpu_model(),
+                "sample": f"{self.sample}, float64 numpy; {self.tokens} tokens in {self.wall:.1f} s of wall time "
+                          f"on {self.n} worker processes"}
+
+    def close(self):
+        for q in self.cmd:
+            q.put(("stop",))
+        for p in self.procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.kill()
+
+
+def _oracle_kind(workload: str) -> str:
+    cfg = W.WORKLOADS[workload]
+    return "kvdown" if "T" in cfg else ("prefill" if "S" in cfg else "decode")
+
+
+def cpu_baseline(workload: str, seed: int, budget_s: float = 12.0):
+    """The float64 oracle's step (decode: absorb_q, attention over the prebuilt cache
+    rows, out_up; prefill: the same per prompt row; rows from hidden states: the
+    projection, norm and rotation) on the host cores for a bounded sample."""
+    host = OracleHost(_oracle_kind(workload), workload, seed)
+    try:
+        host.measure(min(1.0, budget_s))  # warm-up
+        return host.record(host.measure(budget_s))
+    finally:
+        host.close()
 
 
 def run_reference(args, rank, world):
@@ -940,17 +1054,16 @@ def run_reference(args, rank, world):
     cfg = W.WORKLOADS[args.workload]
     prefill = "S" in cfg
     kvdown = "T" in cfg
-    fn = cpu_baseline_kvdown if kvdown else (cpu_baseline_prefill if prefill else cpu_baseline)
-    steps = []
-    for _ in range(max(1, args.warmup)):
-        fn(args.workload, args.seed, budget_s=0.5)
-    per = max(1.0, min(10.0, 60.0 / max(args.steps, 1)))
-    for _ in range(args.steps):
-        steps.append(fn(args.workload, args.seed, budget_s=per))
-    vals = [s["value"] for s in steps]
-    v = statistics.median(vals)
-    cb = dict(steps[-1])
-    cb["value"] = round(v, 3)
+    host = OracleHost(_oracle_kind(args.workload), args.workload, args.seed)
+    try:
+        for _ in range(max(1, args.warmup)):
+            host.measure(0.5)
+        per = max(1.0, min(10.0, 60.0 / max(args.steps, 1)))
+        vals = [host.measure(per) for _ in range(args.steps)]
+        v = statistics.median(vals)
+        cb = host.record(v)
+    finally:
+        host.close()
     if kvdown:
         metric = (f"MLA cache rows from hidden states tokens/s (RMSNorm(h W_DKV) || RoPE(h W_KR), append) at "
                   f"T={cfg['T']},d_model={cfg['d_model']},d_c={cfg['d_c']},d_r={cfg['d_r']} bf16; % of roofline")
@@ -1012,11 +1125,11 @@ def main():
         if "T" in W.WORKLOADS[args.workload]:
             out = run_b300_kvdown(args, rank, world, device)
             if rank == 0 and not args.no_cpu_baseline:
-                out["cpu_baseline"] = cpu_baseline_kvdown(args.workload, args.seed, budget_s=args.cpu_seconds)
+                out["cpu_baseline"] = cpu_baseline(args.workload, args.seed, budget_s=args.cpu_seconds)
         elif "S" in W.WORKLOADS[args.workload]:
             out = run_b300_prefill(args, rank, world, device)
             if rank == 0 and not args.no_cpu_baseline:
-                out["cpu_baseline"] = cpu_baseline_prefill(args.workload, args.seed, budget_s=args.cpu_seconds)
+                out["cpu_baseline"] = cpu_baseline(args.workload, args.seed, budget_s=args.cpu_seconds)
         else:
             out = run_b300(args, rank, world, device)
         if rank == 0:
