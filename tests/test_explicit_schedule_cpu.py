@@ -114,3 +114,21 @@ def model(B, S, H, start, causal, seed=0, scale=1/math.sqrt(192), base=1e4, N_ma
                                                       (1, 100, 1, 20, True, 300)])
 def test_explicit_prefill_schedule_reproduces_oracle(B, S, H, start, causal, extra):
     model(B, S, H, start, causal, N_max=start + S + extra if extra else None)
+
+
+@pytest.mark.parametrize("B,start,S,H", [(1, 0, 300, 2), (2, 37, 200, 4), (4, 0, 8192, 128), (1, 130, 257, 6)])
+def test_kv_rebuild_grid_writes_every_output_once(B, start, S, H):
+    # kvup grid (H feature tiles: H / 2 for K, H / 2 for V; ceil(P / 128) token
+    # tiles; B sequences): every (sequence, token < P, feature) of both buffers is
+    # written by exactly one CTA, and every weight tile lies inside W_UK / W_UV
+    P = start + S
+    feats = H * 128
+    count = np.zeros((2, B, -(-P // 128) * 128, feats // 256), dtype=np.int64)
+    for ft in range(H):
+        is_v = ft >= H // 2
+        f0 = (ft - H // 2 if is_v else ft) * 256
+        assert f0 % 256 == 0 and f0 + 256 <= feats          # the 256-row weight box stays inside
+        for ty in range(-(-P // 128)):
+            t0 = ty * 128
+            count[int(is_v), :, t0:t0 + 128, f0 // 256] += 1  # all B sequences (grid z)
+    assert np.all(count[:, :, :P] == 1)
