@@ -519,12 +519,21 @@ def prefill_flops(cfg):
     return pairs * cfg["H"] * (2 * R + 2 * cfg["d_c"]), pairs
 
 
+def prefill_explicit_flops(cfg):
+    """K / V rebuild (2 B S H (d_k + d_v) d_c) plus causal (query, row) pairs x heads x
+    (2 (d_k + d_r) + 2 d_v)."""
+    B, S, H, d_c, d_r, d_k, d_v = (cfg[k] for k in ("B", "S", "H", "d_c", "d_r", "d_k", "d_v"))
+    pairs = B * S * (S + 1) // 2
+    return 2 * B * S * H * (d_k + d_v) * d_c + pairs * H * (2 * (d_k + d_r) + 2 * d_v), pairs
+
+
 class PrefillWorkload:
     """One prompt step over static buffers: append the B x S prompt rows (RoPE at
     0..S-1), absorb every query at its own position, causal prefill attention,
-    W_UV.  Inputs are far larger than L2."""
+    W_UV.  With explicit=True the step is append + prefill without absorption (K and
+    V rebuilt per head, standard causal attention).  Inputs are far larger than L2."""
 
-    def __init__(self, name, seed, device):
+    def __init__(self, name, seed, device, explicit=False):
         import torch
         import head_latent_attention_29_b300 as mla
         self.mla, self.torch = mla, torch
@@ -548,15 +557,26 @@ class PrefillWorkload:
         self.seq_idx = torch.arange(B, dtype=torch.int32, device=device).repeat_interleave(S)
         self.pos = torch.arange(S, dtype=torch.int32, device=device).repeat(B)
         self.q_start = torch.zeros(B, dtype=torch.int32, device=device)
-        self.q_cat = torch.empty((B, S, H, d_c + d_r), dtype=bf, device=device)
-        self.o_lat = torch.empty((B, S, H, d_c), dtype=bf, device=device)
+        if not explicit:  # the explicit form needs neither the absorbed query nor o_lat
+            self.q_cat = torch.empty((B, S, H, d_c + d_r), dtype=bf, device=device)
+            self.o_lat = torch.empty((B, S, H, d_c), dtype=bf, device=device)
         self.lse = torch.empty((B, S, H), dtype=torch.float32, device=device)
         self.o = torch.empty((B, S, H, d_v), dtype=bf, device=device)
         self.o_host = torch.empty((B, S, H, d_v), dtype=bf).pin_memory()
-        self.ws = mla.prefill_workspace(B, S, H, d_c, bf, device)
-        self.kernels_per_step = 5  # append, absorb GEMM, split attention, combine, out-up GEMM
+        self.explicit = explicit
+        if explicit:
+            self.ws = mla.prefill_explicit_workspace(B, 0, S, H, device)
+            self.kernels_per_step = 3  # append, K / V rebuild GEMM, attention
+        else:
+            self.ws = mla.prefill_workspace(B, S, H, d_c, bf, device)
+            self.kernels_per_step = 5  # append, absorb GEMM, split attention, combine, out-up GEMM
 
     def attn(self):
+        if self.explicit:
+            d = self.dev
+            self.mla.prefill_explicit(d["q_nope"], d["q_rope"], self.cache, self.w_uk, self.w_uv, 0, self.scale,
+                                      True, self.base, self.ws, self.o, self.lse)
+            return
         self.mla.prefill_attn(self.q_cat, self.cache, self.q_start, self.scale, True, self.ws, self.o_lat, self.lse)
 
     def step(self, copy_in=False, copy_out=False):
@@ -566,6 +586,11 @@ class PrefillWorkload:
                 d[k].copy_(v, non_blocking=True)
         mla.cache_append(self.cache, d["c_kv"].view(BS, -1), d["k_r"].view(BS, -1), self.seq_idx, self.pos,
                          self.base)
+        if self.explicit:
+            self.attn()
+            if copy_out:
+                self.o_host.copy_(self.o, non_blocking=True)
+            return
         mla.absorb_q(d["q_nope"].view(BS, self.H, -1), d["q_rope"].view(BS, self.H, -1), self.pos, self.w_uk,
                      self.base, out=self.q_cat.view(BS, self.H, -1))
         self.attn()
@@ -578,7 +603,8 @@ def run_b300_prefill(args, rank, world, device):
     import torch
     import torch.distributed as dist
     torch.cuda.set_device(device)
-    wl = PrefillWorkload(args.workload, args.seed + rank, device)
+    explicit = getattr(args, "explicit", False)
+    wl = PrefillWorkload(args.workload, args.seed + rank, device, explicit)
     cfg = wl.cfg
     stream = torch.cuda.current_stream(device)
 
@@ -631,9 +657,14 @@ def run_b300_prefill(args, rank, world, device):
     d2h = wl.o_host.numel() * wl.o_host.element_size()
 
     hbm, tc_burst, tc_sust, peak_kind = _peaks()
-    flops, pairs = prefill_flops(cfg)
+    flops, pairs = prefill_explicit_flops(cfg) if explicit else prefill_flops(cfg)
     R = cfg["d_c"] + cfg["d_r"]
-    bytes_alg = cfg["B"] * cfg["S"] * cfg["H"] * (R + cfg["d_c"]) * 2 + cfg["B"] * cfg["S"] * R * 2
+    if explicit:  # queries and rows in, rebuilt K / V out and back in, o out
+        kv = cfg["B"] * cfg["S"] * cfg["H"] * (cfg["d_k"] + cfg["d_v"]) * 2
+        bytes_alg = (cfg["B"] * cfg["S"] * (cfg["H"] * (cfg["d_k"] + cfg["d_r"]) + R) * 2 + 2 * kv
+                     + cfg["B"] * cfg["S"] * cfg["H"] * cfg["d_v"] * 2)
+    else:
+        bytes_alg = cfg["B"] * cfg["S"] * cfg["H"] * (R + cfg["d_c"]) * 2 + cfg["B"] * cfg["S"] * R * 2
     tflops = flops / (attn_us * 1e-6) / 1e12
     t_tc = flops / (tc_burst * 1e12)
     t_mem = bytes_alg / (hbm * 1e9)
@@ -646,13 +677,16 @@ def run_b300_prefill(args, rank, world, device):
         "data": "synthetic (seeded N(0,1) latents/keys/queries, N(0,1/512) up-projections)",
         "config": {"workload": args.workload, "B": cfg["B"], "S": cfg["S"], "H": cfg["H"], "d_c": cfg["d_c"],
                    "d_r": cfg["d_r"], "causal": True, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (q_cat 4.8 GB, o_lat 4.3 GB per step)",
-                   "step": "append(B*S rows)+absorb_q(B*S queries)+prefill_attn(split+combine)+out_up"},
+                   "l2": "inputs larger than L2 (queries, rebuilt K / V or q_cat / o_lat: GBs per step)",
+                   "step": ("append(B*S rows)+prefill_explicit(K/V rebuild + causal attention)" if explicit else
+                            "append(B*S rows)+absorb_q(B*S queries)+prefill_attn(split+combine)+out_up")},
         "gpu_launches": wl.kernels_per_step * args.steps,
         "e2e": {"value": round(tokens / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "roofline": {
-            "bound": "tensor", "kernel": "prefill_attn (split tensor-core kernel + combine)",
+            "bound": "tensor",
+            "kernel": ("prefill_explicit (K/V rebuild GEMM + causal attention)" if explicit else
+                       "prefill_attn (split tensor-core kernel + combine)"),
             "achieved": round(tflops, 1), "peak": tc_burst, "unit": "TFLOP/s", "frac": round(tflops / tc_burst, 4),
             "traffic": None, "peak_source": f"{peak_kind} bf16_tflops (burst)",
             "frac_sustained": round(tflops / tc_sust, 4) if tc_sust else None,
@@ -1097,11 +1131,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rotate", type=int, default=ROTATE, help="cache copies rotated between steps (>= 1)")
+    ap.add_argument("--explicit", action="store_true",
+                    help="prefill workloads: the non-absorbed form (K and V rebuilt per head)")
     ap.add_argument("--paged", action="store_true",
                     help="decode workloads: 64-row pages of one pool in shuffled order behind a block table")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.explicit and "S" not in W.WORKLOADS[args.workload]:
+        ap.error("--explicit applies to prefill workloads")
     if args.paged and ("S" in W.WORKLOADS[args.workload] or "T" in W.WORKLOADS[args.workload]):
         ap.error("--paged applies to decode workloads")
 

@@ -26,7 +26,7 @@ __all__ = [
     "MlaError", "LatentCache", "lib", "cache_append", "absorb_q", "decode_workspace",
     "decode_attn", "decode_attn_noalloc", "out_up", "gate", "get_device_error", "debug_inject_fault", "LIB_PATH",
     "PagedLatentCache", "cache_append_paged", "decode_attn_paged", "PAGE_ROWS",
-    "kv_down_workspace", "kv_down_append",
+    "kv_down_workspace", "kv_down_append", "prefill_explicit_workspace", "prefill_explicit",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -103,6 +103,13 @@ _SIGS = {
                                                 ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p,
                                                 ctypes.c_size_t, ctypes.c_void_p]),
+    "mla_prefill_explicit_workspace_size": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                              ctypes.c_int32]),
+    "mla_prefill_explicit": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(_Cache),
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+                                            ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_void_p]),
     "mla_decode_attn_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(_Cache), ctypes.c_void_p,
                                                ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p]),
@@ -464,3 +471,46 @@ def kv_down_append(cache, h: torch.Tensor, w_dkvr: torch.Tensor, gamma: torch.Te
                 else (lib().mla_kv_down_append, "mla_kv_down_append"))
     _check(fn(ctypes.byref(st), _ptr(h), _ptr(w_dkvr), _ptr(gamma), float(eps), _ptr(seq_idx), _ptr(pos), T,
               d_model, float(rope_base), _ptr(workspace), workspace.numel(), _stream(h)), name)
+
+
+def prefill_explicit_workspace(B: int, start: int, S: int, H: int, device="cuda") -> torch.Tensor:
+    """Device scratch for prefill_explicit (the rebuilt K_nope and V)."""
+    n = lib().mla_prefill_explicit_workspace_size(B, start, S, H)
+    if n == 0:
+        raise MlaError(1, "mla_prefill_explicit_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def prefill_explicit(q_nope: torch.Tensor, q_rope: torch.Tensor, cache: LatentCache, w_uk: torch.Tensor,
+                     w_uv: torch.Tensor, start: int, scale: float, causal: bool = True, rope_base: float = 10000.0,
+                     workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                     lse: torch.Tensor | None = None, want_lse: bool = True):
+    """o [B, S, H, d_v] (and lse [B, S, H]) of a prompt chunk at offset `start`
+    without absorption: K and V rebuilt per head from the cached latent rows."""
+    _dev_tensor(q_nope, "q_nope", cache.dtype)
+    _dev_tensor(q_rope, "q_rope", cache.dtype)
+    _dev_tensor(w_uk, "w_uk", cache.dtype)
+    _dev_tensor(w_uv, "w_uv", cache.dtype)
+    B, S, H, d_k = q_nope.shape
+    if B != cache.B or tuple(q_rope.shape) != (B, S, H, cache.d_r):
+        raise ValueError("q_nope / q_rope shapes do not match the cache")
+    d_v = w_uv.shape[1]
+    if tuple(w_uk.shape) != (H, d_k, cache.d_c) or tuple(w_uv.shape) != (H, d_v, cache.d_c):
+        raise ValueError("w_uk must be [H, d_k, d_c] and w_uv [H, d_v, d_c]")
+    if d_k != 128 or d_v != 128:
+        raise MlaError(2, "prefill_explicit (d_k = d_v = 128 only)")
+    if workspace is None:
+        workspace = prefill_explicit_workspace(B, start, S, H, q_nope.device)
+    if out is None:
+        out = torch.empty((B, S, H, d_v), dtype=cache.dtype, device=q_nope.device)
+    _out_tensor(out, "out", (B, S, H, d_v), cache.dtype)
+    if lse is None and want_lse:
+        lse = torch.empty((B, S, H), dtype=torch.float32, device=q_nope.device)
+    if lse is not None:
+        _out_tensor(lse, "lse", (B, S, H), torch.float32)
+    st = cache.struct()
+    _check(lib().mla_prefill_explicit(_ptr(q_nope), _ptr(q_rope), ctypes.byref(st), _ptr(w_uk), _ptr(w_uv),
+                                      int(start), S, 1 if causal else 0, H, float(scale), float(rope_base),
+                                      _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse), _stream(q_nope)),
+           "mla_prefill_explicit")
+    return out, lse

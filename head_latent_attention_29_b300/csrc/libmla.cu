@@ -4,5 +4,6 @@
 #include "k_decode_tc.cu"
 #include "k_headgemm.cu"
 #include "k_kvdown.cu"
+#include "k_prefill_explicit.cu"
 #include "mla_api.cu"
 #include "mla_noalloc.cu"

@@ -301,6 +301,29 @@ MLA_API mla_status mla_kv_down_append_paged(const mla_paged_cache* cache, const 
                  stream, cache->block_table, cache->max_blocks, cache->num_pages);
 }
 
+MLA_API size_t mla_prefill_explicit_workspace_size(int32_t B, int32_t start, int32_t S, int32_t H) {
+  return mla::prefill_explicit_workspace_size(B, start, S, H);
+}
+
+MLA_API mla_status mla_prefill_explicit(const void* q_nope, const void* q_rope, const mla_cache* cache,
+                                        const void* w_uk, const void* w_uv, int32_t start, int32_t S, int32_t causal,
+                                        int32_t H, float scale, float rope_base, void* workspace,
+                                        size_t workspace_bytes, void* o, float* lse, void* stream) {
+  const OpRange range("mla_prefill_explicit");
+  const mla_status st = check_cache(cache);
+  if (st != MLA_OK) return st;
+  if (q_nope == nullptr || q_rope == nullptr || w_uk == nullptr || w_uv == nullptr || o == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (S <= 0 || start < 0 || H <= 0 || static_cast<int64_t>(start) + S > cache->N_max) return MLA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) && !(scale < 0.f) && scale != 0.f) return MLA_ERR_INVALID_ARG;  // NaN
+  if (!(rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(o))
+    return MLA_ERR_INVALID_ARG;
+  if (cache->dtype != MLA_BF16 || cache->d_c != 512 || cache->d_r != 64 || (H & 1) != 0) return MLA_ERR_UNSUPPORTED;
+  return mla::launch_prefill_explicit(q_nope, q_rope, *cache, w_uk, w_uv, start, S, causal, H, scale, rope_base,
+                                      workspace, workspace_bytes, o, lse, as_stream(stream));
+}
+
 MLA_API mla_status mla_debug_inject_fault(int32_t kind) {
   if (kind != 0 && kind != 1) return MLA_ERR_INVALID_ARG;
   mla::set_fault_injection(kind);

@@ -188,6 +188,12 @@ mla_status launch_kv_down(const mla_cache& c, const void* h, const void* w, cons
                           void* ws, size_t ws_bytes, cudaStream_t s, const int32_t* block_table = nullptr,
                           int32_t max_blocks = 0, int32_t num_pages = 0);
 
+// explicit (non-absorbed) prefill: K / V rebuilt per head, then causal attention
+size_t prefill_explicit_workspace_size(int32_t B, int32_t start, int32_t S, int32_t H);
+mla_status launch_prefill_explicit(const void* q_nope, const void* q_rope, const mla_cache& c, const void* w_uk,
+                                   const void* w_uv, int32_t start, int32_t S, int32_t causal, int32_t H, float scale,
+                                   float rope_base, void* ws, size_t ws_bytes, void* o, float* lse, cudaStream_t s);
+
 // tensor-core decode and prefill (bf16): sizes and launch
 void set_fault_injection(int32_t kind);
 size_t decode_tc_workspace_size(int32_t B);

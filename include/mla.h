@@ -283,6 +283,39 @@ MLA_API mla_status mla_decode_attn_paged(const void* q_cat, const mla_paged_cach
                                          size_t workspace_bytes, void* o_lat, float* lse, void* stream);
 
 /*
+ * mla_prefill_explicit_workspace_size -- bytes of device workspace
+ * mla_prefill_explicit needs: the rebuilt K_nope and V, 2 x B x (start + S) x H x
+ * 128 bf16.  0 if a size is not positive (start may be 0).
+ */
+MLA_API size_t mla_prefill_explicit_workspace_size(int32_t B, int32_t start, int32_t S, int32_t H);
+
+/*
+ * mla_prefill_explicit -- prefill of a prompt chunk without absorption.  Every
+ *   head's keys and values are rebuilt from the cached latent rows (0539edu.com
+ *   section 2.2: k = c_KV W_UK, v = c_KV W_UV; the same page notes that absorption
+ *   makes prefill more expensive and that the explicit form is the precision
+ *   fallback), and the prompt runs standard attention per head:
+ *     k_h,t = [c_KV,t W_UK,h^T || k_R,t (as cached, rotated)]
+ *     q_h,i = [q_nope[b][i][h] || RoPE(q_rope[b][i][h], start + i)]
+ *     o[b][i][h] = sum_t softmax_t(scale q_h,i . k_h,t) c_KV,t W_UV,h^T
+ *     lse[b][i][h] = ln sum_t exp(scale q_h,i . k_h,t)
+ *   over t <= start + i when causal, t < start + S otherwise.  The result equals
+ *   mla_prefill_attn followed by mla_out_up (same rows, same queries), with fewer
+ *   FLOPs per score.  All sequences share the chunk offset `start`; rows
+ *   0 .. start + S - 1 of every sequence must be in the cache.
+ *   q_nope [B, S, H, 128], q_rope [B, S, H, 64] bf16 (unrotated); W_UK, W_UV
+ *   [H, 128, 512] bf16; o [B, S, H, 128] bf16 (output); lse [B, S, H] float32 or
+ *   NULL.  Workspace: mla_prefill_explicit_workspace_size(B, start, S, H) bytes,
+ *   16-byte aligned.  Limits: bf16 cache with d_c = 512 and d_r = 64, d_k = d_v =
+ *   128, H even (MLA_ERR_UNSUPPORTED otherwise); start + S <= N_max.
+ */
+MLA_API mla_status mla_prefill_explicit(const void* q_nope, const void* q_rope, const mla_cache* cache,
+                                        const void* w_uk, const void* w_uv, int32_t start, int32_t S,
+                                        int32_t causal, int32_t H, float scale, float rope_base,
+                                        void* workspace, size_t workspace_bytes, void* o, float* lse,
+                                        void* stream);
+
+/*
  * mla_kv_down_workspace_size -- bytes of device workspace mla_kv_down_append needs
  * for T tokens (fp32 partial sums of the projection).  0 if T <= 0 or the sizes
  * are not positive.

@@ -262,3 +262,29 @@ def test_header_compiles_as_c_and_layouts_match_the_binding(tmp_path, libmla):
     assert c == [ctypes.sizeof(C), C.dtype.offset, C.d_r.offset, C.row_stride.offset, C.N_max.offset]
     assert p == [ctypes.sizeof(P), P.num_pages.offset, P.row_stride.offset, P.block_table.offset,
                  P.max_blocks.offset]
+
+
+def test_prefill_explicit_validation(libmla):
+    import head_latent_attention_29_b300 as mla
+    INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 5
+    assert libmla.mla_prefill_explicit_workspace_size(4, 0, 8192, 128) == 2 * 4 * 8192 * 128 * 128 * 2
+    assert libmla.mla_prefill_explicit_workspace_size(1, 37, 200, 2) == 2 * 237 * 2 * 128 * 2
+    assert libmla.mla_prefill_explicit_workspace_size(0, 0, 1, 2) == 0
+    p = ctypes.c_void_p(0x2000)
+    c = mla._Cache(0x1000, 0, 2, 300, 512, 64, 0, 576)
+
+    def call(cache=c, start=0, S=200, H=4, causal=1, scale=0.07, base=1e4, ptr=p, wsb=1 << 30):
+        return libmla.mla_prefill_explicit(ptr, p, ctypes.byref(cache), p, p, start, S, causal, H, scale, base, p,
+                                           wsb, p, None, None)
+
+    assert call(ptr=ctypes.c_void_p(0)) == INVALID
+    assert call(ptr=ctypes.c_void_p(0x2008)) == INVALID         # 16-byte aligned queries
+    assert call(S=0) == INVALID
+    assert call(start=-1) == INVALID
+    assert call(start=101, S=200) == INVALID                    # start + S beyond N_max = 300
+    assert call(scale=float("nan")) == INVALID
+    assert call(base=0.0) == INVALID
+    assert call(H=3) == UNSUPPORTED                             # the K/V rebuild pairs heads
+    assert call(cache=mla._Cache(0x1000, 0, 2, 300, 512, 0, 0, 512)) == UNSUPPORTED  # needs the 64-wide key
+    assert call(cache=mla._Cache(0x1000, 1, 2, 300, 512, 64, 0, 576)) == UNSUPPORTED  # bf16 only
+    assert call(wsb=1024) == WORKSPACE
