@@ -27,6 +27,7 @@ __all__ = [
     "decode_attn", "decode_attn_noalloc", "out_up", "gate", "get_device_error", "debug_inject_fault", "LIB_PATH",
     "PagedLatentCache", "cache_append_paged", "decode_attn_paged", "PAGE_ROWS",
     "kv_down_workspace", "kv_down_append", "prefill_explicit_workspace", "prefill_explicit",
+    "decode_attn_partial", "decode_merge",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -110,6 +111,12 @@ _SIGS = {
                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
                                             ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p,
                                             ctypes.c_void_p]),
+    "mla_decode_attn_partial": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(_Cache), ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p,
+                                               ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "mla_decode_merge": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p]),
     "mla_decode_attn_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(_Cache), ctypes.c_void_p,
                                                ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p]),
@@ -298,6 +305,55 @@ def prefill_attn(q_cat: torch.Tensor, cache: LatentCache, q_start: torch.Tensor,
     _check(lib().mla_prefill_attn(_ptr(q_cat), ctypes.byref(st), _ptr(q_start), S, H, float(scale), int(causal),
                                   _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse), _stream(q_cat)),
            "mla_prefill_attn")
+    return out, lse
+
+
+def decode_attn_partial(q_cat: torch.Tensor, cache: LatentCache, row_begin: torch.Tensor, row_end: torch.Tensor,
+                        scale: float, workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                        lse: torch.Tensor | None = None):
+    """Attention of each sequence's query over its rows [row_begin[b], row_end[b])
+    only, as a partial for decode_merge: (o_part [B, H, d_c], lse_part [B, H] fp32)."""
+    _dev_tensor(q_cat, "q_cat", cache.dtype)
+    B, H, R = q_cat.shape
+    if B != cache.B or R != cache.d_c + cache.d_r:
+        raise ValueError("q_cat shape does not match the cache")
+    _dev_tensor(row_begin, "row_begin", torch.int32)
+    _dev_tensor(row_end, "row_end", torch.int32)
+    if row_begin.numel() != B or row_end.numel() != B:
+        raise ValueError("row_begin and row_end need one entry per sequence")
+    if workspace is None:
+        workspace = decode_workspace(B, H, cache.d_c, cache.dtype, q_cat.device)
+    if out is None:
+        out = torch.empty((B, H, cache.d_c), dtype=cache.dtype, device=q_cat.device)
+    _out_tensor(out, "out", (B, H, cache.d_c), cache.dtype)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q_cat.device)
+    _out_tensor(lse, "lse", (B, H), torch.float32)
+    st = cache.struct()
+    _check(lib().mla_decode_attn_partial(_ptr(q_cat), ctypes.byref(st), _ptr(row_begin), _ptr(row_end), H,
+                                         float(scale), _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
+                                         _stream(q_cat)), "mla_decode_attn_partial")
+    return out, lse
+
+
+def decode_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out: torch.Tensor | None = None,
+                 lse: torch.Tensor | None = None, want_lse: bool = True):
+    """Merge k partials of disjoint row ranges, o_parts [k, B, H, d_c] and lse_parts
+    [k, B, H] fp32, into (o_lat [B, H, d_c], lse [B, H])."""
+    _dev_tensor(o_parts, "o_parts")
+    if o_parts.dim() != 4:
+        raise ValueError("o_parts must be [k, B, H, d_c]")
+    k, B, H, d_c = o_parts.shape
+    _out_tensor(lse_parts, "lse_parts", (k, B, H), torch.float32)
+    if out is None:
+        out = torch.empty((B, H, d_c), dtype=o_parts.dtype, device=o_parts.device)
+    _out_tensor(out, "out", (B, H, d_c), o_parts.dtype)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=o_parts.device)
+    if lse is not None:
+        _out_tensor(lse, "lse", (B, H), torch.float32)
+    _check(lib().mla_decode_merge(_ptr(o_parts), _ptr(lse_parts), k, B, H, d_c, _DT[o_parts.dtype], _ptr(out),
+                                  _ptr(lse), _stream(o_parts)), "mla_decode_merge")
     return out, lse
 
 

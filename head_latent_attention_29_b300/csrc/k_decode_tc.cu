@@ -173,15 +173,48 @@ struct Args {
   const int32_t* block_table;  // paged cache: [seqs][max_blocks] page of each 64-row block; nullptr when
                                //   the cache is contiguous
   int max_blocks, num_pages;
+  const int32_t* row_begin;    // decode over row ranges (the kRanged kernel): [B] first row of sequence b;
+                               //   pb.seq_lens then holds the end (exclusive) of its rows
 };
 
+// Rows of problem pr in a decode over row ranges: [row0, row0 + len) with
+// 0 <= row0 <= row0 + len <= N_max (clamped; out-of-range ranges are recorded by the
+// planner).  Without ranges (kRanged = false) the problem's own length from row 0.
+template <bool kRanged>
+__device__ __forceinline__ int span_row0(const Args& a, int pr) {
+  if constexpr (kRanged) return clamp_len(a.row_begin[pr], a.N_max);
+  else return 0;
+}
+template <bool kRanged>
+__device__ __forceinline__ int span_len(const Args& a, int pr) {
+  if constexpr (kRanged) {
+    const int r0 = clamp_len(a.row_begin[pr], a.N_max), e = clamp_len(a.pb.seq_lens[pr], a.N_max);
+    return e > r0 ? e - r0 : 0;
+  } else {
+    return a.pb.len(pr);
+  }
+}
+template <bool kRanged>
+__device__ __forceinline__ bool span_bad(const Args& a, int pr) {
+  if constexpr (kRanged) {
+    const int r0 = a.row_begin[pr], e = a.pb.seq_lens[pr];
+    return r0 < 0 || e < r0 || e > a.N_max;
+  } else {
+    const int n = a.pb.raw_len(pr);
+    return n < 0 || n > a.N_max;
+  }
+}
+
 // Walks the 64-token blocks [lo, hi) of the flattened token stream.
+template <bool kRanged>
 struct Cursor {
   Problems pbs;
+  const int32_t* rbeg;  // kRanged: the first row of each problem
   long long g, lo, hi, cum;
-  int b, len, nblk, cs;  // b: problem, cs: its cache sequence
-  __device__ void start(const Misc& m, const Problems& p) {
-    pbs = p;
+  int b, len, nblk, cs, r0;  // b: problem, cs: its cache sequence, r0: its first row (kRanged)
+  __device__ void start(const Misc& m, const Args& a) {
+    pbs = a.pb;
+    rbeg = a.row_begin;
     g = lo = m.lo;
     hi = m.hi;
     cum = m.cum0;
@@ -189,6 +222,7 @@ struct Cursor {
     len = m.len0;
     nblk = (len + kBN - 1) / kBN;
     cs = pbs.seq(b);
+    if constexpr (kRanged) r0 = clamp_len(rbeg[b], pbs.n_max);
   }
   __device__ bool ok() const { return g < hi; }
   __device__ void next() {
@@ -196,7 +230,13 @@ struct Cursor {
     while (g < hi && g >= cum + nblk) {
       cum += nblk;
       ++b;
-      len = pbs.len(b);
+      if constexpr (kRanged) {
+        r0 = clamp_len(rbeg[b], pbs.n_max);
+        const int e = clamp_len(pbs.seq_lens[b], pbs.n_max);
+        len = e > r0 ? e - r0 : 0;
+      } else {
+        len = pbs.len(b);
+      }
       nblk = (len + kBN - 1) / kBN;
       cs = pbs.seq(b);
     }
@@ -214,9 +254,11 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base
 // in a contiguous cache; row 0 of the block's page in a paged pool (an index
 // outside the pool is recorded and page 0 read instead, so the load stays in
 // bounds and its barrier completes).
-__device__ __forceinline__ void block_coords(const Args& a, const Cursor& c, int* row, int* plane) {
+template <bool kRanged>
+__device__ __forceinline__ void block_coords(const Args& a, const Cursor<kRanged>& c, int* row, int* plane) {
   if (a.block_table == nullptr) {
-    *row = c.t0();
+    if constexpr (kRanged) *row = c.r0 + c.t0();
+    else *row = c.t0();
     *plane = c.cs;
     return;
   }
@@ -243,6 +285,7 @@ __device__ __forceinline__ uint32_t ring_chunk(uint32_t base, int st, int ch) {
 // The writer of the table (one warp per launch) also checks every length, fills the
 // block prefix table and counts the problems with no rows.  Reads only the problem
 // lengths; writes the workspace only with write_table.
+template <bool kRanged>
 __device__ void plan_run(const Args& a, Misc* misc, bool write_table) {
   const int lane = threadIdx.x & 31;
   const int sw = a.switch_cost;
@@ -252,9 +295,8 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table) {
     const int b = base + lane;
     int nb = 0;
     if (b < a.NP) {
-      const int n = a.pb.raw_len(b);
-      if (write_table && (n < 0 || n > a.N_max)) record_error(MLA_ERR_DEVICE_INDEX, kSiteDecodeLength);
-      nb = (clamp_len(n, a.N_max) + kBN - 1) / kBN;
+      if (write_table && span_bad<kRanged>(a, b)) record_error(MLA_ERR_DEVICE_INDEX, kSiteDecodeLength);
+      nb = (span_len<kRanged>(a, b) + kBN - 1) / kBN;
       empties += nb == 0;
     }
 #pragma unroll
@@ -278,7 +320,7 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table) {
     bool found_lo = !active, found_hi = !active || x_hi >= C;
     for (int base = 0; base < a.NP; base += 32) {
       const int b = base + lane;
-      const int n = b < a.NP ? a.pb.len(b) : 0;
+      const int n = b < a.NP ? span_len<kRanged>(a, b) : 0;
       const int nb = (n + kBN - 1) / kBN;
       const int cost = nb > 0 ? nb + sw : 0;
       int incl = nb, cincl = cost;
@@ -333,7 +375,8 @@ __device__ void plan_run(const Args& a, Misc* misc, bool write_table) {
 
 // Slot of the piece of problem c.b that ends this run: 2 p for the problem that holds
 // the run's first block (b0), 2 p + 1 for the one cut at the run's end.
-__device__ __forceinline__ long long piece_slot(const Cursor& c, int b0) {
+template <class C>
+__device__ __forceinline__ long long piece_slot(const C& c, int b0) {
   return 2 * static_cast<long long>(cluster_id_x()) + (c.b == b0 ? 0 : 1);
 }
 
@@ -341,7 +384,8 @@ __device__ __forceinline__ long long piece_slot(const Cursor& c, int b0) {
 // tensor memory: o = O / l in bf16 if the whole problem ran here, else the
 // unnormalised fp32 piece ([column][head] in its slot, a warp storing 128
 // contiguous bytes per column).
-__device__ __forceinline__ void store_output(const Args& a, const CUtensorMap* omap, const Cursor& c, int b0,
+template <class C>
+__device__ __forceinline__ void store_output(const Args& a, const CUtensorMap* omap, const C& c, int b0,
                                              uint32_t trow, int r, float l, int col0, uint8_t* smem_gen,
                                              uint32_t sbase) {
   if (c.whole()) {
@@ -419,6 +463,7 @@ __device__ __forceinline__ void store_output(const Args& a, const CUtensorMap* o
 // warps 4-7 softmax group A (even blocks), warps 8-11 softmax group B (odd blocks).
 // Output CTA: warp 0 TMA, warp 1 PV MMA, warps 4-7 correction + epilogue (latent
 // columns 0..255), warps 8-11 epilogue (columns 256..511).
+template <bool kRanged>
 __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_constant__ CUtensorMap map,
                                                                    const __grid_constant__ CUtensorMap qmap,
                                                                    const __grid_constant__ CUtensorMap omap,
@@ -474,13 +519,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
   if (threadIdx.x == 0) MLA_TRACE_POINT(63, score_cta ? 0 : 2);
   // the run plan reads only the problem lengths (seq_lens / q_start, which no kernel
   // of this library writes), so it overlaps the previous kernel's tail
-  if (warp == 2) plan_run(a, misc, false);
+  if (warp == 2) plan_run<kRanged>(a, misc, false);
   griddep_launch();
   // the workspace, o_lat and q_cat may still be in use by the previous kernels
   griddep_wait();
   if (score_cta && warp == 3 && cluster_id_x() == 0) {
     Misc tmp;
-    plan_run(a, &tmp, true);  // the block table and run count for the combine
+    plan_run<kRanged>(a, &tmp, true);  // the block table and run count for the combine
   }
   if (score_cta && threadIdx.x == 64 && misc->active) {  // this run's record for the combine
     int32_t* e = a.bnd + 4 * cluster_id_x();
@@ -502,11 +547,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     const uint32_t leader = elect_one();
     const int nload = score_cta ? nch : kChDC;
     const int nst = score_cta ? kStages : kStagesO;
-    Cursor c;
-    c.start(*misc, a.pb);
+    Cursor<kRanged> c;
+    c.start(*misc, a);
     int li = 0;  // ring load index: the score CTA's ring also carries each problem's query
     // 64 cache rows of block c into ring slot st
-    auto load_block = [&](const Cursor& cb, int st) {
+    auto load_block = [&](const Cursor<kRanged>& cb, int st) {
       int row, plane;
       block_coords(a, cb, &row, &plane);
       mbar_arrive_expect_tx_if(leader, bar_addr(sbase, kBarFull + st), nload * kChunk);
@@ -553,8 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t leader = elect_one();
-    Cursor c;
-    c.start(*misc, a.pb);
+    Cursor<kRanged> c;
+    c.start(*misc, a);
     if (score_cta) {
       // S = Q C^T: M = 128 heads, N = 64 tokens, A (the query) from tensor memory
       constexpr uint32_t idesc = idesc_bf16(kM, kBN, false, false);
@@ -636,8 +681,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     const int r = (threadIdx.x - 128) & 127;                    // head row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(r & ~31) << 16;
     float* ref_x = reinterpret_cast<float*>(gbase + kOffX);    // reference exchange between the groups
-    Cursor c;
-    c.start(*misc, a.pb);
+    Cursor<kRanged> c;
+    c.start(*misc, a);
     int k = 0, last_mine = -1, li = 0;  // li: the score ring's load index, as the producer counts it
     for (; c.ok(); c.next(), ++k) {
       const bool first = c.first();
@@ -747,8 +792,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     // and writes the unnormalised partial (m, l, O) at the end of each sequence run.
     const int r = threadIdx.x - 128;
     const uint32_t lane_off = static_cast<uint32_t>(r & ~31) << 16;
-    Cursor c;
-    c.start(*misc, a.pb);
+    Cursor<kRanged> c;
+    c.start(*misc, a);
     float m = 0.f, l = 0.f;
     int k = 0, n_epi = 0;
     for (; c.ok(); c.next(), ++k) {
@@ -828,8 +873,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     const int r = threadIdx.x - 256;
     const uint32_t lane_off = static_cast<uint32_t>(r & ~31) << 16;
     const float* epi = reinterpret_cast<const float*>(gbase + kOffEpi);
-    Cursor c;
-    c.start(*misc, a.pb);
+    Cursor<kRanged> c;
+    c.start(*misc, a);
     int n_epi = 0;
     for (; c.ok(); c.next()) {
       if (!c.last()) continue;
@@ -1075,7 +1120,10 @@ static int pairs_for_device() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
   const int known = cached[dev].load(std::memory_order_acquire);
   if (known > 0) return known;
-  if (ensure_smem_limit(reinterpret_cast<const void*>(decode_split_kernel), kSmemAlloc) != cudaSuccess) return -1;
+  // both instantiations have the same resources; the unranged one stands for both
+  if (ensure_smem_limit(reinterpret_cast<const void*>(decode_split_kernel<false>), kSmemAlloc) != cudaSuccess ||
+      ensure_smem_limit(reinterpret_cast<const void*>(decode_split_kernel<true>), kSmemAlloc) != cudaSuccess)
+    return -1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * kMaxPairs, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1088,7 +1136,7 @@ static int pairs_for_device() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_split_kernel, &cfg) != cudaSuccess || n <= 0) return -1;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_split_kernel<false>, &cfg) != cudaSuccess || n <= 0) return -1;
   const int pairs = n < kMaxPairs ? n : kMaxPairs;
   cached[dev].store(pairs, std::memory_order_release);  // concurrent first calls compute the same value
   return pairs;
@@ -1113,7 +1161,8 @@ struct PagedView {
 
 static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dtc::Problems& pbs, long long np,
                                  int32_t H, float scale, void* ws, size_t ws_bytes, void* o_lat, float* lse,
-                                 cudaStream_t s, const PagedView& pv = PagedView{nullptr, 0, 0}) {
+                                 cudaStream_t s, const PagedView& pv = PagedView{nullptr, 0, 0},
+                                 const int32_t* row_begin = nullptr) {
   using namespace dtc;
   const WsLayout w = ws_layout(np);
   if (ws == nullptr || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MLA_ERR_WORKSPACE;
@@ -1187,6 +1236,7 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   a.block_table = pv.table;
   a.max_blocks = pv.max_blocks;
   a.num_pages = pv.num_pages;
+  a.row_begin = row_begin;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * npairs, 1, 1);
@@ -1202,7 +1252,8 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel, map, qmap, omap, a);
+  cudaError_t e = row_begin != nullptr ? cudaLaunchKernelEx(&cfg, decode_split_kernel<true>, map, qmap, omap, a)
+                                       : cudaLaunchKernelEx(&cfg, decode_split_kernel<false>, map, qmap, omap, a);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   // at most min(runs - 1, problems) problems need a merge; one more row for empty problems
   const long long ncut = np < npairs - 1 ? np : npairs - 1;
@@ -1212,7 +1263,8 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
 
 mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
                             float scale, void* ws, size_t ws_bytes, void* o_lat, float* lse, cudaStream_t s,
-                            const int32_t* block_table, int32_t max_blocks, int32_t num_pages) {
+                            const int32_t* block_table, int32_t max_blocks, int32_t num_pages,
+                            const int32_t* row_begin) {
   dtc::Problems p = {};
   p.seq_lens = seq_lens;
   p.q_start = nullptr;
@@ -1220,7 +1272,7 @@ mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t
   p.causal = 0;
   p.n_max = c.N_max;
   return launch_attn_tc(q_cat, c, p, c.B, H, scale, ws, ws_bytes, o_lat, lse, s,
-                        PagedView{block_table, max_blocks, num_pages});
+                        PagedView{block_table, max_blocks, num_pages}, row_begin);
 }
 
 mla_status launch_prefill_tc(const void* q_cat, const mla_cache& c, const int32_t* q_start, int32_t S,

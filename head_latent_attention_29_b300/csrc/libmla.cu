@@ -5,5 +5,6 @@
 #include "k_headgemm.cu"
 #include "k_kvdown.cu"
 #include "k_prefill_explicit.cu"
+#include "k_merge.cu"
 #include "mla_api.cu"
 #include "mla_noalloc.cu"

@@ -182,6 +182,37 @@ MLA_API mla_status mla_decode_attn(const void* q_cat, const mla_cache* cache, co
                                as_stream(stream));
 }
 
+MLA_API mla_status mla_decode_attn_partial(const void* q_cat, const mla_cache* cache, const int32_t* row_begin,
+                                           const int32_t* row_end, int32_t H, float scale, void* workspace,
+                                           size_t workspace_bytes, void* o_part, float* lse_part, void* stream) {
+  const OpRange range("mla_decode_attn_partial");
+  mla_status st = check_cache(cache);
+  if (st != MLA_OK) return st;
+  if (q_cat == nullptr || row_begin == nullptr || row_end == nullptr || o_part == nullptr || lse_part == nullptr ||
+      H <= 0)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_cat) || !aligned16(o_part) || !aligned4(row_begin) || !aligned4(row_end) || !aligned4(lse_part))
+    return MLA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) && !(scale < 0.f) && scale != 0.f) return MLA_ERR_INVALID_ARG;  // NaN
+  if (cache->dtype != MLA_BF16 || cache->d_c != 512 || (cache->d_r != 0 && cache->d_r != 64) || H > 128)
+    return MLA_ERR_UNSUPPORTED;
+  return mla::launch_decode_tc(q_cat, *cache, row_end, H, scale, workspace, workspace_bytes, o_part, lse_part,
+                               as_stream(stream), nullptr, 0, 0, row_begin);
+}
+
+MLA_API mla_status mla_decode_merge(const void* o_parts, const float* lse_parts, int32_t k, int32_t B, int32_t H,
+                                    int32_t d_c, int32_t dtype, void* o_lat, float* lse, void* stream) {
+  const OpRange range("mla_decode_merge");
+  if (!valid_dtype(dtype)) return MLA_ERR_INVALID_ARG;
+  if (o_parts == nullptr || lse_parts == nullptr || o_lat == nullptr) return MLA_ERR_INVALID_ARG;
+  if (k <= 0 || B <= 0 || H <= 0 || d_c <= 0) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(o_lat) || !aligned4(lse_parts) || (lse != nullptr && !aligned4(lse)))
+    return MLA_ERR_INVALID_ARG;
+  if (d_c % 8 != 0) return MLA_ERR_UNSUPPORTED;
+  return mla::launch_decode_merge(o_parts, lse_parts, k, static_cast<long long>(B) * H, d_c, dtype, o_lat, lse,
+                                  as_stream(stream));
+}
+
 MLA_API size_t mla_prefill_workspace_size(int32_t B, int32_t S, int32_t H, int32_t d_c, int32_t dtype) {
   if (B <= 0 || S <= 0 || H <= 0 || d_c <= 0) return 0;
   if (dtype == MLA_F32) return 256;

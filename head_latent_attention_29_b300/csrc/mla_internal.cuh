@@ -200,7 +200,12 @@ size_t decode_tc_workspace_size(int32_t B);
 size_t prefill_tc_workspace_size(int32_t B, int32_t S);
 mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
                             float scale, void* ws, size_t ws_bytes, void* o_lat, float* lse, cudaStream_t s,
-                            const int32_t* block_table = nullptr, int32_t max_blocks = 0, int32_t num_pages = 0);
+                            const int32_t* block_table = nullptr, int32_t max_blocks = 0, int32_t num_pages = 0,
+                            const int32_t* row_begin = nullptr);
+// log-sum-exp merge of k partials over disjoint row ranges: o_parts [k][rows][d_c],
+// lse_parts [k][rows]
+mla_status launch_decode_merge(const void* o_parts, const float* lse_parts, int32_t k, long long rows, int32_t d_c,
+                               int32_t dtype, void* o, float* lse, cudaStream_t s);
 mla_status launch_prefill_tc(const void* q_cat, const mla_cache& c, const int32_t* q_start, int32_t S,
                              int32_t causal, int32_t H, float scale, void* ws, size_t ws_bytes, void* o_lat,
                              float* lse, cudaStream_t s);

@@ -195,6 +195,47 @@ MLA_API mla_status mla_decode_attn(const void* q_cat, const mla_cache* cache,
                                    float* lse, void* stream);
 
 /*
+ * mla_decode_attn_partial -- decode attention over a range of each sequence's
+ * cached rows, returned as a partial for a later merge.  For sequence b the query
+ * attends to rows [row_begin[b], row_end[b]) only:
+ *     o_part[b][h]   = sum_t softmax_t(s)_t * cache[b][t][0 : d_c],  t in the range
+ *     lse_part[b][h] = ln sum_t exp(s_t)
+ *   with s_t as in mla_decode_attn.  This is the unnormalised partial (m, l, O) of
+ *   the range in log-sum-exp form: with m the row maximum and l = sum exp(s - m),
+ *   O = o_part * l and lse_part = m + ln l.  Partials of disjoint ranges merge
+ *   exactly into the attention over their union (mla_decode_merge).  It is the
+ *   per-shard step of decode sharded by sequence position (the sequence-parallel
+ *   remark of 0539edu.com, section 8: every shard holds some of each sequence's
+ *   rows, computes its partial, and the partials are gathered and merged).
+ *   q_cat, cache, H, scale, workspace: as mla_decode_attn.
+ *   row_begin, row_end [B] int32 device: 0 <= row_begin[b] <= row_end[b] <= N_max
+ *             (else clamped and recorded as MLA_ERR_DEVICE_INDEX).  An empty range
+ *             gives o_part = 0 and lse_part = -inf.
+ *   o_part    [B, H, d_c] bf16 (output);  lse_part [B, H] float32 (output, required).
+ *   Limits: contiguous bf16 cache, d_c = 512, d_r in {0, 64}, 1 <= H <= 128
+ *   (MLA_ERR_UNSUPPORTED otherwise).
+ */
+MLA_API mla_status mla_decode_attn_partial(const void* q_cat, const mla_cache* cache, const int32_t* row_begin,
+                                           const int32_t* row_end, int32_t H, float scale, void* workspace,
+                                           size_t workspace_bytes, void* o_part, float* lse_part, void* stream);
+
+/*
+ * mla_decode_merge -- merge k partials of disjoint row ranges (mla_decode_attn_partial
+ * or any attention output with its log-sum-exp) into the attention over the union:
+ *     M = max_s lse_s,  w_s = exp(lse_s - M)
+ *     o_lat = sum_s w_s o_s / sum_s w_s,   lse = M + ln sum_s w_s
+ *   (the max-subtracted softmax of hotelren.com, section 7.3, across row subsets).
+ *   Rows whose partials are all empty (lse = -inf) give o_lat = 0 and lse = -inf.
+ *   o_parts   [k, B, H, d_c] dtype, contiguous, device (e.g. gathered from k shards)
+ *   lse_parts [k, B, H] float32, device
+ *   o_lat     [B, H, d_c] dtype (output);  lse [B, H] float32 or NULL.
+ *   fp32 arithmetic.  d_c % 8 == 0 (MLA_ERR_UNSUPPORTED otherwise); o_parts and
+ *   o_lat 16-byte aligned.
+ */
+MLA_API mla_status mla_decode_merge(const void* o_parts, const float* lse_parts, int32_t k, int32_t B, int32_t H,
+                                    int32_t d_c, int32_t dtype, void* o_lat, float* lse, void* stream);
+
+/*
  * mla_prefill_workspace_size -- bytes of device workspace mla_prefill_attn needs
  * for B sequences of S queries each (block table and the partials of queries
  * whose rows are split across the GPU).  Returns 0 if the shape is unsupported.
