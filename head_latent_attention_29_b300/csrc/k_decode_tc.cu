@@ -72,7 +72,7 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units: P stays <= 256
 // one's output write stalls the pipeline; with fewer, a run holds at most a couple
 // of problems and hides part of it behind the blocks already in flight.
 constexpr int kSwitchCostMany = 4;
-constexpr int kSwitchCostFew = 2;
+constexpr int kSwitchCostFew = 3;
 constexpr int kThreads = 384;               // 12 warps: see the role map in the kernel
 
 constexpr int kStages = 3;                  // score CTA TMA ring depth (HBM stream)

@@ -366,6 +366,88 @@ __global__ void __launch_bounds__(kFinishThreads) kvd_finish_kernel(const float*
   }
 }
 
+// (2') the same for projections cut into fewer than kFinishGroups K ranges (prompt-
+// sized batches run as one range): one warp per token, four tokens per block, so
+// thousands of tokens are in flight; the ranges are added in order (deterministic),
+// the mean square is a warp reduction.
+constexpr int kWarpPairs = kMaxR / 2 / 32;  // column pairs per lane
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) kvd_finish_warp_kernel(const float* __restrict__ ws, int32_t splits,
+                                                                   int32_t n_tok, int32_t d_c, int32_t d_r,
+                                                                   const T* __restrict__ gamma, float eps,
+                                                                   T* __restrict__ cache, int32_t B, int32_t N_max,
+                                                                   int64_t row_stride,
+                                                                   const int32_t* __restrict__ seq_idx,
+                                                                   const int32_t* __restrict__ pos,
+                                                                   const __grid_constant__ RopeTable rope,
+                                                                   PageMap pages) {
+  __shared__ float s_hi[64], s_lo[64];
+  griddep_launch();
+  rope_table_to_smem(rope, d_r / 2, s_hi, s_lo);
+  griddep_wait();  // the partials come from the previous kernel
+  const int lane = threadIdx.x & 31, warps = kThreads / 32;
+  const int R = d_c + d_r, pairs = R / 2;
+  const size_t split_stride = static_cast<size_t>(n_tok) * R;
+  for (int i = blockIdx.x * warps + (threadIdx.x >> 5); i < n_tok; i += gridDim.x * warps) {
+    const int32_t b = seq_idx[i];
+    const int32_t p = pos[i];
+    if (b < 0 || b >= B || p < 0 || p >= N_max) {  // warp-uniform
+      if (lane == 0) record_error(MLA_ERR_DEVICE_INDEX, kSiteAppendIndex);
+      continue;
+    }
+    int64_t row = static_cast<int64_t>(b) * N_max + p;
+    if (pages.table != nullptr) {
+      const int32_t pg = pages.table[static_cast<int64_t>(b) * pages.max_blocks + p / kPageRows];
+      if (pg < 0 || pg >= pages.num_pages) {
+        if (lane == 0) record_error(MLA_ERR_DEVICE_INDEX, kSitePageIndex);
+        continue;
+      }
+      row = static_cast<int64_t>(pg) * kPageRows + p % kPageRows;
+    }
+    const float* src = ws + static_cast<size_t>(i) * R;
+    float2 v[kWarpPairs];
+#pragma unroll
+    for (int u = 0; u < kWarpPairs; ++u) v[u] = make_float2(0.f, 0.f);
+    for (int sp = 0; sp < splits; ++sp) {
+#pragma unroll
+      for (int u = 0; u < kWarpPairs; ++u) {
+        const int q = lane + 32 * u;
+        if (q < pairs) {
+          const float2 x = *reinterpret_cast<const float2*>(src + sp * split_stride + 2 * q);
+          v[u].x += x.x;
+          v[u].y += x.y;
+        }
+      }
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < kWarpPairs; ++u) {
+      const int q = lane + 32 * u;
+      if (q < pairs && 2 * q < d_c) ss = fmaf(v[u].x, v[u].x, fmaf(v[u].y, v[u].y, ss));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = rsqrtf(ss / static_cast<float>(d_c) + eps);
+    T* dst = cache + row * row_stride;
+#pragma unroll
+    for (int u = 0; u < kWarpPairs; ++u) {
+      const int q = lane + 32 * u;
+      if (q >= pairs) continue;
+      if (2 * q < d_c) {
+        st_elem(dst + 2 * q, v[u].x * r * ld_elem(gamma + 2 * q));
+        st_elem(dst + 2 * q + 1, v[u].y * r * ld_elem(gamma + 2 * q + 1));
+      } else {
+        const int j = q - d_c / 2;
+        float sn, cs;
+        rope_sincos(p, s_hi[j], s_lo[j], &sn, &cs);
+        st_elem(dst + 2 * q, fmaf(v[u].x, cs, -v[u].y * sn));
+        st_elem(dst + 2 * q + 1, fmaf(v[u].x, sn, v[u].y * cs));
+      }
+    }
+  }
+}
+
 }  // namespace kvd
 
 size_t kv_down_workspace_size(int32_t T, int32_t d_model, int32_t d_c, int32_t d_r, int32_t dtype) {
@@ -413,16 +495,32 @@ mla_status launch_kv_down(const mla_cache& c, const void* h, const void* w, cons
     if (e != cudaSuccess) return MLA_ERR_CUDA;
   }
   const PageMap pages = {block_table, max_blocks, num_pages};
-  const int grid = T < 148 * 16 ? T : 148 * 16;
   cudaError_t e;
-  if (c.dtype == MLA_BF16)
-    e = launch_pdl(kvd_finish_kernel<__nv_bfloat16>, dim3(grid), dim3(kFinishThreads), 0, s, wsf, p.splits, T, c.d_c,
-                   c.d_r, static_cast<const __nv_bfloat16*>(gamma), eps, static_cast<__nv_bfloat16*>(c.data), c.B,
-                   c.N_max, static_cast<int64_t>(c.row_stride), seq_idx, pos, rope_table(c.d_r, rope_base), pages);
-  else
-    e = launch_pdl(kvd_finish_kernel<float>, dim3(grid), dim3(kFinishThreads), 0, s, wsf, p.splits, T, c.d_c, c.d_r,
-                   static_cast<const float*>(gamma), eps, static_cast<float*>(c.data), c.B, c.N_max,
-                   static_cast<int64_t>(c.row_stride), seq_idx, pos, rope_table(c.d_r, rope_base), pages);
+  const auto* gm = static_cast<const __nv_bfloat16*>(gamma);
+  auto* cb = static_cast<__nv_bfloat16*>(c.data);
+  const int64_t rs = static_cast<int64_t>(c.row_stride);
+  const RopeTable rt = rope_table(c.d_r, rope_base);
+  if (p.splits >= kFinishGroups) {  // a K split: four groups share each token's ranges
+    const int grid = T < 148 * 16 ? T : 148 * 16;
+    if (c.dtype == MLA_BF16)
+      e = launch_pdl(kvd_finish_kernel<__nv_bfloat16>, dim3(grid), dim3(kFinishThreads), 0, s, wsf, p.splits, T,
+                     c.d_c, c.d_r, gm, eps, cb, c.B, c.N_max, rs, seq_idx, pos, rt, pages);
+    else
+      e = launch_pdl(kvd_finish_kernel<float>, dim3(grid), dim3(kFinishThreads), 0, s, wsf, p.splits, T, c.d_c,
+                     c.d_r, static_cast<const float*>(gamma), eps, static_cast<float*>(c.data), c.B, c.N_max, rs,
+                     seq_idx, pos, rt, pages);
+  } else {  // few ranges: one warp per token, thousands of tokens in flight
+    const int warps = kThreads / 32;
+    const int need = (T + warps - 1) / warps;
+    const int grid = need < 148 * 32 ? need : 148 * 32;
+    if (c.dtype == MLA_BF16)
+      e = launch_pdl(kvd_finish_warp_kernel<__nv_bfloat16>, dim3(grid), dim3(kThreads), 0, s, wsf, p.splits, T,
+                     c.d_c, c.d_r, gm, eps, cb, c.B, c.N_max, rs, seq_idx, pos, rt, pages);
+    else
+      e = launch_pdl(kvd_finish_warp_kernel<float>, dim3(grid), dim3(kThreads), 0, s, wsf, p.splits, T, c.d_c,
+                     c.d_r, static_cast<const float*>(gamma), eps, static_cast<float*>(c.data), c.B, c.N_max, rs,
+                     seq_idx, pos, rt, pages);
+  }
   return cuda_status(e);
 }
 
