@@ -163,12 +163,17 @@ constexpr int kPBytes = 2 * kChunkBytes;   // P keys 0-63, 64-127: 32 KB
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kKStages * kKBytes;
 constexpr int kOffP = kOffV + kVStages * kVBytes;
-constexpr int kOffBar = kOffP + kPBytes;
+constexpr int kOffX = kOffP + kPBytes;         // row maxima / sums exchanged by the two halves: [2][2][128] fp32
+constexpr int kOffBar = kOffX + 2 * 2 * 128 * 4;
 // barriers (8 bytes each)
 constexpr int kBarKFull = 0, kBarKEmpty = 2, kBarVFull = 4, kBarVEmpty = 6, kBarSFull = 8, kBarSFree = 10,
-              kBarPFull = 12, kBarPvDone = 13, kBarQReady = 14, kBarDrain = 15, kNumBars = 16;
+              kBarPFull = 12, kBarPvDone = 13, kBarQReady = 14, kBarDrain = 15, kBarX = 16, kNumBars = 18;
 constexpr int kAttnSmem = kOffBar + 8 * kNumBars + 1024;  // + alignment slack
-constexpr int kAttnThreads = 256;  // warp 0: Q and K loads, 1: MMA, 2: V loads, 3: idle, 4-7: softmax
+// warp 0: Q and K loads, 1: MMA, 2: V loads, 3: idle, 4-11: softmax.  Warps 4-7 take
+// score columns 0-63 of their rows (and O columns 0-63), warps 8-11 columns 64-127
+// of the same rows (TMEM lanes 32 (w % 4) ...).
+constexpr int kAttnThreads = 384;
+constexpr int kSoftmaxThreads = 256;
 // tensor memory columns
 constexpr uint32_t kColS = 0;      // two 128-column S buffers
 constexpr uint32_t kColO = 256;    // O, 128 columns
@@ -227,11 +232,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       mbar_init(bar_at(sbase, kBarVFull + i), 1);
       mbar_init(bar_at(sbase, kBarVEmpty + i), 1);
       mbar_init(bar_at(sbase, kBarSFull + i), 1);
-      mbar_init(bar_at(sbase, kBarSFree + i), kQ);
+      mbar_init(bar_at(sbase, kBarSFree + i), kSoftmaxThreads);
+      mbar_init(bar_at(sbase, kBarX + i), kSoftmaxThreads);
     }
-    mbar_init(bar_at(sbase, kBarPFull), kQ);
+    mbar_init(bar_at(sbase, kBarPFull), kSoftmaxThreads);
     mbar_init(bar_at(sbase, kBarPvDone), 1);
-    mbar_init(bar_at(sbase, kBarQReady), kQ);
+    mbar_init(bar_at(sbase, kBarQReady), kSoftmaxThreads);
     mbar_init(bar_at(sbase, kBarDrain), 1);
     s_abort = 0;
     fence_mbar_init();
@@ -321,16 +327,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     tc_commit_if(leader, bar_at(sbase, kBarDrain));
     warp_wait(bar_at(sbase, kBarDrain), 0, abort);
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax, one query row per thread
-    const int r = threadIdx.x - 128;
+    // ------------------------------------------------------------ softmax: two threads per query row
+    // Thread (half hf, row r) owns score columns [64 hf, 64 hf + 64) of every key tile
+    // and O columns [64 hf, 64 hf + 64).  Per tile the two halves exchange their row
+    // maxima through shared memory (a barrier of all softmax threads, bounded like
+    // every wait), so that both take the same reference; each keeps the sum of its own
+    // half, and the halves' sums are added once at the end.
+    const int hf = (warp - 4) >> 2;
+    const int r = (threadIdx.x - 128) & 127;
     const uint32_t lane_off = static_cast<uint32_t>(r & ~31) << 16;
     const int qi = q0 + r;                               // prompt index of this row
     const int qpos = a.start + min(qi, a.S - 1);         // rows past the prompt mirror its last query
     const int limit = a.causal ? qpos : a.P - 1;         // last key this row reads
+    float* xch = reinterpret_cast<float*>(gbase + kOffX);  // [slot][half][row]
     bool ok = true;
-    // the query row into tensor memory, its RoPE part rotated at the row's position
+    // the query row into tensor memory (half 0: the two no-position blocks; half 1: the
+    // RoPE block, rotated at the row's position)
     if (warp_wait(bar_at(sbase, kBarKFull + 0), 0, abort)) {
-      for (int ch = 0; ch < 3; ++ch) {
+      for (int ch = hf == 0 ? 0 : 2; ch < (hf == 0 ? 2 : 3); ++ch) {
         const uint8_t* row = gbase + kOffK + ch * kChunkBytes + r * 128;
         uint32_t v[32];
 #pragma unroll
@@ -361,53 +375,55 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 
     float m_ref = 0.f, l = 0.f;
     for (int j = 0; ok && j < nkt; ++j) {
-      const int sb = j & 1, kbase = j * kKT;
+      const int sb = j & 1, kbase = j * kKT + hf * 64;
       if (!warp_wait(bar_at(sbase, kBarSFull + sb), (j >> 1) & 1, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t s_col = tmem + lane_off + kColS + sb * kKT;
-      // pass 1: the row maximum over the keys this row reads
-      float mloc = -INFINITY;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sr[64];
-        tmem_ld64(s_col + hf * 64, sr);
-        tmem_wait_ld();
+      uint32_t sr[64];
+      tmem_ld64(tmem + lane_off + kColS + sb * kKT + hf * 64, sr);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar_at(sbase, kBarSFree + sb));  // this half of S is in registers
+      // keys past the row's limit only on the diagonal (causal) or last (non-causal) tile
+      if (__any_sync(0xffffffffu, kbase + 63 > limit)) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (kbase + hf * 64 + c <= limit) mloc = fmaxf(mloc, __uint_as_float(sr[c]));
+          if (kbase + c > limit) sr[c] = __float_as_uint(-INFINITY);
       }
-      mloc *= a.scale_log2;
+      float mx[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) mx[c] = __uint_as_float(sr[c]);
+#pragma unroll
+      for (int c = 4; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sr[c]));
+      const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+      // both halves' maxima: the same reference on both sides of the row
+      xch[(sb * 2 + hf) * kQ + r] = mloc;
+      mbar_arrive(bar_at(sbase, kBarX + sb));
+      if (!warp_wait(bar_at(sbase, kBarX + sb), (j >> 1) & 1, abort)) {
+        ok = false;
+        break;
+      }
+      const float mt = fmaxf(mloc, xch[(sb * 2 + (hf ^ 1)) * kQ + r]);
       float alpha = 1.f;
       if (j == 0) {
-        m_ref = mloc;  // key 0 is always read: finite
-      } else if (mloc > m_ref + kRescaleThreshold) {
-        alpha = fast_exp2(m_ref - mloc);
-        m_ref = mloc;
+        m_ref = mt;  // key 0 is always read: finite
+      } else if (mt > m_ref + kRescaleThreshold) {
+        alpha = fast_exp2(m_ref - mt);
+        m_ref = mt;
       }
-      // pass 2: probabilities as bf16 pairs, and their row sum as rounded
-      uint32_t pk[64];
-      float psum = 0.f;
+      // probabilities as bf16 pairs, and this half's row sum as rounded
+      uint32_t pk[32];
+      float psum[4] = {0.f, 0.f, 0.f, 0.f};
       const float neg = -m_ref;
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sr[64];
-        tmem_ld64(s_col + hf * 64, sr);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const int t = kbase + hf * 64 + c;
-          const float p0 = t <= limit ? fast_exp2(fmaf(__uint_as_float(sr[c]), a.scale_log2, neg)) : 0.f;
-          const float p1 = t + 1 <= limit ? fast_exp2(fmaf(__uint_as_float(sr[c + 1]), a.scale_log2, neg)) : 0.f;
-          const uint32_t w = pack_bf16x2(p0, p1);
-          pk[hf * 32 + c / 2] = w;
-          psum += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
-        }
+      for (int c = 0; c < 64; c += 2) {
+        const uint32_t w = pack_bf16x2(fast_exp2(fmaf(__uint_as_float(sr[c]), a.scale_log2, neg)),
+                                       fast_exp2(fmaf(__uint_as_float(sr[c + 1]), a.scale_log2, neg)));
+        pk[c / 2] = w;
+        psum[(c / 2) & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
       }
-      tc_fence_before();
-      mbar_arrive(bar_at(sbase, kBarSFree + sb));
       // the previous tile's PV product has finished with P and O
       if (j >= 1 && !warp_wait(bar_at(sbase, kBarPvDone), (j - 1) & 1, abort)) {
         ok = false;
@@ -415,50 +431,54 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       }
       tc_fence_after();
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
-        for (int cc = 0; cc < kDK / 32; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_off + kColO + cc * 32, v);
+          tmem_ld32(tmem + lane_off + kColO + hf * 64 + cc * 32, v);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st32(tmem + lane_off + kColO + cc * 32, v);
+          tmem_st32(tmem + lane_off + kColO + hf * 64 + cc * 32, v);
         }
         tmem_wait_st();
       }
-      l = l * alpha + psum;
-      // row r of P (K-major, 128-byte swizzle: keys 0-63 then 64-127)
-      uint8_t* prow = gbase + kOffP + r * 128;
+      l = l * alpha + ((psum[0] + psum[1]) + (psum[2] + psum[3]));
+      // this half of row r of P (K-major, 128-byte swizzle: keys 64 hf .. 64 hf + 63)
+      uint8_t* prow = gbase + kOffP + hf * kChunkBytes + r * 128;
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(prow + hf * kChunkBytes + ((u ^ (r & 7)) << 4)) =
-              make_uint4(pk[hf * 32 + 4 * u], pk[hf * 32 + 4 * u + 1], pk[hf * 32 + 4 * u + 2], pk[hf * 32 + 4 * u + 3]);
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       fence_proxy_async_cta();
       tc_fence_before();
       mbar_arrive(bar_at(sbase, kBarPFull));
     }
-    // epilogue: O / l and the log-sum-exp, rows inside the prompt only
+    // epilogue: the halves' sums added, O / l and the log-sum-exp, rows inside the prompt
     if (ok && nkt > 0 && warp_wait(bar_at(sbase, kBarPvDone), (nkt - 1) & 1, abort)) {
-      tc_fence_after();
-      const float inv = 1.f / l;
-      __nv_bfloat16* orow = a.o + ((static_cast<size_t>(b) * a.S + qi) * a.H + h) * kDK;
-      for (int cc = 0; cc < kDK / 32; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + kColO + cc * 32, v);
-        tmem_wait_ld();
-        if (qi < a.S) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+      const int sx = nkt & 1;  // the exchange slot the last tile did not use
+      xch[(sx * 2 + hf) * kQ + r] = l;
+      mbar_arrive(bar_at(sbase, kBarX + sx));
+      if (warp_wait(bar_at(sbase, kBarX + sx), (nkt >> 1) & 1, abort)) {
+        const float ltot = l + xch[(sx * 2 + (hf ^ 1)) * kQ + r];
+        tc_fence_after();
+        const float inv = 1.f / ltot;
+        __nv_bfloat16* orow = a.o + ((static_cast<size_t>(b) * a.S + qi) * a.H + h) * kDK + hf * 64;
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + kColO + hf * 64 + cc * 32, v);
+          tmem_wait_ld();
+          if (qi < a.S) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
-                                pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
-                                pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
-                                pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
+                                  pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
+                                  pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
+                                  pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
+          }
         }
+        if (hf == 0 && qi < a.S && a.lse != nullptr)
+          a.lse[(static_cast<size_t>(b) * a.S + qi) * a.H + h] = (m_ref + __log2f(ltot)) * 0.69314718055994531f;
       }
-      if (qi < a.S && a.lse != nullptr)
-        a.lse[(static_cast<size_t>(b) * a.S + qi) * a.H + h] = (m_ref + __log2f(l)) * 0.69314718055994531f;
     }
   }
   tc_fence_before();
