@@ -751,12 +751,14 @@ class KvDownWorkload:
         for w in self.ws_list:
             call(w)  # one eager run each: one-time host setup happens outside capture
         torch.cuda.synchronize(device)
-        self.graphs, self.e2e = [], []
-        for w in self.ws_list:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
+        # one graph holds a step per weight copy, back to back as a model's layers
+        # would issue them (programmatic launch between steps, no graph-launch gap
+        # inside); a replay is `rotate` steps
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            for w in self.ws_list:
                 call(w)
-            self.graphs.append(g)
+        self.e2e = []
         # end to end: h in from pinned memory, the written rows back to pinned memory
         self.rows_dev = torch.empty((T, d_c + d_r), dtype=bf, device=device)
         for w in self.ws_list[:1]:
@@ -768,8 +770,9 @@ class KvDownWorkload:
                 self.rows_host.copy_(self.rows_dev, non_blocking=True)
             self.e2e.append(g)
 
-    def step(self, i):
-        self.graphs[i % self.rotate].replay()
+    def replay(self):
+        """`rotate` steps, each on its own weight copy."""
+        self.graph.replay()
 
 
 def run_b300_kvdown(args, rank, world, device):
@@ -784,17 +787,19 @@ def run_b300_kvdown(args, rank, world, device):
         if world > 1:
             dist.barrier()
 
-    for i in range(args.warmup):
-        wl.step(i)
+    for i in range(max(1, math.ceil(args.warmup / wl.rotate))):
+        wl.replay()
     torch.cuda.synchronize(device)
     steps = args.steps if wl.T <= 4096 else max(3, min(args.steps, 200))
+    replays = max(1, math.ceil(steps / wl.rotate))
+    steps = replays * wl.rotate
     with ClockSampler(torch.cuda.current_device()) as clk:
         barrier()
         torch.cuda.synchronize(device)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(steps):
-            wl.step(i)
+        for i in range(replays):
+            wl.replay()
         e1.record(stream)
         torch.cuda.synchronize(device)
         barrier()

@@ -18,7 +18,11 @@
 // dozen tokens still spreads the weight stream over every SM.  Each CTA writes its
 // fp32 partial tile to the workspace.  (2) One block per token sums the partials in
 // a fixed order (deterministic), normalises the latent part, rotates the key part
-// and stores the row in the cache dtype.  Shapes the tensor-core kernel does not
+// and stores the row in the cache dtype.  The projection lets the finishing kernel
+// launch (programmatic dependent launch) only once its own wait on the previous
+// kernel has returned, so the finishing kernel may read the token's slot, gains and
+// rotation before it waits for the partials: of the chain of dependent loads, only
+// the partials remain after the projection.  Shapes the tensor-core kernel does not
 // take (fp32, odd widths) use a CUDA-core kernel for (1) with a single range.
 #include "mla_internal.cuh"
 #include "mla_ptx.cuh"
@@ -106,7 +110,6 @@ __global__ void __launch_bounds__(kThreads) kvd_gemm_kernel(const __grid_constan
   const int nk = k_hi - k_lo;  // >= 1: splits <= nk
   const uint32_t tmem_cols = g.n_tile <= 32 ? 32 : (g.n_tile <= 64 ? 64 : (g.n_tile <= 128 ? 128 : 256));
 
-  griddep_launch();
   if (threadIdx.x == 0) {
     for (int i = 0; i < nst; ++i) {
       mbar_init(bars + 8 * i, 1);
@@ -147,6 +150,7 @@ __global__ void __launch_bounds__(kThreads) kvd_gemm_kernel(const __grid_constan
     const int first = nk < nst ? nk : nst;
     for (int k = 0; k < first; ++k) load_w(k, k);
     griddep_wait();
+    griddep_launch();
     for (int k = 0; k < first; ++k) load_h(k, k);
     for (int k = first; k < nk; ++k) {
       const int st = k % nst;
@@ -156,6 +160,8 @@ __global__ void __launch_bounds__(kThreads) kvd_gemm_kernel(const __grid_constan
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    griddep_wait();
+    griddep_launch();
     const uint32_t leader = elect_one();
     const uint32_t idesc = idesc_bf16(kBM, g.n_tile, true, false);
     for (int k = 0; k < nk; ++k) {
@@ -172,6 +178,9 @@ __global__ void __launch_bounds__(kThreads) kvd_gemm_kernel(const __grid_constan
       tc_commit_if(leader, bars + 8 * (kMaxStages + st));
     }
     tc_commit_if(leader, bars + 8 * (2 * kMaxStages));
+  } else {
+    griddep_wait();
+    griddep_launch();
   }
   __syncwarp();
 
@@ -215,8 +224,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) kvd_simt_kernel(const T* __restrict__ h, const T* __restrict__ w,
                                                             int32_t n_tok, int32_t d_model, int32_t R,
                                                             float* __restrict__ ws) {
-  griddep_launch();
   griddep_wait();  // h may come from the previous kernel, which may still read ws
+  griddep_launch();  // after the wait: the finishing kernel reads its row slots early
   const int m = blockIdx.x * kThreads + threadIdx.x;
   const int n0 = blockIdx.y * kSimtTokens;
   float acc[kSimtTokens];
@@ -243,7 +252,9 @@ __global__ void __launch_bounds__(kThreads) kvd_simt_kernel(const T* __restrict_
 // L2, so a chain of dependent loads would cost an L2 round trip per range), and
 // group 0 adds the four group sums in group order.  The summation order is fixed,
 // so the result is deterministic.  The latent pairs feed the mean square; the key
-// pairs are exactly RoPE's rotation pairs.
+// pairs are exactly RoPE's rotation pairs.  The block's first token's slot, gains
+// and rotation are read before the wait for the partials (the projection kernels
+// trigger this launch only after their own wait has returned).
 // ---------------------------------------------------------------------------
 constexpr int kFinishGroups = 4;
 constexpr int kFinishThreads = kThreads * kFinishGroups;
@@ -264,27 +275,62 @@ __global__ void __launch_bounds__(kFinishThreads) kvd_finish_kernel(const float*
   __shared__ float s_red[kThreads / 32];
   griddep_launch();
   rope_table_to_smem(rope, d_r / 2, s_hi, s_lo);
-  griddep_wait();  // the partials come from the previous kernel
   const int R = d_c + d_r;
   const int pairs = R / 2;
   const int g = threadIdx.x / kThreads, t = threadIdx.x % kThreads;
   const int lane = t & 31, warp = t >> 5;
   const size_t split_stride = static_cast<size_t>(n_tok) * R;
-  for (int i = blockIdx.x; i < n_tok; i += gridDim.x) {
-    const int32_t b = seq_idx[i];
-    const int32_t p = pos[i];
-    if (b < 0 || b >= B || p < 0 || p >= N_max) {  // block-uniform
-      if (threadIdx.x == 0) record_error(MLA_ERR_DEVICE_INDEX, kSiteAppendIndex);
-      continue;
-    }
+  // A token's cache slot, gains and rotation do not depend on the partials, so the
+  // block's first token has them read before the wait: the projection signals its
+  // dependents only after its own wait, so whatever wrote seq_idx, pos or the page
+  // table has completed.  Slot -1: a bad sequence or position, -2: a bad page.
+  auto slot = [&](int i, int32_t* p_out) -> int64_t {
+    const int32_t b = __ldcg(seq_idx + i);
+    const int32_t p = __ldcg(pos + i);
+    *p_out = p;
+    if (b < 0 || b >= B || p < 0 || p >= N_max) return -1;
     int64_t row = static_cast<int64_t>(b) * N_max + p;
     if (pages.table != nullptr) {
-      const int32_t pg = pages.table[static_cast<int64_t>(b) * pages.max_blocks + p / kPageRows];
-      if (pg < 0 || pg >= pages.num_pages) {
-        if (threadIdx.x == 0) record_error(MLA_ERR_DEVICE_INDEX, kSitePageIndex);
-        continue;
-      }
+      const int32_t pg = __ldcg(pages.table + static_cast<int64_t>(b) * pages.max_blocks + p / kPageRows);
+      if (pg < 0 || pg >= pages.num_pages) return -2;
       row = static_cast<int64_t>(pg) * kPageRows + p % kPageRows;
+    }
+    return row;
+  };
+  // per column pair of a group-0 thread: (gamma, gamma) of a latent pair, (cos, sin)
+  // of a key pair
+  float2 coef[kPairsPerThread];
+  auto coefs = [&](int32_t p) {
+#pragma unroll
+    for (int u = 0; u < kPairsPerThread; ++u) {
+      const int q = t + u * kThreads;
+      if (q >= pairs) continue;
+      if (2 * q < d_c) {
+        coef[u] = make_float2(ld_elem(gamma + 2 * q), ld_elem(gamma + 2 * q + 1));
+      } else {
+        const int j = q - d_c / 2;
+        float sn, cs;
+        rope_sincos(p, s_hi[j], s_lo[j], &sn, &cs);
+        coef[u] = make_float2(cs, sn);
+      }
+    }
+  };
+  int i = blockIdx.x;
+  int32_t p = 0;
+  int64_t row = -1;
+  if (i < n_tok) {
+    row = slot(i, &p);
+    if (g == 0 && row >= 0) coefs(p);
+  }
+  griddep_wait();  // the partials come from the previous kernel
+  for (; i < n_tok; i += gridDim.x) {
+    if (i != static_cast<int>(blockIdx.x)) {
+      row = slot(i, &p);
+      if (g == 0 && row >= 0) coefs(p);
+    }
+    if (row < 0) {  // block-uniform
+      if (threadIdx.x == 0) record_error(MLA_ERR_DEVICE_INDEX, row == -1 ? kSiteAppendIndex : kSitePageIndex);
+      continue;
     }
     const float* src = ws + static_cast<size_t>(i) * R;
     float2 v[kPairsPerThread];
@@ -351,12 +397,10 @@ __global__ void __launch_bounds__(kFinishThreads) kvd_finish_kernel(const float*
         const int q = t + u * kThreads;
         if (q >= pairs) continue;
         if (2 * q < d_c) {
-          st_elem(dst + 2 * q, v[u].x * r * ld_elem(gamma + 2 * q));
-          st_elem(dst + 2 * q + 1, v[u].y * r * ld_elem(gamma + 2 * q + 1));
+          st_elem(dst + 2 * q, v[u].x * r * coef[u].x);
+          st_elem(dst + 2 * q + 1, v[u].y * r * coef[u].y);
         } else {
-          const int j = q - d_c / 2;
-          float sn, cs;
-          rope_sincos(p, s_hi[j], s_lo[j], &sn, &cs);
+          const float cs = coef[u].x, sn = coef[u].y;
           st_elem(dst + 2 * q, fmaf(v[u].x, cs, -v[u].y * sn));
           st_elem(dst + 2 * q + 1, fmaf(v[u].x, sn, v[u].y * cs));
         }

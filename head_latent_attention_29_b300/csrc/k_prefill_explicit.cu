@@ -17,7 +17,8 @@
 // (256 output features, 128 tokens, sequence) tile, A = the cached latent rows
 // (K-major, straight from the cache through TMA), B = W_UK or W_UV rows (K-major),
 // K = d_c = 512, written as bf16 [B][P][H][128] (P = start + S rows per sequence).
-// (2) attn_kernel: one CTA per (sequence, head, 128-query tile), heavy tiles first.
+// (2) attn_kernel: one CTA per (sequence, head, 128-query tile); the tiles of one head
+//     are consecutive (heaviest first), so resident CTAs share its K / V in L2.
 // The query (192 wide, its RoPE part rotated on the way) sits in tensor memory as
 // the A operand of S = Q K^T (M = 128 queries, N = 128 keys); S is double-buffered
 // in tensor memory so that the softmax of one key tile overlaps the S product of
@@ -209,10 +210,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   volatile int* abort = &s_abort;
   const int warp = threadIdx.x >> 5;
 
-  // work item: heavy (late) query tiles first
-  const int bh = a.B * a.H;
-  const int qt = a.q_tiles - 1 - static_cast<int>(blockIdx.x) / bh;
-  const int rem = static_cast<int>(blockIdx.x) % bh;
+  // work item: the query tiles of one (sequence, head) are consecutive, the heaviest
+  // (latest) first, so the CTAs resident at any time cover a few heads and share
+  // their keys and values in L2 instead of each streaming its own head from HBM
+  const int qt = a.q_tiles - 1 - static_cast<int>(blockIdx.x) % a.q_tiles;
+  const int rem = static_cast<int>(blockIdx.x) / a.q_tiles;
   const int b = rem / a.H, h = rem % a.H;
   const int q0 = qt * kQ;
   // keys this tile reads: 0 .. last (causal: the last query's position)

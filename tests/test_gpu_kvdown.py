@@ -68,8 +68,10 @@ def _untouched_nan(cache, seq, pos, R):
 
 # tensor-core projection: one and several 128-column tiles with a 64-wide last tile,
 # token tiles of 16..256 and a ragged second token tile, K split over the SMs
+# (K ranges: 30 at d_model 7168, 16 at 1024, 32 at 2048, 2 at 128, 1 at 64)
 @pytest.mark.parametrize("T,d_model,d_r", [(1, 7168, 64), (5, 1024, 64), (32, 7168, 64), (300, 512, 64),
-                                           (17, 2048, 0), (64, 64, 64)])
+                                           (17, 2048, 0), (64, 64, 64), (64, 7168, 64), (65, 7168, 64),
+                                           (33, 128, 64)])
 def test_kv_down_tensor_core_path(mla, T, d_model, d_r):
     d_c, B, N_max, eps = 512, 4, 300, 1e-6
     mat, seq, pos = _inputs(T, d_model, d_c, d_r, "bf16", seed=T + d_model)
