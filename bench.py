@@ -470,7 +470,7 @@ def run_b300(args, rank, world, device):
             "d_k": cfg["d_k"], "d_v": cfg["d_v"], "tokens_cached": int(np.sum(wl.lens)),
             "parallelism": f"replicas x{world}",
             "l2": f"{wl.rotate} rotating cache copies ({wl.rotate * bytes_attn / 1e6:.0f} MB vs 126 MB L2)",
-            "step": "append+absorb_q+decode_attn(split+combine)+out_up" + ("+gate" if wl.gated else ""),
+            "step": "absorb_q_append(append + absorb in one launch)+decode_attn(split+combine)+out_up" + ("+gate" if wl.gated else ""),
             "cache": "paged (64-row pages, shuffled block table)" if wl.paged else "contiguous [B, N_max, 576]",
         },
         "gpu_launches": wl.kernels_per_step * args.steps,

@@ -26,7 +26,7 @@ __all__ = [
     "MlaError", "LatentCache", "lib", "cache_append", "absorb_q", "decode_workspace",
     "decode_attn", "decode_attn_noalloc", "out_up", "gate", "get_device_error", "debug_inject_fault", "LIB_PATH",
     "PagedLatentCache", "cache_append_paged", "decode_attn_paged", "PAGE_ROWS",
-    "kv_down_workspace", "kv_down_append", "prefill_explicit_workspace", "prefill_explicit",
+    "kv_down_workspace", "kv_down_append", "absorb_q_append", "prefill_explicit_workspace", "prefill_explicit",
     "decode_attn_partial", "decode_merge",
 ]
 
@@ -73,6 +73,15 @@ _SIGS = {
     "mla_absorb_q": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                     ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                     ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p]),
+    "mla_absorb_q_append": (ctypes.c_int, [ctypes.POINTER(_Cache), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                           ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p]),
+    "mla_absorb_q_append_paged": (ctypes.c_int, [ctypes.POINTER(_PagedCache), ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                                 ctypes.c_void_p]),
     "mla_decode_workspace_size": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     "mla_decode_attn": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(_Cache), ctypes.c_void_p, ctypes.c_int32,
                                        ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
@@ -237,6 +246,41 @@ def absorb_q(q_nope: torch.Tensor, q_rope: torch.Tensor | None, q_pos: torch.Ten
         out = torch.empty((B, H, d_c + d_r), dtype=q_nope.dtype, device=q_nope.device)
     _check(lib().mla_absorb_q(_ptr(q_nope), _ptr(q_rope), _ptr(q_pos), _ptr(w_uk), _ptr(out), B, H, d_k, d_c, d_r,
                               _DT[q_nope.dtype], float(rope_base), _stream(q_nope)), "mla_absorb_q")
+    return out
+
+
+def absorb_q_append(cache, c_kv: torch.Tensor, k_r: torch.Tensor | None, seq_idx: torch.Tensor, pos: torch.Tensor,
+                    q_nope: torch.Tensor, q_rope: torch.Tensor | None, q_pos: torch.Tensor, w_uk: torch.Tensor,
+                    rope_base: float = 10000.0, out: torch.Tensor | None = None) -> torch.Tensor:
+    """cache_append(cache, c_kv, k_r, seq_idx, pos) and absorb_q(q_nope, q_rope, q_pos,
+    w_uk) in one call (one launch for bf16); returns q_cat [B, H, d_c + d_r].  The
+    cache is a LatentCache or a PagedLatentCache."""
+    _dev_tensor(q_nope, "q_nope", cache.dtype)
+    B, H, d_k = q_nope.shape
+    _dev_tensor(w_uk, "w_uk", cache.dtype)
+    if tuple(w_uk.shape) != (H, d_k, cache.d_c):
+        raise ValueError("w_uk must be [H, d_k, d_c]")
+    if cache.d_r > 0:
+        _dev_tensor(q_rope, "q_rope", cache.dtype)
+        _dev_tensor(k_r, "k_r", cache.dtype)
+    _dev_tensor(q_pos, "q_pos", torch.int32)
+    _dev_tensor(c_kv, "c_kv", cache.dtype)
+    _dev_tensor(seq_idx, "seq_idx", torch.int32)
+    _dev_tensor(pos, "pos", torch.int32)
+    T = seq_idx.numel()
+    if pos.numel() != T or c_kv.numel() != T * cache.d_c:
+        raise ValueError("c_kv, seq_idx and pos need one row / entry per appended token")
+    R = cache.d_c + cache.d_r
+    if out is None:
+        out = torch.empty((B, H, R), dtype=cache.dtype, device=q_nope.device)
+    _out_tensor(out, "out", (B, H, R), cache.dtype)
+    st = cache.struct()
+    paged = isinstance(cache, PagedLatentCache)
+    fn, name = ((lib().mla_absorb_q_append_paged, "mla_absorb_q_append_paged") if paged
+                else (lib().mla_absorb_q_append, "mla_absorb_q_append"))
+    kr, qr = (k_r, q_rope) if cache.d_r > 0 else (None, None)
+    _check(fn(ctypes.byref(st), _ptr(c_kv), _ptr(kr), _ptr(seq_idx), _ptr(pos), T, _ptr(q_nope), _ptr(qr),
+              _ptr(q_pos), _ptr(w_uk), _ptr(out), B, H, d_k, float(rope_base), _stream(q_nope)), name)
     return out
 
 

@@ -5,6 +5,10 @@
 //   out_up   : o[b][h][d]     = sum_c o_lat[b][h][c] W_UV[h][d][c]
 //              (0539edu.com section 3.1: W_UV applied after attention)
 //
+// The absorb launch can also append the decode step's new cache rows (the work of
+// mla_cache_append, spread over the idle warps of every CTA): the step then has one
+// kernel boundary fewer, and the attention that follows waits for both.
+//
 // Both are computed transposed, D[m][n] = sum_k A_h[m][k] X_h[n][k], with the
 // weight dimension as M (128-row tiles) and the batch as N, so that the weights --
 // the bytes that dominate -- are streamed once through TMA and every MMA is a full
@@ -25,6 +29,20 @@ constexpr int kStagesHG = 8;         // a whole K = 512 in flight
 constexpr int kSmemBudgetHG = 200 * 1024;
 constexpr int kThreadsHG = 128;
 
+// The new rows cache[seq_idx[i]][pos[i]] = [c_kv[i] || RoPE(k_r[i], pos[i])] written
+// by an absorb launch (cache == nullptr: none); the rotation uses the query's table.
+struct AppendArgs {
+  __nv_bfloat16* cache;
+  int32_t B, N_max, d_c, d_r;
+  int64_t row_stride;             // elements
+  const __nv_bfloat16* c_kv;      // [T][d_c], 16-byte rows
+  const __nv_bfloat16* k_r;       // [T][d_r]
+  const int32_t* seq_idx;
+  const int32_t* pos;
+  int32_t T;
+  PageMap pages;
+};
+
 struct GemmArgs {
   int H, M, K;                    // per-head problem: M x K weights, K-long activations
   int nb;                         // batch rows (N) in total
@@ -39,6 +57,7 @@ struct GemmArgs {
   int rope_col;                   // first output column of the rotated part (d_c)
   RopeTable rope;                 // turns per position of each RoPE pair, i < d_r / 2
   int gate;                       // epilogue: out[n][m] *= sigmoid(D[m][n]) instead of storing D
+  AppendArgs app;                 // absorb only
 };
 
 // The query's position part, q_cat[n][h][d_c + 2j, +1] = RoPE(q_rope[n][h][2j, 2j+1],
@@ -89,6 +108,49 @@ __device__ __forceinline__ void rope_rows(const GemmArgs& g, int h, int n0, int 
     const float x0 = __uint_as_float(x << 16), x1 = __uint_as_float(x & 0xFFFF0000u);
     *reinterpret_cast<uint32_t*>(g.out + n * g.out_n_stride + h * g.out_h_stride + g.rope_col + 2 * j) =
         pack_bf16x2(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+  }
+}
+
+// The appended rows, as work items spread over the kRopeThreads idle threads of
+// every CTA of the grid: item k is 16-byte chunk u of row i's latent part
+// (u < d_c / 8, a copy) or RoPE pair u - d_c / 8 of its key part, with
+// (i, u) = (k / U, k % U), U = d_c / 8 + d_r / 2.  A bad sequence, position or page
+// skips the item and is recorded, as mla_cache_append does.
+__device__ __forceinline__ void append_rows(const GemmArgs& g, int cta, int ctas, int t) {
+  const AppendArgs& a = g.app;
+  const int chunks = a.d_c / 8, U = chunks + a.d_r / 2;
+  const long long items = static_cast<long long>(a.T) * U;
+  for (long long k = static_cast<long long>(cta) * kRopeThreads + t; k < items;
+       k += static_cast<long long>(ctas) * kRopeThreads) {
+    const int i = static_cast<int>(k / U), u = static_cast<int>(k - static_cast<long long>(i) * U);
+    const int32_t b = a.seq_idx[i];
+    const int32_t p = a.pos[i];
+    if (b < 0 || b >= a.B || p < 0 || p >= a.N_max) {
+      record_error(MLA_ERR_DEVICE_INDEX, kSiteAppendIndex);
+      continue;
+    }
+    int64_t row = static_cast<int64_t>(b) * a.N_max + p;
+    if (a.pages.table != nullptr) {
+      const int32_t pg = a.pages.table[static_cast<int64_t>(b) * a.pages.max_blocks + p / kPageRows];
+      if (pg < 0 || pg >= a.pages.num_pages) {
+        record_error(MLA_ERR_DEVICE_INDEX, kSitePageIndex);
+        continue;
+      }
+      row = static_cast<int64_t>(pg) * kPageRows + p % kPageRows;
+    }
+    __nv_bfloat16* dst = a.cache + row * a.row_stride;
+    if (u < chunks) {
+      *reinterpret_cast<uint4*>(dst + 8 * u) =
+          *reinterpret_cast<const uint4*>(a.c_kv + static_cast<int64_t>(i) * a.d_c + 8 * u);
+    } else {
+      const int j = u - chunks;
+      float sn, cs;
+      rope_sincos(p, g.rope.u_hi[j], g.rope.u_lo[j], &sn, &cs);
+      const __nv_bfloat16* kr = a.k_r + static_cast<int64_t>(i) * a.d_r + 2 * j;
+      const float x0 = __bfloat162float(kr[0]), x1 = __bfloat162float(kr[1]);
+      dst[a.d_c + 2 * j] = __float2bfloat16_rn(fmaf(x0, cs, -x1 * sn));
+      dst[a.d_c + 2 * j + 1] = __float2bfloat16_rn(fmaf(x0, sn, x1 * cs));
+    }
   }
 }
 
@@ -180,9 +242,12 @@ __global__ void __launch_bounds__(kThreadsHG) head_gemm_kernel(const __grid_cons
       tc_commit_if(leader, bars + 8 * (kStagesHG + st));
     }
     tc_commit_if(leader, bars + 8 * (2 * kStagesHG));
-  } else if (kAMN && g.d_r > 0) {
-    griddep_wait();  // q_cat may still be read by the previous kernel
-    rope_rows(g, h, n0, mt, gridDim.x, threadIdx.x - 64);
+  } else if (kAMN && (g.d_r > 0 || g.app.cache != nullptr)) {
+    griddep_wait();  // q_cat and the cache may still be read by the previous kernel
+    if (g.d_r > 0) rope_rows(g, h, n0, mt, gridDim.x, threadIdx.x - 64);
+    if (g.app.cache != nullptr)
+      append_rows(g, (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x,
+                  gridDim.x * gridDim.y * gridDim.z, threadIdx.x - 64);
   }
   __syncwarp();
 
@@ -336,9 +401,15 @@ bool headgemm_gate_supported(int32_t d_model, int32_t width) { return d_model % 
 
 mla_status launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int32_t* q_pos, const void* w_uk,
                               void* q_cat, int32_t B, int32_t H, int32_t d_k, int32_t d_c, int32_t d_r,
-                              float rope_base, cudaStream_t s) {
+                              float rope_base, cudaStream_t s, const AppendRows* app) {
   using namespace hg;
   GemmArgs g = {};
+  if (app != nullptr) {
+    const mla_cache& c = *app->cache;
+    g.app = {static_cast<__nv_bfloat16*>(c.data), c.B, c.N_max, c.d_c, c.d_r, static_cast<int64_t>(c.row_stride),
+             static_cast<const __nv_bfloat16*>(app->c_kv), static_cast<const __nv_bfloat16*>(app->k_r),
+             app->seq_idx, app->pos, app->T, {app->block_table, app->max_blocks, app->num_pages}};
+  }
   g.H = H;
   g.M = d_c;
   g.K = d_k;

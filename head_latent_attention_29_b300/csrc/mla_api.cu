@@ -156,6 +156,69 @@ MLA_API mla_status mla_absorb_q(const void* q_nope, const void* q_rope, const in
                               as_stream(stream));
 }
 
+namespace {
+
+// mla_absorb_q_append on a (contiguous or paged) cache view
+mla_status absorb_q_append(const mla_cache& c, const void* c_kv, const void* k_r, const int32_t* seq_idx,
+                           const int32_t* pos, int32_t T, const void* q_nope, const void* q_rope,
+                           const int32_t* q_pos, const void* w_uk, void* q_cat, int32_t B, int32_t H, int32_t d_k,
+                           float rope_base, void* stream, const int32_t* block_table, int32_t max_blocks,
+                           int32_t num_pages) {
+  const int32_t d_c = c.d_c, d_r = c.d_r;
+  if (T < 0 || B <= 0 || H <= 0 || d_k <= 0) return MLA_ERR_INVALID_ARG;
+  if (q_nope == nullptr || w_uk == nullptr || q_cat == nullptr || q_pos == nullptr) return MLA_ERR_INVALID_ARG;
+  if (d_r > 0 && q_rope == nullptr) return MLA_ERR_INVALID_ARG;
+  if (T > 0 && (c_kv == nullptr || seq_idx == nullptr || pos == nullptr || (d_r > 0 && k_r == nullptr)))
+    return MLA_ERR_INVALID_ARG;
+  if (!(rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (d_r > 128) return MLA_ERR_UNSUPPORTED;
+  const cudaStream_t s = as_stream(stream);
+  if (c.dtype == MLA_BF16) {
+    // bf16: one tensor-core launch or MLA_ERR_UNSUPPORTED, as mla_absorb_q
+    if (!mla::headgemm_absorb_supported(d_k, d_c, d_r)) return MLA_ERR_UNSUPPORTED;
+    if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q_cat) || (d_r > 0 && !aligned4(q_rope)) ||
+        (T > 0 && !aligned16(c_kv)))
+      return MLA_ERR_INVALID_ARG;
+    const mla::AppendRows app = {&c, c_kv, k_r, seq_idx, pos, T, block_table, max_blocks, num_pages};
+    return mla::launch_absorb_q_tc(q_nope, q_rope, q_pos, w_uk, q_cat, B, H, d_k, d_c, d_r, rope_base, s,
+                                   T > 0 ? &app : nullptr);
+  }
+  // fp32: the CUDA-core append and absorb kernels, one after the other
+  if (static_cast<size_t>(32) * d_k * sizeof(float) > 200 * 1024) return MLA_ERR_UNSUPPORTED;
+  if (T > 0) {
+    const mla_status st =
+        mla::launch_cache_append(c, c_kv, k_r, seq_idx, pos, T, rope_base, s, block_table, max_blocks, num_pages);
+    if (st != MLA_OK) return st;
+  }
+  return mla::launch_absorb_q(q_nope, q_rope, q_pos, w_uk, q_cat, B, H, d_k, d_c, d_r, MLA_F32, rope_base, s);
+}
+
+}  // namespace
+
+MLA_API mla_status mla_absorb_q_append(const mla_cache* cache, const void* c_kv, const void* k_r,
+                                       const int32_t* seq_idx, const int32_t* pos, int32_t T, const void* q_nope,
+                                       const void* q_rope, const int32_t* q_pos, const void* w_uk, void* q_cat,
+                                       int32_t B, int32_t H, int32_t d_k, float rope_base, void* stream) {
+  const OpRange range("mla_absorb_q_append");
+  const mla_status st = check_cache(cache);
+  if (st != MLA_OK) return st;
+  return absorb_q_append(*cache, c_kv, k_r, seq_idx, pos, T, q_nope, q_rope, q_pos, w_uk, q_cat, B, H, d_k,
+                         rope_base, stream, nullptr, 0, 0);
+}
+
+MLA_API mla_status mla_absorb_q_append_paged(const mla_paged_cache* cache, const void* c_kv, const void* k_r,
+                                             const int32_t* seq_idx, const int32_t* pos, int32_t T,
+                                             const void* q_nope, const void* q_rope, const int32_t* q_pos,
+                                             const void* w_uk, void* q_cat, int32_t B, int32_t H, int32_t d_k,
+                                             float rope_base, void* stream) {
+  const OpRange range("mla_absorb_q_append_paged");
+  mla_cache view;
+  const mla_status st = check_paged(cache, &view);
+  if (st != MLA_OK) return st;
+  return absorb_q_append(view, c_kv, k_r, seq_idx, pos, T, q_nope, q_rope, q_pos, w_uk, q_cat, B, H, d_k,
+                         rope_base, stream, cache->block_table, cache->max_blocks, cache->num_pages);
+}
+
 MLA_API size_t mla_decode_workspace_size(int32_t B, int32_t H, int32_t d_c, int32_t dtype) {
   if (B <= 0 || H <= 0 || d_c <= 0) return 0;
   if (dtype == MLA_F32) return 256;  // the fp32 path needs no scratch; a token size keeps the API uniform

@@ -166,9 +166,21 @@ mla_status launch_gate(const void* h, const void* w_g, void* o, int32_t B, int32
                        int32_t dtype, cudaStream_t s);
 bool headgemm_absorb_supported(int32_t d_k, int32_t d_c, int32_t d_r);
 bool headgemm_out_up_supported(int32_t d_c, int32_t d_v);
+// The new cache rows an absorb launch also writes (mla_absorb_q_append): as
+// launch_cache_append's arguments; block_table != nullptr for a paged pool.
+struct AppendRows {
+  const mla_cache* cache;
+  const void* c_kv;
+  const void* k_r;
+  const int32_t* seq_idx;
+  const int32_t* pos;
+  int32_t T;
+  const int32_t* block_table;
+  int32_t max_blocks, num_pages;
+};
 mla_status launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int32_t* q_pos, const void* w_uk,
                               void* q_cat, int32_t B, int32_t H, int32_t d_k, int32_t d_c, int32_t d_r,
-                              float rope_base, cudaStream_t s);
+                              float rope_base, cudaStream_t s, const AppendRows* app = nullptr);
 bool headgemm_gate_supported(int32_t d_model, int32_t width);
 mla_status launch_gate_tc(const void* h, const void* w_g, void* o, int32_t B, int32_t d_model, int32_t width,
                           cudaStream_t s);

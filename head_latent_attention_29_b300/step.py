@@ -1,7 +1,9 @@
 """CUDA-graph runner for one MLA decode step.
 
-A decode step launches five or six short kernels (append, absorb, split-KV
-attention, combine, out-up, optionally the gate).  At ~tens of microseconds per
+A decode step launches four or five short kernels for a bf16 cache (the new
+rows appended by the absorb launch, split-KV attention, combine, out-up,
+optionally the gate; an fp32 cache takes separate append and absorb kernels and
+a one-kernel attention).  At ~tens of microseconds per
 step the host-side launch cost matters, so the step is captured once into a CUDA
 graph over static buffers and replayed.  Every kernel in the graph is a libmla
 kernel; the graph only removes host launch overhead.
@@ -10,8 +12,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (LatentCache, PagedLatentCache, absorb_q, cache_append, cache_append_paged, decode_attn,
-               decode_attn_paged, decode_workspace, gate, out_up)
+from . import LatentCache, PagedLatentCache, absorb_q_append, decode_attn, decode_attn_paged, decode_workspace, gate, \
+    out_up
 
 
 class DecodeStep:
@@ -50,17 +52,19 @@ class DecodeStep:
         self.o_lat = torch.empty((B, H, d_c), dtype=dt, device=dev)
         self.lse = torch.empty((B, H), dtype=torch.float32, device=dev)
         self.o = torch.empty((B, H, d_v), dtype=dt, device=dev)
-        self.kernels_per_step = 5 + (1 if w_g is not None else 0)
+        # bf16: absorb + append, split attention, combine, out-up; fp32: append,
+        # absorb, attention, out-up
+        self.kernels_per_step = 4 + (1 if w_g is not None else 0)
         self.graph = None
         self.stream = stream
 
     def launch(self) -> None:
         """Queue the step's kernels on the current stream (no graph)."""
         d = self.inputs
-        paged = isinstance(self.cache, PagedLatentCache)
-        append, attend = (cache_append_paged, decode_attn_paged) if paged else (cache_append, decode_attn)
-        append(self.cache, d["c_kv"], d.get("k_r"), self.seq_idx, self.pos, self.rope_base)
-        absorb_q(d["q_nope"], d.get("q_rope"), self.pos, self.w_uk, self.rope_base, out=self.q_cat)
+        attend = decode_attn_paged if isinstance(self.cache, PagedLatentCache) else decode_attn
+        # the new rows and the absorbed queries in one call (one launch for bf16)
+        absorb_q_append(self.cache, d["c_kv"], d.get("k_r"), self.seq_idx, self.pos, d["q_nope"], d.get("q_rope"),
+                        self.pos, self.w_uk, self.rope_base, out=self.q_cat)
         attend(self.q_cat, self.cache, self.seq_lens, self.scale, self.ws, self.o_lat, self.lse)
         out_up(self.o_lat, self.w_uv, out=self.o)
         if self.w_g is not None:

@@ -157,6 +157,26 @@ MLA_API mla_status mla_absorb_q(const void* q_nope, const void* q_rope, const in
                                 void* stream);
 
 /*
+ * mla_absorb_q_append -- mla_cache_append of T new rows and mla_absorb_q of B
+ *   queries in one call: q_cat = [q_nope . W_UK || RoPE(q_rope, q_pos)] and
+ *   cache[seq_idx[i]][pos[i]] = [c_kv[i] || RoPE(k_r[i], pos[i])], both with the
+ *   same rope_base (d_c and d_r are the cache's, the dtype the cache's).  The
+ *   results are bit-identical to the two calls.
+ *   bf16: one tensor-core launch (the rows are written by the absorb grid's idle
+ *   warps), so a decode step has one kernel boundary fewer; the limits and
+ *   alignments of mla_absorb_q, plus a 16-byte aligned c_kv (MLA_ERR_INVALID_ARG
+ *   otherwise).  f32: the two CUDA-core kernels, one after the other.
+ *   T == 0 appends nothing.  Bad rows are skipped and recorded as
+ *   mla_cache_append does.  The query rows and the appended rows must not
+ *   overlap in memory.
+ */
+MLA_API mla_status mla_absorb_q_append(const mla_cache* cache, const void* c_kv, const void* k_r,
+                                       const int32_t* seq_idx, const int32_t* pos, int32_t T,
+                                       const void* q_nope, const void* q_rope, const int32_t* q_pos,
+                                       const void* w_uk, void* q_cat, int32_t B, int32_t H, int32_t d_k,
+                                       float rope_base, void* stream);
+
+/*
  * mla_decode_workspace_size -- bytes of device workspace mla_decode_attn needs
  * for B sequences and H heads of width d_c (split-KV partials, the block prefix
  * table and the split plan).  The size depends on the current device's SM count.
@@ -307,6 +327,14 @@ MLA_API mla_status mla_gate(const void* h, const void* w_g, void* o, int32_t B, 
 MLA_API mla_status mla_cache_append_paged(const mla_paged_cache* cache, const void* c_kv, const void* k_r,
                                           const int32_t* seq_idx, const int32_t* pos, int32_t T,
                                           float rope_base, void* stream);
+
+/* mla_absorb_q_append with the rows placed in a paged cache (as
+ * mla_cache_append_paged). */
+MLA_API mla_status mla_absorb_q_append_paged(const mla_paged_cache* cache, const void* c_kv, const void* k_r,
+                                             const int32_t* seq_idx, const int32_t* pos, int32_t T,
+                                             const void* q_nope, const void* q_rope, const int32_t* q_pos,
+                                             const void* w_uk, void* q_cat, int32_t B, int32_t H, int32_t d_k,
+                                             float rope_base, void* stream);
 
 /*
  * mla_decode_attn_paged -- mla_decode_attn over a paged cache (same result, bit

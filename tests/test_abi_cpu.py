@@ -115,6 +115,16 @@ def test_bf16_head_gemms_refuse_what_the_tensor_cores_do_not_take(libmla):
     kvd = libmla.mla_kv_down_append
     assert kvd(ctypes.byref(c), a, a, a, 1e-6, a, a, 4, 200, 1e4, a, 1 << 20, None) == UNSUPPORTED  # d_model % 64
     assert kvd(ctypes.byref(c), odd, a, a, 1e-6, a, a, 4, 256, 1e4, a, 1 << 20, None) == INVALID
+    # the append-and-absorb call: mla_absorb_q's limits, plus a 16-byte aligned c_kv
+    fused = libmla.mla_absorb_q_append
+    assert fused(None, a, a, a, a, 4, a, a, a, a, a, 32, 128, 128, 1e4, None) == INVALID            # no cache
+    assert fused(ctypes.byref(c), a, a, a, a, -1, a, a, a, a, a, 32, 128, 128, 1e4, None) == INVALID  # T < 0
+    assert fused(ctypes.byref(c), a, a, a, a, 4, a, a, a, a, a, 32, 128, 100, 1e4, None) == UNSUPPORTED  # d_k % 64
+    assert fused(ctypes.byref(c), odd, a, a, a, 4, a, a, a, a, a, 32, 128, 128, 1e4, None) == INVALID  # c_kv
+    assert fused(ctypes.byref(c), a, a, a, a, 4, odd, a, a, a, a, 32, 128, 128, 1e4, None) == INVALID  # q_nope
+    assert fused(ctypes.byref(c), a, a, a, a, 4, a, a, a, a, a, 32, 128, 128, 0.0, None) == INVALID    # base
+    c192 = mla._Cache(0x1000, 0, 4, 300, 192, 64, 0, 256)   # d_c % 128 != 0: no tensor-core absorb
+    assert fused(ctypes.byref(c192), a, a, a, a, 4, a, a, a, a, a, 32, 128, 128, 1e4, None) == UNSUPPORTED
 
 
 def test_product_path_fails_loudly_without_the_library(tmp_path, monkeypatch):
