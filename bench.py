@@ -227,6 +227,51 @@ def time_attention(replay, stream, device, launches_per_replay: int = 10):
         "median_us_at_max_clock": at_max, "clocks": ck}}
 
 
+def time_seqpar(wl, k: int, stream, device) -> dict:
+    """Decode sharded by sequence position on this one GPU: shard 0's partial (its
+    share of every sequence's rows, `seqpar.shard_rows`) and the merge of k partials,
+    each timed as the attention op is (ten-launch graphs over the rotating caches).
+    A k-GPU run adds the all-gather of the partials between the two."""
+    import torch
+    from head_latent_attention_29_b300.seqpar import shard_rows
+    mla, B, H = wl.mla, wl.B, wl.H
+    b0, b1 = shard_rows(wl.lens, k, 0)
+    begin, end = torch.from_numpy(b0).to(device), torch.from_numpy(b1).to(device)
+    scale = wl.cfg["scale"]
+    d_c = wl.steps[0].o_lat.shape[-1]
+    o_p = [torch.empty((B, H, d_c), dtype=torch.bfloat16, device=device) for _ in wl.steps]
+    l_p = [torch.empty((B, H), dtype=torch.float32, device=device) for _ in wl.steps]
+    for st, o, l in zip(wl.steps, o_p, l_p):  # eager once: one-time host setup outside capture
+        mla.decode_attn_partial(st.q_cat, st.cache, begin, end, scale, st.ws, out=o, lse=l)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(10):
+            j = i % len(wl.steps)
+            st = wl.steps[j]
+            mla.decode_attn_partial(st.q_cat, st.cache, begin, end, scale, st.ws, out=o_p[j], lse=l_p[j])
+    part = time_attention(g.replay, stream, device)
+    o_parts = torch.stack([o_p[0]] * k)
+    l_parts = torch.stack([l_p[0]] * k)
+    o_m = torch.empty((B, H, d_c), dtype=torch.bfloat16, device=device)
+    l_m = torch.empty((B, H), dtype=torch.float32, device=device)
+    mla.decode_merge(o_parts, l_parts, out=o_m, lse=l_m)
+    torch.cuda.synchronize(device)
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2):
+        for _ in range(10):
+            mla.decode_merge(o_parts, l_parts, out=o_m, lse=l_m)
+    mer = time_attention(g2.replay, stream, device)
+    st, word = mla.get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {st} ({word:#x}) in the sequence-sharded timing")
+    return {"shards": k, "shard_timed": 0, "rows_of_shard": int(np.sum(b1 - b0)),
+            "partial_us": round(part["us"], 3), "merge_us": round(mer["us"], 3),
+            "per_gpu_us_without_collective": round(part["us"] + mer["us"], 3),
+            "collective": (f"all-gather of {k} partials (o bf16 [B,H,{d_c}] + lse fp32 [B,H]) between the "
+                           "partial and the merge: not measured, one GPU per box")}
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     """The largest value of x over all ranks (the slowest replica sets the job's
     time); no collective for a single process."""
@@ -453,6 +498,7 @@ def run_b300(args, rank, world, device):
     # --steps is), each bracketed by events; the median replay gives the time
     attn = time_attention(wl.attn_graph.replay, stream, device)
     attn_us = attn["us"]
+    seqpar = time_seqpar(wl, args.seq_shards, stream, device) if getattr(args, "seq_shards", 0) > 1 else None
 
     # ---- end to end: pinned inputs in, result out, host waits for every step
     n_e2e = max(20, min(args.steps // 10, 2000))
@@ -526,6 +572,9 @@ def run_b300(args, rank, world, device):
         },
         "clocks": clk.summary(),
     }
+    if seqpar is not None:
+        seqpar["unsharded_attn_us"] = round(attn_us, 3)
+        out["seqpar"] = seqpar
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.workload, args.seed, budget_s=args.cpu_seconds)
     return out
@@ -1170,6 +1219,9 @@ def main():
                     help="prefill workloads: the non-absorbed form (K and V rebuilt per head)")
     ap.add_argument("--paged", action="store_true",
                     help="decode workloads: 64-row pages of one pool in shuffled order behind a block table")
+    ap.add_argument("--seq-shards", type=int, default=0,
+                    help="decode workloads: also time one shard's partial and the merge of this many "
+                         "sequence-position shards (one GPU; the collective between them is not timed)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1177,6 +1229,8 @@ def main():
         ap.error("--explicit applies to prefill workloads")
     if args.paged and ("S" in W.WORKLOADS[args.workload] or "T" in W.WORKLOADS[args.workload]):
         ap.error("--paged applies to decode workloads")
+    if args.seq_shards and (args.paged or "S" in W.WORKLOADS[args.workload] or "T" in W.WORKLOADS[args.workload]):
+        ap.error("--seq-shards applies to decode workloads on a contiguous cache")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
