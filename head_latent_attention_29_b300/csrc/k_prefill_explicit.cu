@@ -167,6 +167,8 @@ constexpr int kOffP = kOffV + kVStages * kVBytes;
 constexpr int kOffX = kOffP + kPBytes;         // row maxima / sums exchanged by the two halves: [2][2][128] fp32
 constexpr int kOffBar = kOffX + 2 * 2 * 128 * 4;
 // barriers (8 bytes each)
+// The softmax side arrives once per warp (after __syncwarp) on S-free, the maxima
+// exchange, P-full and query-ready: 8 arrivals per phase instead of 256.
 constexpr int kBarKFull = 0, kBarKEmpty = 2, kBarVFull = 4, kBarVEmpty = 6, kBarSFull = 8, kBarSFree = 10,
               kBarPFull = 12, kBarPvDone = 13, kBarQReady = 14, kBarDrain = 15, kBarX = 16, kNumBars = 18;
 constexpr int kAttnSmem = kOffBar + 8 * kNumBars + 1024;  // + alignment slack
@@ -234,12 +236,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       mbar_init(bar_at(sbase, kBarVFull + i), 1);
       mbar_init(bar_at(sbase, kBarVEmpty + i), 1);
       mbar_init(bar_at(sbase, kBarSFull + i), 1);
-      mbar_init(bar_at(sbase, kBarSFree + i), kSoftmaxThreads);
-      mbar_init(bar_at(sbase, kBarX + i), kSoftmaxThreads);
+      mbar_init(bar_at(sbase, kBarSFree + i), kSoftmaxThreads / 32);
+      mbar_init(bar_at(sbase, kBarX + i), kSoftmaxThreads / 32);
     }
-    mbar_init(bar_at(sbase, kBarPFull), kSoftmaxThreads);
+    mbar_init(bar_at(sbase, kBarPFull), kSoftmaxThreads / 32);
     mbar_init(bar_at(sbase, kBarPvDone), 1);
-    mbar_init(bar_at(sbase, kBarQReady), kSoftmaxThreads);
+    mbar_init(bar_at(sbase, kBarQReady), kSoftmaxThreads / 32);
     mbar_init(bar_at(sbase, kBarDrain), 1);
     s_abort = 0;
     fence_mbar_init();
@@ -373,7 +375,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     } else {
       ok = false;
     }
-    mbar_arrive(bar_at(sbase, kBarQReady));
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar_at(sbase, kBarQReady));
 
     float m_ref = 0.f, l = 0.f;
     for (int j = 0; ok && j < nkt; ++j) {
@@ -387,7 +390,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       tmem_ld64(tmem + lane_off + kColS + sb * kKT + hf * 64, sr);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar_at(sbase, kBarSFree + sb));  // this half of S is in registers
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(bar_at(sbase, kBarSFree + sb));  // this half of S is in registers
       // keys past the row's limit only on the diagonal (causal) or last (non-causal) tile
       if (__any_sync(0xffffffffu, kbase + 63 > limit)) {
 #pragma unroll
@@ -402,7 +406,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
       // both halves' maxima: the same reference on both sides of the row
       xch[(sb * 2 + hf) * kQ + r] = mloc;
-      mbar_arrive(bar_at(sbase, kBarX + sb));
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(bar_at(sbase, kBarX + sb));
       if (!warp_wait(bar_at(sbase, kBarX + sb), (j >> 1) & 1, abort)) {
         ok = false;
         break;
@@ -452,13 +457,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       fence_proxy_async_cta();
       tc_fence_before();
-      mbar_arrive(bar_at(sbase, kBarPFull));
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(bar_at(sbase, kBarPFull));
     }
     // epilogue: the halves' sums added, O / l and the log-sum-exp, rows inside the prompt
     if (ok && nkt > 0 && warp_wait(bar_at(sbase, kBarPvDone), (nkt - 1) & 1, abort)) {
       const int sx = nkt & 1;  // the exchange slot the last tile did not use
       xch[(sx * 2 + hf) * kQ + r] = l;
-      mbar_arrive(bar_at(sbase, kBarX + sx));
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(bar_at(sbase, kBarX + sx));
       if (warp_wait(bar_at(sbase, kBarX + sx), (nkt >> 1) & 1, abort)) {
         const float ltot = l + xch[(sx * 2 + (hf ^ 1)) * kQ + r];
         tc_fence_after();
