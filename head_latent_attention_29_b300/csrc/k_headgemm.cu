@@ -123,6 +123,14 @@ __device__ __forceinline__ void append_rows(const GemmArgs& g, int cta, int ctas
   for (long long k = static_cast<long long>(cta) * kRopeThreads + t; k < items;
        k += static_cast<long long>(ctas) * kRopeThreads) {
     const int i = static_cast<int>(k / U), u = static_cast<int>(k - static_cast<long long>(i) * U);
+    // the item's source data does not depend on where the row goes: its load is issued
+    // together with the slot's, one round trip for both
+    uint4 chunk = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t kpair = 0u;
+    if (u < chunks)
+      chunk = *reinterpret_cast<const uint4*>(a.c_kv + static_cast<int64_t>(i) * a.d_c + 8 * u);
+    else
+      kpair = *reinterpret_cast<const uint32_t*>(a.k_r + static_cast<int64_t>(i) * a.d_r + 2 * (u - chunks));
     const int32_t b = a.seq_idx[i];
     const int32_t p = a.pos[i];
     if (b < 0 || b >= a.B || p < 0 || p >= a.N_max) {
@@ -140,14 +148,12 @@ __device__ __forceinline__ void append_rows(const GemmArgs& g, int cta, int ctas
     }
     __nv_bfloat16* dst = a.cache + row * a.row_stride;
     if (u < chunks) {
-      *reinterpret_cast<uint4*>(dst + 8 * u) =
-          *reinterpret_cast<const uint4*>(a.c_kv + static_cast<int64_t>(i) * a.d_c + 8 * u);
+      *reinterpret_cast<uint4*>(dst + 8 * u) = chunk;
     } else {
       const int j = u - chunks;
       float sn, cs;
       rope_sincos(p, g.rope.u_hi[j], g.rope.u_lo[j], &sn, &cs);
-      const __nv_bfloat16* kr = a.k_r + static_cast<int64_t>(i) * a.d_r + 2 * j;
-      const float x0 = __bfloat162float(kr[0]), x1 = __bfloat162float(kr[1]);
+      const float x0 = __uint_as_float(kpair << 16), x1 = __uint_as_float(kpair & 0xFFFF0000u);
       dst[a.d_c + 2 * j] = __float2bfloat16_rn(fmaf(x0, cs, -x1 * sn));
       dst[a.d_c + 2 * j + 1] = __float2bfloat16_rn(fmaf(x0, sn, x1 * cs));
     }

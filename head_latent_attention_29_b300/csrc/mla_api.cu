@@ -177,7 +177,7 @@ mla_status absorb_q_append(const mla_cache& c, const void* c_kv, const void* k_r
     // bf16: one tensor-core launch or MLA_ERR_UNSUPPORTED, as mla_absorb_q
     if (!mla::headgemm_absorb_supported(d_k, d_c, d_r)) return MLA_ERR_UNSUPPORTED;
     if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q_cat) || (d_r > 0 && !aligned4(q_rope)) ||
-        (T > 0 && !aligned16(c_kv)))
+        (T > 0 && (!aligned16(c_kv) || (d_r > 0 && !aligned4(k_r)))))
       return MLA_ERR_INVALID_ARG;
     const mla::AppendRows app = {&c, c_kv, k_r, seq_idx, pos, T, block_table, max_blocks, num_pages};
     return mla::launch_absorb_q_tc(q_nope, q_rope, q_pos, w_uk, q_cat, B, H, d_k, d_c, d_r, rope_base, s,

@@ -164,8 +164,8 @@ MLA_API mla_status mla_absorb_q(const void* q_nope, const void* q_rope, const in
  *   results are bit-identical to the two calls.
  *   bf16: one tensor-core launch (the rows are written by the absorb grid's idle
  *   warps), so a decode step has one kernel boundary fewer; the limits and
- *   alignments of mla_absorb_q, plus a 16-byte aligned c_kv (MLA_ERR_INVALID_ARG
- *   otherwise).  f32: the two CUDA-core kernels, one after the other.
+ *   alignments of mla_absorb_q, plus a 16-byte aligned c_kv and a 4-byte aligned
+ *   k_r (MLA_ERR_INVALID_ARG otherwise).  f32: the two CUDA-core kernels, one after the other.
  *   T == 0 appends nothing.  Bad rows are skipped and recorded as
  *   mla_cache_append does.  The query rows and the appended rows must not
  *   overlap in memory.

@@ -121,6 +121,8 @@ def test_bf16_head_gemms_refuse_what_the_tensor_cores_do_not_take(libmla):
     assert fused(ctypes.byref(c), a, a, a, a, -1, a, a, a, a, a, 32, 128, 128, 1e4, None) == INVALID  # T < 0
     assert fused(ctypes.byref(c), a, a, a, a, 4, a, a, a, a, a, 32, 128, 100, 1e4, None) == UNSUPPORTED  # d_k % 64
     assert fused(ctypes.byref(c), odd, a, a, a, 4, a, a, a, a, a, 32, 128, 128, 1e4, None) == INVALID  # c_kv
+    assert fused(ctypes.byref(c), a, ctypes.c_void_p(0x10002), a, a, 4, a, a, a, a, a, 32, 128, 128, 1e4,
+                 None) == INVALID                                                                      # k_r
     assert fused(ctypes.byref(c), a, a, a, a, 4, odd, a, a, a, a, 32, 128, 128, 1e4, None) == INVALID  # q_nope
     assert fused(ctypes.byref(c), a, a, a, a, 4, a, a, a, a, a, 32, 128, 128, 0.0, None) == INVALID    # base
     c192 = mla._Cache(0x1000, 0, 4, 300, 192, 64, 0, 256)   # d_c % 128 != 0: no tensor-core absorb
