@@ -45,16 +45,6 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
-// OR-reduction of a predicate over a named barrier.
-__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t nthreads, bool v) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.or.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(out) : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads) : "memory");
-  return out != 0;
-}
-
 // One lane of the (converged) warp: 1 for the elected lane, 0 for the others.
 // Single-thread tcgen05 / TMA instructions are issued by the whole warp with the
 // elected lane as predicate, so that their operands stay warp-uniform; issuing
@@ -80,16 +70,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
-}
-
-// Arrive on the barrier at the same shared-memory offset in cluster CTA `cta`,
-// releasing this thread's prior writes (including remote shared stores) at
-// cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar, uint32_t cta) {
-  asm volatile(
-      "{\n\t.reg .b32 ra;\n\tmapa.shared::cluster.u32 ra, %0, %1;\n\t"
-      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}"
-      :: "r"(bar), "r"(cta) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
@@ -162,44 +142,6 @@ __device__ __forceinline__ void tma_load_2d_if(uint32_t pred, uint32_t dst, cons
       :: "r"(pred), "r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar) : "memory");
 }
 
-// 3-D tiled TMA load into this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];"
-      :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
-}
-
-// Prefetch a 3-D tile into L2 (no shared memory involved).
-__device__ __forceinline__ void tma_prefetch_3d_if(uint32_t pred, const CUtensorMap* map, int x, int y, int z) {
-  asm volatile(
-      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
-      "@q cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%1, {%2, %3, %4}];\n\t}"
-      :: "r"(pred), "l"(map), "r"(x), "r"(y), "r"(z) : "memory");
-}
-
-// Same, with an L2 cache-eviction policy.
-__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                                 int x, int y, int z, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
-      :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy) : "memory");
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
 // ---------------------------------------------------------------- proxies
 // TMA store of a 3-D box from shared memory (bulk-group completion).  Boxes that
 // reach past the tensor's extent are clipped; coordinates must be non-negative.
@@ -221,27 +163,6 @@ __device__ __forceinline__ void fence_proxy_async_cta() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-}
-
-// 16-byte store into the shared memory of cluster CTA `cta` at the offset that
-// `local` has in this CTA.
-__device__ __forceinline__ void st_cluster_v4(uint32_t local, uint32_t cta, uint32_t a, uint32_t b,
-                                              uint32_t c, uint32_t d) {
-  asm volatile(
-      "{\n\t.reg .b32 ra;\n\tmapa.shared::cluster.u32 ra, %0, %1;\n\t"
-      "st.shared::cluster.v4.b32 [ra], {%2, %3, %4, %5};\n\t}"
-      :: "r"(local), "r"(cta), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_f32(uint32_t local, uint32_t cta, float v) {
-  asm volatile(
-      "{\n\t.reg .b32 ra;\n\tmapa.shared::cluster.u32 ra, %0, %1;\n\t"
-      "st.shared::cluster.f32 [ra], %2;\n\t}"
-      :: "r"(local), "r"(cta), "f"(v) : "memory");
-}
-
 // Asynchronous 16-byte store into the shared memory of cluster CTA `cta` (at the
 // offset `local` has in this CTA), completing 16 bytes of transaction count on that
 // CTA's barrier at offset `bar`.  Visibility comes with the barrier phase.
@@ -258,28 +179,6 @@ __device__ __forceinline__ void st_async_v2(uint32_t local, uint32_t bar, uint32
       "{\n\t.reg .b32 ra, rb;\n\tmapa.shared::cluster.u32 ra, %0, %2;\n\tmapa.shared::cluster.u32 rb, %1, %2;\n\t"
       "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [ra], {%3, %4}, [rb];\n\t}"
       :: "r"(local), "r"(bar), "r"(cta), "r"(a), "r"(b) : "memory");
-}
-
-__device__ __forceinline__ void st_async_b32(uint32_t local, uint32_t bar, uint32_t cta, uint32_t v) {
-  asm volatile(
-      "{\n\t.reg .b32 ra, rb;\n\tmapa.shared::cluster.u32 ra, %0, %2;\n\tmapa.shared::cluster.u32 rb, %1, %2;\n\t"
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [ra], %3, [rb];\n\t}"
-      :: "r"(local), "r"(bar), "r"(cta), "r"(v) : "memory");
-}
-
-// Bulk copy (copy engine) of `bytes` from this CTA's shared memory to the same-offset
-// region `dst_local` of cluster CTA `cta`, completing bytes on that CTA's barrier.
-__device__ __forceinline__ void bulk_copy_to_cluster_if(uint32_t pred, uint32_t dst_local, uint32_t src, uint32_t bytes,
-                                                        uint32_t bar_local, uint32_t cta) {
-  asm volatile(
-      "{\n\t.reg .pred q;\n\t.reg .b32 rd, rb;\n\tsetp.ne.b32 q, %0, 0;\n\t"
-      "mapa.shared::cluster.u32 rd, %1, %5;\n\tmapa.shared::cluster.u32 rb, %4, %5;\n\t"
-      "@q cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [rd], [%2], %3, [rb];\n\t}"
-      :: "r"(pred), "r"(dst_local), "r"(src), "r"(bytes), "r"(bar_local), "r"(cta) : "memory");
-}
-
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
 }
 
 // Bulk prefetch of `bytes` (multiple of 16) contiguous bytes into L2; p 16-byte aligned.
@@ -321,32 +220,23 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Arrive (once) on a local mbarrier when all previously issued tcgen05 ops of
-// this thread have completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               :: "r"(bar) : "memory");
-}
-
-// Same, arriving on the barrier at this offset in every cluster CTA of `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               :: "r"(bar), "h"(mask) : "memory");
-}
-
 // Elected-lane forms of commit and MMA (see elect_one).
+// Arrive (once) on a local mbarrier when all previously issued tcgen05 ops of this
+// thread have completed.
 __device__ __forceinline__ void tc_commit_if(uint32_t pred, uint32_t bar) {
   asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
                "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}"
                :: "r"(pred), "r"(bar) : "memory");
 }
 
+// Same, arriving on the barrier at this offset in every cluster CTA of `mask`.
 __device__ __forceinline__ void tc_commit_mc_if(uint32_t pred, uint32_t bar, uint16_t mask) {
   asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
                "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%1], %2;\n\t}"
                :: "r"(pred), "r"(bar), "h"(mask) : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate).
 __device__ __forceinline__ void mma_ts_if(uint32_t pred, uint32_t d, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
   asm volatile(
@@ -355,30 +245,13 @@ __device__ __forceinline__ void mma_ts_if(uint32_t pred, uint32_t d, uint32_t a_
       :: "r"(pred), "r"(d), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16.
 __device__ __forceinline__ void mma_ss_if(uint32_t pred, uint32_t d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 q, %0, 0;\n\tsetp.ne.b32 p, %5, 0;\n\t"
       "@q tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, p;\n\t}"
       :: "r"(pred), "r"(d), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate).
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-      :: "r"(d), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16.
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      :: "r"(d), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
