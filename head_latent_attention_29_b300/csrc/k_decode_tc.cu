@@ -914,8 +914,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 constexpr int kCombineThreads = 256;
 constexpr int kCombinePieces = 2;
 
+// The grouped merge (combine_groups > 1): group g of the combine merges pieces g,
+// g + G, ... of each cut problem into an fp32 partial (its running maximum and sum
+// per head, its unnormalised sum per head and column); merge_groups_kernel merges
+// the G partials.  cutp[y] is the problem the y-th cut is in (-1: none).
+struct GroupArgs {
+  int G;
+  int32_t* cutp;  // [cuts]
+  float* gm;      // [G][cuts][128]
+  float* gl;      // [G][cuts][128]
+  float* ga;      // [G][cuts][128][512]
+  int cuts;
+};
+
+template <bool kGrouped>
 __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, long long P, __nv_bfloat16* s_o,
-                                             const int32_t* bnd) {
+                                             const int32_t* bnd, const GroupArgs& gr, int g, int y) {
   constexpr int kPitch = 40;  // staged row: 32 bf16 columns + 16 bytes of padding
   const int t = threadIdx.x;
   if (p == 0) {
@@ -940,17 +954,20 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
   int p_last = p;                           // the run holding the problem's last block
   while (p_last + 1 < P && bnd[4 * (p_last + 1) + 3] < ce) ++p_last;
   const long long slot_first = 2 * p_first + (bnd[4 * p_first + 3] == cb ? 0 : 1);
+  if (kGrouped && g == 0 && cb32 == 0 && t == 0) gr.cutp[y] = pr;
 
   const int h0 = (t & 63) * 2, c0 = cb32 * 32 + (t >> 6) * 8;
   float acc[8][2];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = 0.f;
   float M[2] = {-INFINITY, -INFINITY}, L[2] = {0.f, 0.f};
-  for (int q0 = p_first; q0 <= p_last; q0 += kCombinePieces) {
+  // this group's pieces: p_first + g, p_first + g + G, ... (all of them when G = 1)
+  const int G = kGrouped ? gr.G : 1;
+  for (int q0 = p_first + (kGrouped ? g : 0); q0 <= p_last; q0 += kCombinePieces * G) {
     float2 m[kCombinePieces], l[kCombinePieces], v[kCombinePieces][8];
 #pragma unroll
     for (int u = 0; u < kCombinePieces; ++u) {
-      const int q = q0 + u;
+      const int q = q0 + u * G;
       if (q <= p_last) {
         const long long slot = q == p_first ? slot_first : 2 * static_cast<long long>(q);
         m[u] = *reinterpret_cast<const float2*>(a.part_m + slot * kM + h0);
@@ -1001,6 +1018,22 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
     M[0] = mn[0];
     M[1] = mn[1];
   }
+  if (kGrouped) {
+    // this group's partial, in the log2 units of the pieces (a group with no piece
+    // leaves M = -inf, L = 0, acc = 0)
+    const long long gi = static_cast<long long>(g) * gr.cuts + y;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float* dst = gr.ga + (gi * kM + h0 + i) * kDC + c0;
+      *reinterpret_cast<float4*>(dst) = make_float4(acc[0][i], acc[1][i], acc[2][i], acc[3][i]);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4][i], acc[5][i], acc[6][i], acc[7][i]);
+    }
+    if (cb32 == 0 && t < 64) {
+      *reinterpret_cast<float2*>(gr.gm + gi * kM + h0) = make_float2(M[0], M[1]);
+      *reinterpret_cast<float2*>(gr.gl + gi * kM + h0) = make_float2(L[0], L[1]);
+    }
+    return;
+  }
   __syncthreads();  // the previous item's tile has been written out
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -1031,7 +1064,8 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
 // Block (x, j) merges columns [32 x, 32 x + 32) of the j-th problem that needs a
 // merge (found from the run table: boundary p cuts a problem and is the first
 // boundary inside it); the last row of blocks writes the problems with no rows.
-__global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(const Args a) {
+template <bool kGrouped>
+__global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(const Args a, const GroupArgs gr) {
   __shared__ __align__(16) __nv_bfloat16 s_o[kM * 40];
   __shared__ int32_t s_bnd[4 * kMaxPairs];
   __shared__ int s_p;
@@ -1043,7 +1077,7 @@ __global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(const Args 
   const int P = a.hdr[1];
   __syncthreads();
   if (blockIdx.y == gridDim.y - 1) {
-    combine_item(a, blockIdx.x, 0, P, s_o, s_bnd);
+    if (blockIdx.z == 0) combine_item<kGrouped>(a, blockIdx.x, 0, P, s_o, s_bnd, gr, 0, 0);
     return;
   }
   // boundary p (1 <= p < P) needs a merge if it cuts a problem that starts in run p - 1
@@ -1063,7 +1097,100 @@ __global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(const Args 
     if (need && rank == static_cast<int>(blockIdx.y)) s_p = p;
   }
   __syncthreads();
-  if (s_p > 0) combine_item(a, blockIdx.x, s_p, P, s_o, s_bnd);
+  // -1 unless this row's item writes its problem (the same thread, later): fewer cuts
+  // than rows leave the rest of the rows without one
+  if (kGrouped && blockIdx.z == 0 && blockIdx.x == 0 && threadIdx.x == 0) gr.cutp[blockIdx.y] = -1;
+  if (s_p > 0) combine_item<kGrouped>(a, blockIdx.x, s_p, P, s_o, s_bnd, gr, blockIdx.z, blockIdx.y);
+}
+
+// The second step of the grouped merge: block (x, y) merges the G partials of
+// columns [32 x, 32 x + 32) of the y-th cut problem, thread t heads 2(t % 64), +1
+// and columns 8(t / 64)..+7 (the combine's item layout), two partials per round.
+__global__ void __launch_bounds__(kCombineThreads) merge_groups_kernel(const Args a, const GroupArgs gr) {
+  __shared__ __align__(16) __nv_bfloat16 s_o[kM * 40];
+  constexpr int kPitch = 40;
+  griddep_launch();
+  griddep_wait();  // the group partials
+  const int y = blockIdx.y, cb32 = blockIdx.x, t = threadIdx.x;
+  const int pr = gr.cutp[y];
+  if (pr < 0) return;
+  const int h0 = (t & 63) * 2, c0 = cb32 * 32 + (t >> 6) * 8;
+  float acc[8][2];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = 0.f;
+  float M[2] = {-INFINITY, -INFINITY}, L[2] = {0.f, 0.f};
+  for (int g0 = 0; g0 < gr.G; g0 += 2) {
+    float2 m[2], l[2];
+    float4 v[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const long long gi = static_cast<long long>(g0 + u) * gr.cuts + y;
+      m[u] = *reinterpret_cast<const float2*>(gr.gm + gi * kM + h0);
+      l[u] = *reinterpret_cast<const float2*>(gr.gl + gi * kM + h0);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float* src = gr.ga + (gi * kM + h0 + i) * kDC + c0;
+        v[u][2 * i] = *reinterpret_cast<const float4*>(src);
+        v[u][2 * i + 1] = *reinterpret_cast<const float4*>(src + 4);
+      }
+    }
+    float mn[2] = {M[0], M[1]};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      mn[0] = fmaxf(mn[0], m[u].x);
+      mn[1] = fmaxf(mn[1], m[u].y);
+    }
+    // a partial with no pieces (M = -inf) weighs 0; so does the start (M = -inf)
+    const float al0 = M[0] == -INFINITY ? 0.f : exp2f(M[0] - mn[0]);
+    const float al1 = M[1] == -INFINITY ? 0.f : exp2f(M[1] - mn[1]);
+    L[0] *= al0;
+    L[1] *= al1;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      acc[j][0] *= al0;
+      acc[j][1] *= al1;
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float w0 = m[u].x == -INFINITY ? 0.f : exp2f(m[u].x - mn[0]);
+      const float w1 = m[u].y == -INFINITY ? 0.f : exp2f(m[u].y - mn[1]);
+      L[0] = fmaf(w0, l[u].x, L[0]);
+      L[1] = fmaf(w1, l[u].y, L[1]);
+      const float x0[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+      const float x1[8] = {v[u][2].x, v[u][2].y, v[u][2].z, v[u][2].w, v[u][3].x, v[u][3].y, v[u][3].z, v[u][3].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc[j][0] = fmaf(w0, x0[j], acc[j][0]);
+        acc[j][1] = fmaf(w1, x1[j], acc[j][1]);
+      }
+    }
+    M[0] = mn[0];
+    M[1] = mn[1];
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float inv = 1.f / L[i];
+    uint4 pk;
+    pk.x = pack_bf16x2(acc[0][i] * inv, acc[1][i] * inv);
+    pk.y = pack_bf16x2(acc[2][i] * inv, acc[3][i] * inv);
+    pk.z = pack_bf16x2(acc[4][i] * inv, acc[5][i] * inv);
+    pk.w = pack_bf16x2(acc[6][i] * inv, acc[7][i] * inv);
+    *reinterpret_cast<uint4*>(s_o + (h0 + i) * kPitch + (t >> 6) * 8) = pk;
+  }
+  if (a.lse != nullptr && cb32 == 0 && t < 64) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      if (h0 + i < a.H)
+        a.lse[static_cast<long long>(pr) * a.H + h0 + i] = (M[i] + log2f(L[i])) * 0.69314718055994531f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int id = k * kCombineThreads + t, row = id >> 2, q = id & 3;
+    if (row < a.H)
+      *reinterpret_cast<uint4*>(a.o_lat + (static_cast<long long>(pr) * a.H + row) * kDC + cb32 * 32 + q * 8) =
+          *reinterpret_cast<const uint4*>(s_o + row * kPitch + q * 8);
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -1087,8 +1214,25 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Pieces of one cut problem are merged by G groups of blocks (every G-th piece each)
+// and a second kernel merges the G partials, when few problems share many runs (a
+// long single sequence is cut into as many pieces as there are runs, and one block
+// per 32 columns would merge them two at a time, one L2 round trip per pair).  G
+// from the pieces a problem can expect, e = runs / problems: 1 below 16 pieces
+// (the merge then costs less than the second launch), else a power of two near e / 8.
+constexpr int kMaxGroups = 16;
+__host__ __device__ constexpr int combine_groups(long long np, int npairs) {
+  const long long e = np > 0 ? (npairs + np - 1) / np : 1;
+  if (e < 16) return 1;
+  int g = 1;
+  while (2 * g <= e / 8 && 2 * g <= kMaxGroups) g *= 2;
+  return g;
+}
+
 struct WsLayout {
-  size_t hdr, bnd, cum, m, l, s, o, total;
+  size_t hdr, bnd, cum, m, l, s, o;
+  size_t cutp, gm, gl, ga;  // grouped merge (combine_groups > 1): cut problems, group partials
+  size_t total;
 };
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -1106,7 +1250,17 @@ constexpr WsLayout ws_layout(long long np) {
   w.l = w.m + align256(sizeof(float) * slots * kM);
   w.s = w.l + align256(sizeof(float) * slots * kM);
   w.o = w.s + align256(sizeof(float) * slots * kChunksPerRow * kM);
-  w.total = w.o + 2 * slots * kM * kDC;  // fp16
+  const size_t end = w.o + align256(2 * slots * kM * kDC);  // fp16
+  // the grouped merge of problems cut into many pieces (sized for the most runs a
+  // launch can have)
+  const long long g = combine_groups(np, kMaxPairs);
+  const long long ncut = np < kMaxPairs ? np : kMaxPairs;
+  const size_t gp = g > 1 ? static_cast<size_t>(g * ncut) : 0;
+  w.cutp = end;
+  w.gm = w.cutp + (g > 1 ? align256(sizeof(int32_t) * static_cast<size_t>(ncut)) : 0);
+  w.gl = w.gm + align256(sizeof(float) * gp * kM);
+  w.ga = w.gl + align256(sizeof(float) * gp * kM);
+  w.total = w.ga + sizeof(float) * gp * kM * kDC;
   return w;
 }
 
@@ -1258,7 +1412,23 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
   // at most min(runs - 1, problems) problems need a merge; one more row for empty problems
   const long long ncut = np < npairs - 1 ? np : npairs - 1;
   const unsigned rows = static_cast<unsigned>(ncut > 0 ? ncut : 0) + 1u;
-  return cuda_status(launch_pdl(combine_kernel, dim3(kDC / 32, rows), dim3(kCombineThreads), 0, s, a));
+  GroupArgs gr = {};
+  gr.G = combine_groups(np, npairs);
+  gr.cuts = static_cast<int>(rows - 1);
+  if (gr.G > 1) {
+    gr.cutp = reinterpret_cast<int32_t*>(wsb + w.cutp);
+    gr.gm = reinterpret_cast<float*>(wsb + w.gm);
+    gr.gl = reinterpret_cast<float*>(wsb + w.gl);
+    gr.ga = reinterpret_cast<float*>(wsb + w.ga);
+  }
+  if (gr.G == 1)
+    return cuda_status(launch_pdl(combine_kernel<false>, dim3(kDC / 32, rows), dim3(kCombineThreads), 0, s, a, gr));
+  if (launch_pdl(combine_kernel<true>, dim3(kDC / 32, rows, gr.G), dim3(kCombineThreads), 0, s, a, gr) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (rows > 1)
+    return cuda_status(launch_pdl(merge_groups_kernel, dim3(kDC / 32, rows - 1), dim3(kCombineThreads), 0, s, a, gr));
+  return MLA_OK;
 }
 
 mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,

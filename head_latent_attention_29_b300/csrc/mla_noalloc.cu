@@ -9,8 +9,9 @@
 // the library image itself (a file-scope device array), so the call allocates
 // nothing.
 //
-// The buffer holds the workspace of a batch of up to kNoAllocMaxBatch sequences
-// (about 22 MB).  Every GPU that loads the library keeps it until the process
+// The buffer holds the workspace of any batch of up to kNoAllocMaxBatch sequences
+// (about 25 MB: batches of a few long sequences add the partials of the grouped
+// merge).  Every GPU that loads the library keeps it until the process
 // exits.  All calls on a device share it, so calls whose kernels could overlap on
 // the GPU (different streams without ordering between them) race on it.  The
 // kernels overwrite every scratch word they later read (run table, partial
@@ -22,7 +23,17 @@
 namespace mla {
 
 constexpr int kNoAllocMaxBatch = 32;
-constexpr size_t kNoAllocScratchBytes = dtc::ws_layout(kNoAllocMaxBatch).total;
+// the largest workspace of any batch up to kNoAllocMaxBatch (small batches add the
+// partials of the grouped merge)
+constexpr size_t noalloc_scratch_bytes() {
+  size_t m = 0;
+  for (int b = 1; b <= kNoAllocMaxBatch; ++b) {
+    const size_t t = dtc::ws_layout(b).total;
+    if (t > m) m = t;
+  }
+  return m;
+}
+constexpr size_t kNoAllocScratchBytes = noalloc_scratch_bytes();
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

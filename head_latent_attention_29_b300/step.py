@@ -53,7 +53,9 @@ class DecodeStep:
         self.lse = torch.empty((B, H), dtype=torch.float32, device=dev)
         self.o = torch.empty((B, H, d_v), dtype=dt, device=dev)
         # bf16: absorb + append, split attention, combine, out-up; fp32: append,
-        # absorb, attention, out-up
+        # absorb, attention, out-up (a bf16 batch of at most four sequences adds the
+        # grouped merge's second kernel when each sequence is cut into 16 or more
+        # pieces; not counted here)
         self.kernels_per_step = 4 + (1 if w_g is not None else 0)
         self.graph = None
         self.stream = stream

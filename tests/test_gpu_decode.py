@@ -254,3 +254,16 @@ def test_out_up_batch_shapes(mla, B):
     o = mla.out_up(to_device(o_lat, "bf16"), to_device(w_uv, "bf16"))
     ref = O.out_up(W.widen(o_lat, "bf16"), W.widen(w_uv, "bf16"))
     check_bf16(o.float().cpu().numpy(), ref, f"o B={B}")
+
+
+# ---------------------------------------------------------------------------
+# A few long sequences: each is cut into many pieces (as many as there are runs
+# for a single sequence), which the combine merges in groups and a second kernel
+# merges across groups; every sequence against the oracle
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("lens", [[20000], [30000, 100], [9000, 12000, 64, 7000], [16384] * 5, [65536]])
+def test_decode_few_long_sequences_grouped_merge(mla, lens):
+    o, lse, ro, rlse = _decode_direct(mla, lens, H=128, d_r=64, seed=50 + len(lens))
+    for b in range(len(lens)):
+        check_bf16(o[b], ro[b], f"few long sequences b={b} n={lens[b]}")
+    np.testing.assert_allclose(lse, rlse, atol=2e-2, rtol=1e-3)
