@@ -904,15 +904,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 // L = sum l_s 2^(m_s - M), o = sum 2^(m_s - M) O_s / L, lse = (M + log2 L) ln 2.
 // Work item (x, p) is latent columns [32 x, 32 x + 32) of the problem that run
 // boundary p cuts, if p is the first boundary inside it; items (x, 0) write the zero
-// output of problems with no rows.  One block per item.  Thread t
-// owns heads 2(t % 64), +1 and columns 8(t / 64)..+7: a warp reads 256 contiguous
-// bytes per column of a piece, and up to kCombinePieces pieces are in flight at once
-// (their maximum first, then one weighted sum).  The merged tile is staged in shared
-// memory ([head][column], padded rows) and written out as 64-byte runs.  Two pieces
-// per round keep a thread at 64 registers, so four blocks fit on an SM and a B = 32
-// launch's ~530 blocks run in one wave.
-constexpr int kCombineThreads = 256;
-constexpr int kCombinePieces = 2;
+// output of problems with no rows.  One block per item.  Thread t owns heads
+// 2(t % 64), +1 and kCols columns from kCols (t / 64): a warp reads 256 contiguous
+// bytes per column of a piece, and up to kPieces pieces are in flight at once (their
+// maximum first, then one weighted sum).  The merged tile is staged in shared memory
+// ([head][column], padded rows) and written out as 64-byte runs.  Two shapes of
+// item, both at 64 registers a thread: the narrow one (256 threads of 8 columns, two
+// pieces per round) fits four blocks on an SM, so a B = 32 launch's ~530 items run
+// in one wave; the wide one (512 threads of 4 columns, three pieces per round: a
+// problem spans two to four runs, so mostly one round) fits two, and is taken when
+// the launch's items fit in one wave of it.
+template <bool kWide>
+struct CombineShape {
+  static constexpr int kThreads = kWide ? 512 : 256;
+  static constexpr int kPieces = kWide ? 3 : 2;
+  static constexpr int kCols = kWide ? 4 : 8;
+  static constexpr int kBlocksPerSm = kWide ? 2 : 4;
+};
+constexpr int kMergeThreads = 256;
 
 // The grouped merge (combine_groups > 1): group g of the combine merges pieces g,
 // g + G, ... of each cut problem into an fp32 partial (its running maximum and sum
@@ -927,14 +936,14 @@ struct GroupArgs {
   int cuts;
 };
 
-template <bool kGrouped>
+template <bool kGrouped, bool kWide>
 __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, long long P, __nv_bfloat16* s_o,
                                              const int32_t* bnd, const GroupArgs& gr, int g, int y) {
   constexpr int kPitch = 40;  // staged row: 32 bf16 columns + 16 bytes of padding
   const int t = threadIdx.x;
   if (p == 0) {
     if (a.hdr[2] == 0) return;
-    for (int pr = t; pr < a.NP; pr += kCombineThreads) {
+    for (int pr = t; pr < a.NP; pr += CombineShape<kWide>::kThreads) {
       if (a.cum[pr] != a.cum[pr + 1]) continue;
       for (int h = 0; h < a.H; ++h) {
         uint4* dst = reinterpret_cast<uint4*>(a.o_lat + (static_cast<long long>(pr) * a.H + h) * kDC + cb32 * 32);
@@ -956,43 +965,40 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
   const long long slot_first = 2 * p_first + (bnd[4 * p_first + 3] == cb ? 0 : 1);
   if (kGrouped && g == 0 && cb32 == 0 && t == 0) gr.cutp[y] = pr;
 
-  const int h0 = (t & 63) * 2, c0 = cb32 * 32 + (t >> 6) * 8;
-  float acc[8][2];
+  constexpr int kThreads = CombineShape<kWide>::kThreads, kPieces = CombineShape<kWide>::kPieces,
+                kCols = CombineShape<kWide>::kCols;
+  const int h0 = (t & 63) * 2, c0 = cb32 * 32 + (t >> 6) * kCols;
+  float acc[kCols][2];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = 0.f;
+  for (int j = 0; j < kCols; ++j) acc[j][0] = acc[j][1] = 0.f;
   float M[2] = {-INFINITY, -INFINITY}, L[2] = {0.f, 0.f};
   // this group's pieces: p_first + g, p_first + g + G, ... (all of them when G = 1)
   const int G = kGrouped ? gr.G : 1;
-  for (int q0 = p_first + (kGrouped ? g : 0); q0 <= p_last; q0 += kCombinePieces * G) {
-    float2 m[kCombinePieces], l[kCombinePieces], v[kCombinePieces][8];
+  for (int q0 = p_first + (kGrouped ? g : 0); q0 <= p_last; q0 += kPieces * G) {
+    float2 m[kPieces], l[kPieces], sc[kPieces];
+    uint2 w[kPieces][kCols / 2];  // column pair jp: heads h0, h0 + 1, two fp16 each
 #pragma unroll
-    for (int u = 0; u < kCombinePieces; ++u) {
+    for (int u = 0; u < kPieces; ++u) {
       const int q = q0 + u * G;
       if (q <= p_last) {
         const long long slot = q == p_first ? slot_first : 2 * static_cast<long long>(q);
         m[u] = *reinterpret_cast<const float2*>(a.part_m + slot * kM + h0);
         l[u] = *reinterpret_cast<const float2*>(a.part_l + slot * kM + h0);
-        const float2 sc = *reinterpret_cast<const float2*>(a.part_s + (slot * kChunksPerRow + cb32) * kM + h0);
+        sc[u] = *reinterpret_cast<const float2*>(a.part_s + (slot * kChunksPerRow + cb32) * kM + h0);
         // [pair][head][2]: heads h0, h0 + 1 of column pair cp are 4 consecutive halves
         const __half* src = a.part_o + (slot * (kDC / 2 * kM) + static_cast<long long>(c0 / 2) * kM + h0) * 2;
 #pragma unroll
-        for (int jp = 0; jp < 4; ++jp) {
-          const uint2 w = *reinterpret_cast<const uint2*>(src + jp * kM * 2);
-          const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));  // head h0: columns 2jp, 2jp+1
-          const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));  // head h0+1
-          v[u][2 * jp] = make_float2(a0.x * sc.x, a1.x * sc.y);
-          v[u][2 * jp + 1] = make_float2(a0.y * sc.x, a1.y * sc.y);
-        }
+        for (int jp = 0; jp < kCols / 2; ++jp) w[u][jp] = *reinterpret_cast<const uint2*>(src + jp * kM * 2);
       } else {
         m[u] = make_float2(-INFINITY, -INFINITY);
-        l[u] = make_float2(0.f, 0.f);
+        l[u] = sc[u] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[u][j] = make_float2(0.f, 0.f);
+        for (int jp = 0; jp < kCols / 2; ++jp) w[u][jp] = make_uint2(0u, 0u);
       }
     }
     float mn[2] = {M[0], M[1]};
 #pragma unroll
-    for (int u = 0; u < kCombinePieces; ++u) {
+    for (int u = 0; u < kPieces; ++u) {
       mn[0] = fmaxf(mn[0], m[u].x);
       mn[1] = fmaxf(mn[1], m[u].y);
     }
@@ -1000,19 +1006,24 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
     L[0] *= al0;
     L[1] *= al1;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kCols; ++j) {
       acc[j][0] *= al0;
       acc[j][1] *= al1;
     }
 #pragma unroll
-    for (int u = 0; u < kCombinePieces; ++u) {
+    for (int u = 0; u < kPieces; ++u) {
       const float w0 = exp2f(m[u].x - mn[0]), w1 = exp2f(m[u].y - mn[1]);  // 0 for absent pieces
       L[0] = fmaf(w0, l[u].x, L[0]);
       L[1] = fmaf(w1, l[u].y, L[1]);
+      const float s0 = w0 * sc[u].x, s1 = w1 * sc[u].y;  // the piece's 32-column scale folded in
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        acc[j][0] = fmaf(w0, v[u][j].x, acc[j][0]);
-        acc[j][1] = fmaf(w1, v[u][j].y, acc[j][1]);
+      for (int jp = 0; jp < kCols / 2; ++jp) {
+        const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&w[u][jp].x));  // head h0
+        const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&w[u][jp].y));  // head h0 + 1
+        acc[2 * jp][0] = fmaf(s0, a0.x, acc[2 * jp][0]);
+        acc[2 * jp + 1][0] = fmaf(s0, a0.y, acc[2 * jp + 1][0]);
+        acc[2 * jp][1] = fmaf(s1, a1.x, acc[2 * jp][1]);
+        acc[2 * jp + 1][1] = fmaf(s1, a1.y, acc[2 * jp + 1][1]);
       }
     }
     M[0] = mn[0];
@@ -1025,8 +1036,9 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       float* dst = gr.ga + (gi * kM + h0 + i) * kDC + c0;
-      *reinterpret_cast<float4*>(dst) = make_float4(acc[0][i], acc[1][i], acc[2][i], acc[3][i]);
-      *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4][i], acc[5][i], acc[6][i], acc[7][i]);
+#pragma unroll
+      for (int j = 0; j < kCols; j += 4)
+        *reinterpret_cast<float4*>(dst + j) = make_float4(acc[j][i], acc[j + 1][i], acc[j + 2][i], acc[j + 3][i]);
     }
     if (cb32 == 0 && t < 64) {
       *reinterpret_cast<float2*>(gr.gm + gi * kM + h0) = make_float2(M[0], M[1]);
@@ -1038,12 +1050,14 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const float inv = 1.f / L[i];
-    uint4 pk;
-    pk.x = pack_bf16x2(acc[0][i] * inv, acc[1][i] * inv);
-    pk.y = pack_bf16x2(acc[2][i] * inv, acc[3][i] * inv);
-    pk.z = pack_bf16x2(acc[4][i] * inv, acc[5][i] * inv);
-    pk.w = pack_bf16x2(acc[6][i] * inv, acc[7][i] * inv);
-    *reinterpret_cast<uint4*>(s_o + (h0 + i) * kPitch + (t >> 6) * 8) = pk;
+    uint32_t pk[kCols / 2];
+#pragma unroll
+    for (int j = 0; j < kCols / 2; ++j) pk[j] = pack_bf16x2(acc[2 * j][i] * inv, acc[2 * j + 1][i] * inv);
+    __nv_bfloat16* dst = s_o + (h0 + i) * kPitch + (t >> 6) * kCols;
+    if constexpr (kCols == 8)
+      *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    else
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
   }
   if (a.lse != nullptr && cb32 == 0 && t < 64) {
 #pragma unroll
@@ -1053,8 +1067,8 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
   }
   __syncthreads();
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int id = k * kCombineThreads + t, row = id >> 2, q = id & 3;
+  for (int k = 0; k < kM * 4 / kThreads; ++k) {
+    const int id = k * kThreads + t, row = id >> 2, q = id & 3;
     if (row < a.H)
       *reinterpret_cast<uint4*>(a.o_lat + (static_cast<long long>(pr) * a.H + row) * kDC + cb32 * 32 + q * 8) =
           *reinterpret_cast<const uint4*>(s_o + row * kPitch + q * 8);
@@ -1064,20 +1078,21 @@ __device__ __forceinline__ void combine_item(const Args& a, int cb32, int p, lon
 // Block (x, j) merges columns [32 x, 32 x + 32) of the j-th problem that needs a
 // merge (found from the run table: boundary p cuts a problem and is the first
 // boundary inside it); the last row of blocks writes the problems with no rows.
-template <bool kGrouped>
-__global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(const Args a, const GroupArgs gr) {
+template <bool kGrouped, bool kWide>
+__global__ void __launch_bounds__(CombineShape<kWide>::kThreads, CombineShape<kWide>::kBlocksPerSm)
+    combine_kernel(const Args a, const GroupArgs gr) {
   __shared__ __align__(16) __nv_bfloat16 s_o[kM * 40];
   __shared__ int32_t s_bnd[4 * kMaxPairs];
   __shared__ int s_p;
   griddep_launch();
   griddep_wait();  // the pieces of the split kernel
   // the run table in one round of loads (entries past the run count are not used)
-  for (int i = threadIdx.x; i < 4 * kMaxPairs; i += kCombineThreads) s_bnd[i] = a.bnd[i];
+  for (int i = threadIdx.x; i < 4 * kMaxPairs; i += CombineShape<kWide>::kThreads) s_bnd[i] = a.bnd[i];
   if (threadIdx.x == 0) s_p = 0;
   const int P = a.hdr[1];
   __syncthreads();
   if (blockIdx.y == gridDim.y - 1) {
-    if (blockIdx.z == 0) combine_item<kGrouped>(a, blockIdx.x, 0, P, s_o, s_bnd, gr, 0, 0);
+    if (blockIdx.z == 0) combine_item<kGrouped, kWide>(a, blockIdx.x, 0, P, s_o, s_bnd, gr, 0, 0);
     return;
   }
   // boundary p (1 <= p < P) needs a merge if it cuts a problem that starts in run p - 1
@@ -1100,13 +1115,13 @@ __global__ void __launch_bounds__(kCombineThreads, 4) combine_kernel(const Args 
   // -1 unless this row's item writes its problem (the same thread, later): fewer cuts
   // than rows leave the rest of the rows without one
   if (kGrouped && blockIdx.z == 0 && blockIdx.x == 0 && threadIdx.x == 0) gr.cutp[blockIdx.y] = -1;
-  if (s_p > 0) combine_item<kGrouped>(a, blockIdx.x, s_p, P, s_o, s_bnd, gr, blockIdx.z, blockIdx.y);
+  if (s_p > 0) combine_item<kGrouped, kWide>(a, blockIdx.x, s_p, P, s_o, s_bnd, gr, blockIdx.z, blockIdx.y);
 }
 
 // The second step of the grouped merge: block (x, y) merges the G partials of
 // columns [32 x, 32 x + 32) of the y-th cut problem, thread t heads 2(t % 64), +1
-// and columns 8(t / 64)..+7 (the combine's item layout), two partials per round.
-__global__ void __launch_bounds__(kCombineThreads) merge_groups_kernel(const Args a, const GroupArgs gr) {
+// and columns 8(t / 64)..+7, two partials per round.
+__global__ void __launch_bounds__(kMergeThreads) merge_groups_kernel(const Args a, const GroupArgs gr) {
   __shared__ __align__(16) __nv_bfloat16 s_o[kM * 40];
   constexpr int kPitch = 40;
   griddep_launch();
@@ -1186,7 +1201,7 @@ __global__ void __launch_bounds__(kCombineThreads) merge_groups_kernel(const Arg
   __syncthreads();
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
-    const int id = k * kCombineThreads + t, row = id >> 2, q = id & 3;
+    const int id = k * kMergeThreads + t, row = id >> 2, q = id & 3;
     if (row < a.H)
       *reinterpret_cast<uint4*>(a.o_lat + (static_cast<long long>(pr) * a.H + row) * kDC + cb32 * 32 + q * 8) =
           *reinterpret_cast<const uint4*>(s_o + row * kPitch + q * 8);
@@ -1217,7 +1232,7 @@ static EncodeTiledFn encode_fn() {
 // Pieces of one cut problem are merged by G groups of blocks (every G-th piece each)
 // and a second kernel merges the G partials, when few problems share many runs (a
 // long single sequence is cut into as many pieces as there are runs, and one block
-// per 32 columns would merge them two at a time, one L2 round trip per pair).  G
+// per 32 columns would merge them a few at a time, one L2 round trip per round).  G
 // from the pieces a problem can expect, e = runs / problems: 1 below 16 pieces
 // (the merge then costs less than the second launch), else a power of two near e / 8.
 constexpr int kMaxGroups = 16;
@@ -1421,14 +1436,19 @@ static mla_status launch_attn_tc(const void* q_cat, const mla_cache& c, const dt
     gr.gl = reinterpret_cast<float*>(wsb + w.gl);
     gr.ga = reinterpret_cast<float*>(wsb + w.ga);
   }
+  // the wide item shape when the launch's items fit in one wave of it (two blocks an
+  // SM, about two SMs a cluster)
+  const dim3 grid(kDC / 32, rows, static_cast<unsigned>(gr.G));
+  const bool wide = static_cast<long long>(grid.x) * grid.y * grid.z <= 2LL * 2 * npairs;
+  cudaError_t err;
   if (gr.G == 1)
-    return cuda_status(launch_pdl(combine_kernel<false>, dim3(kDC / 32, rows), dim3(kCombineThreads), 0, s, a, gr));
-  if (launch_pdl(combine_kernel<true>, dim3(kDC / 32, rows, gr.G), dim3(kCombineThreads), 0, s, a, gr) !=
-      cudaSuccess)
-    return MLA_ERR_CUDA;
-  if (rows > 1)
-    return cuda_status(launch_pdl(merge_groups_kernel, dim3(kDC / 32, rows - 1), dim3(kCombineThreads), 0, s, a, gr));
-  return MLA_OK;
+    err = wide ? launch_pdl(combine_kernel<false, true>, grid, dim3(CombineShape<true>::kThreads), 0, s, a, gr)
+             : launch_pdl(combine_kernel<false, false>, grid, dim3(CombineShape<false>::kThreads), 0, s, a, gr);
+  else
+    err = wide ? launch_pdl(combine_kernel<true, true>, grid, dim3(CombineShape<true>::kThreads), 0, s, a, gr)
+             : launch_pdl(combine_kernel<true, false>, grid, dim3(CombineShape<false>::kThreads), 0, s, a, gr);
+  if (err != cudaSuccess || gr.G == 1 || rows == 1) return cuda_status(err);
+  return cuda_status(launch_pdl(merge_groups_kernel, dim3(kDC / 32, rows - 1), dim3(kMergeThreads), 0, s, a, gr));
 }
 
 mla_status launch_decode_tc(const void* q_cat, const mla_cache& c, const int32_t* seq_lens, int32_t H,
