@@ -74,6 +74,8 @@ def _paged_and_contiguous(mla, lens, H, d_r, seed, spare=3, max_blocks=None):
     ([1000] * 7, 64, 64),
     ([3000, 65, 900], 64, 0),
     ([513, 2], 16, 64),
+    ([24000], 128, 64),           # one long sequence: the grouped merge
+    ([12000, 9000, 70], 128, 64),
 ])
 def test_paged_decode_bit_equal_to_contiguous(mla, lens, H, d_r):
     q_bits, rows, paged, flat, lens = _paged_and_contiguous(mla, lens, H, d_r, seed=len(lens) + H)

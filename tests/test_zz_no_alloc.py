@@ -29,9 +29,12 @@ def mla():
 
 def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(mla):
     scale = 1.0 / math.sqrt(192)
-    # two calls in a row on different batches: the second must not see the first's
-    # scratch (the lengths differ, so the run plans and the cut problems differ)
-    for k, (seed, lens) in enumerate([(31, [4096, 100, 65, 2000, 1]), (32, [777, 3000, 64, 5000] * 8)]):
+    # calls in a row on different batches: none may see another's scratch (the
+    # lengths differ, so the run plans and the cut problems differ); the last two are
+    # a few long sequences, whose pieces go through the grouped merge's partials
+    cases = [(31, [4096, 100, 65, 2000, 1]), (32, [777, 3000, 64, 5000] * 8), (33, [30000]),
+             (34, [20000, 16000, 9000])]
+    for k, (seed, lens) in enumerate(cases):
         lens = np.asarray(lens, dtype=np.int32)
         q_bits, rows = direct_decode_inputs(seed, lens, 128, 512, 64)
         q, cache = upload_direct(mla, q_bits, rows, 512, 64, int(lens.max()))
