@@ -196,7 +196,8 @@ MLA_API size_t mla_decode_workspace_size(int32_t B, int32_t H, int32_t d_c, int3
  *   hotelren.com section 7.3 for the max subtraction.)
  *   The tokens of all sequences are split into equal runs across the GPU; each
  *   run produces an unnormalised partial (m, l, O) and a log-sum-exp combine
- *   merges the runs of each sequence.
+ *   merges the runs of each sequence (in two steps, groups of pieces and then the
+ *   groups, when a batch of a few long sequences is cut into many pieces each).
  *   q_cat     [B, H, d_c + d_r]  dtype = cache->dtype
  *   seq_lens  [B] int32 device; 0 <= seq_lens[b] <= N_max.  A sequence of length 0
  *             gives o_lat = 0 and lse = -inf.  Out-of-range lengths are clamped
@@ -439,7 +440,7 @@ MLA_API mla_status mla_kv_down_append_paged(const mla_paged_cache* cache, const 
  *   whose device memory is fixed when they start, or embedders that only own the
  *   input and output buffers a host framework gives them.  This entry point computes exactly what mla_decode_attn does,
  *   with the same kernels, but takes the split-KV scratch from a buffer built into
- *   the library (about 22 MB per GPU that loads the library, held until the
+ *   the library (about 25 MB per GPU that loads the library, held until the
  *   process exits), so it allocates nothing.
  *   Arguments are those of mla_decode_attn minus the workspace.  Limits: bf16 cache
  *   only (MLA_ERR_UNSUPPORTED otherwise) and at most 32 sequences (cache->B > 32
