@@ -909,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 // bytes per column of a piece, and up to kPieces pieces are in flight at once (their
 // maximum first, then one weighted sum).  The merged tile is staged in shared memory
 // ([head][column], padded rows) and written out as 64-byte runs.  Two shapes of
-// item, both at 64 registers a thread: the narrow one (256 threads of 8 columns, two
+// item, both within 64 registers a thread: the narrow one (256 threads of 8 columns, two
 // pieces per round) fits four blocks on an SM, so a B = 32 launch's ~530 items run
 // in one wave; the wide one (512 threads of 4 columns, three pieces per round: a
 // problem spans two to four runs, so mostly one round) fits two, and is taken when
