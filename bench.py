@@ -849,7 +849,10 @@ class KvDownWorkload:
         self.gamma = up(gamma).to(device)
         seq, pos, B, N = kvdown_rows_slots(cfg)
         self.seq, self.pos = torch.from_numpy(seq).to(device), torch.from_numpy(pos).to(device)
-        seq_l, pos_l = self.seq.long(), self.pos.long()
+        # every device buffer a captured graph touches stays referenced from here: each
+        # capture empties the allocator's cache, so a buffer freed earlier would leave a
+        # graph with a released address
+        self.seq_l, self.pos_l = self.seq.long(), self.pos.long()
         self.cache = mla.LatentCache(B, N, d_c, d_r, dtype=bf, device=device)
         self.ws = mla.kv_down_workspace(T, dm, d_c, d_r, bf, device)
         self.eps, self.base = cfg["eps"], cfg["rope_base"]
@@ -870,15 +873,29 @@ class KvDownWorkload:
             for w in self.ws_list:
                 call(w)
         self.e2e = []
-        # end to end: h in from pinned memory, the written rows back to pinned memory
-        self.rows_dev = torch.empty((T, d_c + d_r), dtype=bf, device=device)
-        for w in self.ws_list[:1]:
+        # end to end: h in from pinned memory, the written rows back to pinned memory;
+        # decode-sized steps get four independent sets of buffers (h, cache, workspace,
+        # rows), so that steps of different sets can be in flight at once
+        self.rows_hosts = [self.rows_host]
+        self.e2e_sets = []  # (h, cache, workspace, rows) of each set, kept alive with its graph
+        n_sets = 4 if T <= 4096 else 1
+        for j in range(n_sets):
+            h_d = self.h if j == 0 else self.h.clone()
+            cache = self.cache if j == 0 else mla.LatentCache(B, N, d_c, d_r, dtype=bf, device=device)
+            ws = self.ws if j == 0 else mla.kv_down_workspace(T, dm, d_c, d_r, bf, device)
+            rows_dev = torch.empty((T, d_c + d_r), dtype=bf, device=device)
+            if j > 0:
+                self.rows_hosts.append(torch.empty((T, d_c + d_r), dtype=bf).pin_memory())
+            w = self.ws_list[j % len(self.ws_list)]
+            self.e2e_sets.append((h_d, cache, ws, rows_dev))
+            mla.kv_down_append(cache, h_d, w, self.gamma, self.seq, self.pos, self.eps, self.base, ws)
+            torch.cuda.synchronize(device)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                self.h.copy_(self.h_host, non_blocking=True)
-                call(w)
-                self.rows_dev.copy_(self.cache.data[seq_l, pos_l, : d_c + d_r])
-                self.rows_host.copy_(self.rows_dev, non_blocking=True)
+                h_d.copy_(self.h_host, non_blocking=True)
+                mla.kv_down_append(cache, h_d, w, self.gamma, self.seq, self.pos, self.eps, self.base, ws)
+                rows_dev.copy_(cache.data[self.seq_l, self.pos_l, : d_c + d_r])
+                self.rows_hosts[j].copy_(rows_dev, non_blocking=True)
             self.e2e.append(g)
 
     def replay(self):
@@ -918,15 +935,41 @@ def run_b300_kvdown(args, rank, world, device):
     value = job_throughput(wl.T, world, ms_step * 1e-3)
 
     n_e2e = max(20, min(steps // 10, 2000)) if wl.T <= 4096 else 5
-    wl.e2e[0].replay()
+    for g in wl.e2e:
+        g.replay()
     torch.cuda.synchronize(device)
+    # one step at a time: the host waits for each step's rows before the next step
     barrier()
     t0 = time.perf_counter()
     for _ in range(n_e2e):
         wl.e2e[0].replay()
         stream.synchronize()
     barrier()
-    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world, device)
+    e2e_serial_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world, device)
+    # one step per buffer set in flight, each set on its own stream (independent
+    # batches of new tokens), the host waiting for each step's rows len(sets) behind
+    e2e_s, in_flight = e2e_serial_s, 1
+    k = len(wl.e2e)
+    if k > 1:
+        streams = [torch.cuda.Stream(device) for _ in range(k)]
+        torch.cuda.synchronize(device)
+        barrier()
+        t0 = time.perf_counter()
+        pending = []
+        for i in range(n_e2e):
+            s = streams[i % k]
+            with torch.cuda.stream(s):
+                wl.e2e[i % k].replay()
+            ev = torch.cuda.Event()
+            ev.record(s)
+            pending.append(ev)
+            if len(pending) == k:
+                pending.pop(0).synchronize()
+        for ev in pending:
+            ev.synchronize()
+        barrier()
+        e2e_s, in_flight = max_over_ranks((time.perf_counter() - t0) / n_e2e, world, device), k
+        torch.cuda.synchronize(device)
 
     hbm, tc_burst, tc_sust, peak_kind = _peaks()
     bytes_alg, flops = kvdown_bytes_flops(cfg)
@@ -949,7 +992,8 @@ def run_b300_kvdown(args, rank, world, device):
                    "step": "kv_down_append (projection on the tensor cores + norm/RoPE/store)"},
         "gpu_launches": wl.kernels_per_step * steps,
         "e2e": {"value": round(wl.T * world / e2e_s, 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": wl.h_host.numel() * 2, "d2h_bytes_per_step": wl.rows_host.numel() * 2},
+                "h2d_bytes_per_step": wl.h_host.numel() * 2, "d2h_bytes_per_step": wl.rows_host.numel() * 2,
+                "steps_in_flight": in_flight, "value_one_step_at_a_time": round(wl.T * world / e2e_serial_s, 1)},
         "roofline": {
             "bound": "tensor" if tensor else "hbm", "kernel": "kv_down_append (projection + finish)",
             "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s" if tensor else "GB/s",
